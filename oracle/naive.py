@@ -1,0 +1,137 @@
+"""O1 — naive materialised attention in numpy fp64.  TEST INFRASTRUCTURE ONLY.
+
+What is computed (the plain definition, applied to inputs widened exactly to fp64):
+
+    S = scale * Q K^T                    [AIE "Das Grundproblem"; JOHE "Введение"]
+    P = softmax(S) over the key axis     (masked entries contribute nothing)
+    O = P V
+    LSE_i = log sum_j exp(S_ij)          (natural log, over the allowed keys)
+
+The pages write the transpose of K as ``K.T`` on 4-D tensors ([AIE]) and as
+``K.transpose(-2, -3)`` in the "Проблема 1" listing of [JOHE]; both are read as
+the transpose of the last two axes, which is what [JOHE]'s benchmark section
+uses.  The causal mask ([ZIMA] "Kernel-Fusion ..." lists masking among the fused
+steps) is aligned bottom-right: query i may see key j iff j <= i + (Nk - Nq).
+For Nq == Nk this is the usual j <= i.  A query that sees no key at all
+(only possible when causal and Nq > Nk) gets O = 0 and LSE = -inf.
+
+Backward (gradient of the forward for an upstream dO; [JOHE] "Стадии
+вычисления", pass 2 recomputes these from the same blocks without storing P —
+here P is simply materialised):
+
+    dV = P^T dO
+    dP = dO V^T
+    dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)        (softmax Jacobian)
+    dQ = scale * dS K
+    dK = scale * dS^T Q
+
+Decode is the forward with a single query against a KV cache, non-causal
+([ZIMA] "Weniger IO bedeutet nicht, dass der KV-Cache entfällt": the cache
+stays, attention streams it).  ``decode_split`` states the split-KV form: each
+contiguous chunk of keys gives a partial (normalised partial output, partial
+LSE) and the partials merge with the same max-shift rule as the online
+recurrence of [AIE] "Lösung: Online Softmax".
+"""
+import numpy as np
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def allowed(Nq, Nk, causal, rows=None):
+    """Boolean [len(rows), Nk]: which keys each query row may attend to.
+
+    ``rows`` are query indices in [0, Nq) (default: all).  Causal alignment is
+    bottom-right (key j visible to query i iff j <= i + Nk - Nq).
+    """
+    rows = np.arange(Nq) if rows is None else np.asarray(rows)
+    cols = np.arange(Nk)
+    if not causal:
+        return np.ones((rows.size, Nk), dtype=bool)
+    return cols[None, :] <= (rows[:, None] + (Nk - Nq))
+
+
+def forward(q, k, v, scale, causal=False, rows=None, Nq=None, return_p=False):
+    """Materialised forward.
+
+    q: [..., R, d] query rows (R = Nq, or the sampled rows when ``rows`` given)
+    k: [..., Nk, d], v: [..., Nk, dv]
+    rows: optional query indices of the R given rows (for the causal mask);
+          Nq: total number of queries (needed with ``rows`` for the causal offset).
+    Returns O [..., R, dv], LSE [..., R] (and P when return_p).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    R, Nk = q.shape[-2], k.shape[-2]
+    if rows is None:
+        Nq = R
+    mask = allowed(Nq, Nk, causal, rows)
+    s = scale * (q @ np.swapaxes(k, -1, -2))
+    s = np.where(mask, s, -np.inf)
+    m = s.max(axis=-1, keepdims=True)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    e = np.exp(s - m_safe)                      # exp(-inf) = 0 for masked keys
+    l = e.sum(axis=-1, keepdims=True)
+    has = l > 0
+    p = np.where(has, e / np.where(has, l, 1.0), 0.0)
+    o = p @ v
+    lse = np.where(has, m_safe + np.log(np.where(has, l, 1.0)), -np.inf)[..., 0]
+    if return_p:
+        return o, lse, p
+    return o, lse
+
+
+def backward(q, k, v, do, scale, causal=False):
+    """Gradients (dQ, dK, dV) of O = softmax(scale Q K^T [masked]) V for upstream dO."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    _, _, p = forward(q, k, v, scale, causal, return_p=True)
+    dv = np.swapaxes(p, -1, -2) @ do
+    dp = do @ np.swapaxes(v, -1, -2)
+    ds = p * (dp - (p * dp).sum(axis=-1, keepdims=True))
+    dq = scale * (ds @ k)
+    dk = scale * (np.swapaxes(ds, -1, -2) @ q)
+    return dq, dk, dv
+
+
+def decode(q, kcache, vcache, scale):
+    """One query per (b, h) against its cache.  q [B,H,d], caches [B,H,Nk,d].
+
+    Returns O [B,H,dv], LSE [B,H]: the forward with Nq = 1, non-causal.
+    """
+    o, lse = forward(_f64(q)[..., None, :], kcache, vcache, scale, causal=False)
+    return o[..., 0, :], lse[..., 0]
+
+
+def split_bounds(Nk, num_splits):
+    """Contiguous key chunks [s*c, min((s+1)*c, Nk)) with c = ceil(Nk / num_splits).
+
+    A chunk past the end is empty; its partial has LSE = -inf and weight 0.
+    """
+    c = -(-Nk // num_splits)
+    return [(min(s * c, Nk), min((s + 1) * c, Nk)) for s in range(num_splits)]
+
+
+def decode_split(q, kcache, vcache, scale, num_splits):
+    """Split-KV decode written out: per-chunk partials, then the LSE merge.
+
+    Partial of chunk s:  lse_s = log sum_{j in s} exp(x_j),  o_s = sum_j exp(x_j - lse_s) v_j
+    Merge:               LSE = M + log sum_s exp(lse_s - M),  M = max_s lse_s
+                         O   = sum_s exp(lse_s - LSE) o_s
+    Returns (O, LSE, partial_o [B,H,S,dv], partial_lse [B,H,S]).
+    """
+    q, kc, vc = _f64(q), _f64(kcache), _f64(vcache)
+    B, H, Nk, _ = kc.shape
+    dv = vc.shape[-1]
+    po = np.zeros((B, H, num_splits, dv))
+    pl = np.full((B, H, num_splits), -np.inf)
+    for s, (a, b) in enumerate(split_bounds(Nk, num_splits)):
+        if b <= a:
+            continue
+        o, l = forward(q[..., None, :], kc[:, :, a:b], vc[:, :, a:b], scale)
+        po[:, :, s] = o[..., 0, :]
+        pl[:, :, s] = l[..., 0]
+    m = pl.max(axis=-1, keepdims=True)
+    w = np.exp(pl - m)
+    lse = m[..., 0] + np.log(w.sum(axis=-1))
+    o = (np.exp(pl - lse[..., None])[..., None] * po).sum(axis=-2)
+    return o, lse, po, pl
