@@ -1,0 +1,213 @@
+"""Exact tiled attention on GB300 (sm_103a) — Python binding of the C ABI.
+
+The functions ``fa_fwd``, ``fa_bwd``, ``fa_decode``, ``fa_bwd_workspace_bytes``,
+``fa_decode_workspace_bytes``, ``fa_get_last_device_error``,
+``fa_set_wait_timeout_ns``, ``fa_status_string`` and ``fa_version`` carry the
+names and arguments of ``include/fa.h`` and only marshal arguments: every step
+of the computation runs in the CUDA kernels of ``libfa_gb300.so``.  PyTorch
+supplies device memory (``data_ptr``) and the stream.  ``forward``,
+``backward`` and ``decode`` are conveniences that allocate the outputs and the
+workspace with torch and then call the same entry points.
+
+There is no fallback: if the shared library is missing, or a call returns an
+error status, a ``FAError`` is raised.
+"""
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "fa.h")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_ALIGNMENT = -3
+FA_ERR_WORKSPACE = -4
+FA_ERR_CUDA = -5
+FA_ERR_TIMEOUT = -6
+
+_lib = None
+
+_NAMES = {FA_OK: "FA_OK", FA_ERR_INVALID_ARG: "FA_ERR_INVALID_ARG",
+          FA_ERR_UNSUPPORTED: "FA_ERR_UNSUPPORTED", FA_ERR_ALIGNMENT: "FA_ERR_ALIGNMENT",
+          FA_ERR_WORKSPACE: "FA_ERR_WORKSPACE", FA_ERR_CUDA: "FA_ERR_CUDA",
+          FA_ERR_TIMEOUT: "FA_ERR_TIMEOUT"}
+
+
+class FAError(RuntimeError):
+    """A C-ABI call returned a status other than FA_OK (or the library is missing)."""
+
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (what, _NAMES.get(status, "?"), status))
+
+
+def build(force=False):
+    """Compile libfa_gb300.so in-tree (nvcc, sm_103a) and return its path."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def load():
+    """Load the shared library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise FAError(FA_ERR_CUDA, "loading %s (not built; call build())" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.fa_bwd_workspace_bytes.restype = sz
+    lib.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp, sz, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.fa_decode_workspace_bytes.restype = sz
+    lib.fa_decode.argtypes = [vp] * 5 + [i, i, i, i, f, i, vp, sz, vp]
+    lib.fa_decode.restype = i
+    lib.fa_get_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+    lib.fa_get_last_device_error.restype = i
+    lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.fa_set_wait_timeout_ns.restype = ctypes.c_uint64
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = i
+    _lib = lib
+    return lib
+
+
+def declared_symbols():
+    """Names of the functions declared in include/fa.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+# ------------------------------------------------------------------ raw entry points
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _raise(status, what):
+    if status != FA_OK:
+        raise FAError(status, what)
+
+
+def fa_status_string(status):
+    try:
+        return load().fa_status_string(int(status)).decode()
+    except FAError:
+        return "status %d" % status
+
+
+def fa_version():
+    return load().fa_version()
+
+
+def fa_set_wait_timeout_ns(ns):
+    return int(load().fa_set_wait_timeout_ns(int(ns)))
+
+
+def fa_get_last_device_error(stream=None):
+    """Synchronise the stream; return (status, [code, site, block, aux]) and clear the word."""
+    detail = (ctypes.c_int * 4)()
+    st = load().fa_get_last_device_error(_stream(stream), detail)
+    return st, list(detail)
+
+
+def fa_bwd_workspace_bytes(B, H, Nq, Nk, d):
+    return int(load().fa_bwd_workspace_bytes(B, H, Nq, Nk, d))
+
+
+def fa_decode_workspace_bytes(B, H, Nk, d, num_splits=0):
+    return int(load().fa_decode_workspace_bytes(B, H, Nk, d, num_splits))
+
+
+def fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream=None):
+    _raise(load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                         float(scale), int(bool(causal)), _stream(stream)), "fa_fwd")
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace,
+           workspace_bytes, stream=None):
+    _raise(load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+                         _ptr(workspace), int(workspace_bytes), _stream(stream)), "fa_bwd")
+
+
+def fa_decode(q, kcache, vcache, o, lse, B, H, Nk, d, scale, num_splits, workspace,
+              workspace_bytes, stream=None):
+    _raise(load().fa_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(o), _ptr(lse), B, H, Nk,
+                            d, float(scale), int(num_splits), _ptr(workspace),
+                            int(workspace_bytes), _stream(stream)), "fa_decode")
+
+
+# ------------------------------------------------------------------ conveniences
+def _check(t, name, shape):
+    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+        raise ValueError("%s must be a contiguous bf16 CUDA tensor" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+def forward(q, k, v, scale=None, causal=False, stream=None):
+    """O, LSE for q [B,H,Nq,d], k/v [B,H,Nk,d] (bf16 CUDA).  LSE is fp32 [B,H,Nq]."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    _check(q, "q", (B, H, Nq, d))
+    _check(k, "k", (B, H, Nk, d))
+    _check(v, "v", (B, H, Nk, d))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dO, scale=None, causal=False, stream=None, workspace=None):
+    """dQ, dK, dV (bf16) for the forward output o / lse and upstream gradient dO."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    for t, n, s in ((q, "q", (B, H, Nq, d)), (k, "k", (B, H, Nk, d)), (v, "v", (B, H, Nk, d)),
+                    (o, "o", (B, H, Nq, d)), (dO, "dO", (B, H, Nq, d))):
+        _check(t, n, s)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    nbytes = fa_bwd_workspace_bytes(B, H, Nq, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace,
+           workspace.numel() * workspace.element_size(), stream)
+    return dq, dk, dv
+
+
+def decode(q, kcache, vcache, scale=None, num_splits=0, stream=None, workspace=None,
+           want_lse=True):
+    """O [B,H,d] bf16 (and LSE [B,H] fp32) for one query per (b, h) against the caches."""
+    B, H, d = q.shape
+    Nk = kcache.shape[2]
+    _check(q, "q", (B, H, d))
+    _check(kcache, "kcache", (B, H, Nk, d))
+    _check(vcache, "vcache", (B, H, Nk, d))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    nbytes = fa_decode_workspace_bytes(B, H, Nk, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if want_lse else None
+    fa_decode(q, kcache, vcache, o, lse, B, H, Nk, d, scale, num_splits, workspace,
+              workspace.numel() * workspace.element_size(), stream)
+    return (o, lse) if want_lse else o

@@ -1,0 +1,268 @@
+// The C ABI declared in include/fa.h: argument validation, TMA tensor-map
+// encoding, the per-device error word, and the launches.  No allocation, no
+// fallback: every call either launches the GPU kernels or returns an error.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+__device__ DevError g_dev_error;  // one per device (per context)
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::mutex g_mu;
+DevError* g_err_addr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Per-device state, looked up with the current device active.
+int device_state(DevError** err, int* num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_err_addr[dev]) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_dev_error) != cudaSuccess || !a) return FA_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+            return FA_ERR_CUDA;
+        g_err_addr[dev] = static_cast<DevError*>(a);
+        g_num_sms[dev] = sms;
+    }
+    if (err) *err = g_err_addr[dev];
+    if (num_sms) *num_sms = g_num_sms[dev];
+    return FA_OK;
+}
+
+int encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !f)
+            return FA_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    *fn = g_encode;
+    return FA_OK;
+}
+
+// 3-D map over a contiguous (BH, N, d) bf16 tensor: dims (d, N, BH), box
+// (64, 128, 1), 128-byte swizzle (matches the MMA shared-memory descriptors).
+int make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int st = encoder(&enc);
+    if (st != FA_OK) return st;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// Shared shape checks.  Sizes must keep every element index below 2^31 per
+// tensor row block and the total within 64-bit byte offsets.
+int check_shape(int B, int H, int Nq, int Nk, int d) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const long long BH = (long long)B * H;
+    if (BH > (1ll << 24)) return FA_ERR_UNSUPPORTED;  // work-tile indices stay in int
+    if ((long long)Nq * BH > (1ll << 36) || (long long)Nk * BH > (1ll << 36)) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+size_t bwd_ws_bytes(int B, int H, int Nq, int d) {
+    const size_t rows = (size_t)B * H * Nq;
+    return rows * d * 4 + ((rows * 4 + 255) & ~(size_t)255);
+}
+
+int decode_auto_splits(int Nk) {
+    // chunks of at least 256 keys, at most 16 chunks
+    int s = (Nk + 255) / 256;
+    return s < 1 ? 1 : (s > 16 ? 16 : s);
+}
+
+size_t decode_ws_bytes(int B, int H, int d, int splits) {
+    const size_t parts = (size_t)B * H * splits;
+    return parts * d * 4 + ((parts * 4 + 255) & ~(size_t)255);
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+uint64_t fa_set_wait_timeout_ns(uint64_t ns) {
+    if (ns < 1000000ull) ns = 1000000ull;
+    return g_timeout_ns.exchange(ns);
+}
+
+const char* fa_status_string(int st) {
+    switch (st) {
+        case FA_OK: return "ok";
+        case FA_ERR_INVALID_ARG: return "invalid argument";
+        case FA_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128)";
+        case FA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case FA_ERR_WORKSPACE: return "workspace missing or too small";
+        case FA_ERR_CUDA: return "CUDA call failed";
+        case FA_ERR_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+           int Nk, int d, float scale, int causal, void* stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, Nq, Nk, d);
+    if (st != FA_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_ALIGNMENT;
+    FwdLaunch a;
+    st = device_state(&a.err, &a.num_sms);
+    if (st != FA_OK) return st;
+    const int BH = B * H;
+    if (make_map(&a.map_q, q, BH, Nq, d) || make_map(&a.map_k, k, BH, Nk, d) ||
+        make_map(&a.map_v, v, BH, Nk, d))
+        return FA_ERR_CUDA;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.timeout_ns = g_timeout_ns.load();
+    return launch_fwd(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+    if (check_shape(B, H, Nq, Nk, d) != FA_OK) return 0;
+    return bwd_ws_bytes(B, H, Nq, d);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+           void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+           void* workspace, size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, Nq, Nk, d);
+    if (st != FA_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return FA_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < bwd_ws_bytes(B, H, Nq, d)) return FA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
+    BwdLaunch a;
+    st = device_state(&a.err, &a.num_sms);
+    if (st != FA_OK) return st;
+    const int BH = B * H;
+    if (make_map(&a.map_q, q, BH, Nq, d) || make_map(&a.map_k, k, BH, Nk, d) ||
+        make_map(&a.map_v, v, BH, Nk, d) || make_map(&a.map_do, dO, BH, Nq, d))
+        return FA_ERR_CUDA;
+    a.q = q;
+    a.k = k;
+    a.o = o;
+    a.dO = dO;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dq_acc = static_cast<float*>(workspace);
+    a.delta = a.dq_acc + (size_t)BH * Nq * d;
+    a.B = B;
+    a.H = H;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.timeout_ns = g_timeout_ns.load();
+    return launch_bwd(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int Nk, int d, int num_splits) {
+    if (check_shape(B, H, 1, Nk, d) != FA_OK || num_splits > 256) return 0;
+    const int s = num_splits <= 0 ? decode_auto_splits(Nk) : num_splits;
+    return decode_ws_bytes(B, H, d, s);
+}
+
+int fa_decode(const void* q, const void* kcache, const void* vcache, void* o, float* lse, int B, int H,
+              int Nk, int d, float scale, int num_splits, void* workspace, size_t workspace_bytes,
+              void* stream) {
+    if (!q || !kcache || !vcache || !o) return FA_ERR_INVALID_ARG;
+    if (!scale_ok(scale) || num_splits > 256) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, 1, Nk, d);
+    if (st != FA_OK) return st;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+        (lse && !aligned16(lse)))
+        return FA_ERR_ALIGNMENT;
+    const int splits = num_splits <= 0 ? decode_auto_splits(Nk) : num_splits;
+    if (!workspace || workspace_bytes < decode_ws_bytes(B, H, d, splits)) return FA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
+    st = device_state(nullptr, nullptr);
+    if (st != FA_OK) return st;
+    DecodeLaunch a;
+    a.q = q;
+    a.kc = kcache;
+    a.vc = vcache;
+    a.o = o;
+    a.lse = lse;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = a.part_o + (size_t)B * H * splits * d;
+    a.B = B;
+    a.H = H;
+    a.Nk = Nk;
+    a.d = d;
+    a.splits = splits;
+    a.chunk = (Nk + splits - 1) / splits;
+    a.scale = scale;
+    return launch_decode(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_get_last_device_error(void* stream, int* detail) {
+    if (detail)
+        for (int i = 0; i < 4; ++i) detail[i] = 0;
+    DevError* err = nullptr;
+    if (device_state(&err, nullptr) != FA_OK) return FA_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FA_ERR_CUDA;
+    DevError h;
+    if (cudaMemcpy(&h, err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+    if (h.code != 0) {
+        DevError z = {0, 0, 0, 0};
+        if (cudaMemcpy(err, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    if (detail) {
+        detail[0] = h.code;
+        detail[1] = h.site;
+        detail[2] = h.block;
+        detail[3] = h.aux;
+    }
+    return h.code == 0 ? FA_OK : FA_ERR_TIMEOUT;
+}
+
+}  // extern "C"

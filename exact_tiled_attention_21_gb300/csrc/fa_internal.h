@@ -1,0 +1,65 @@
+// Internal launch interfaces between the C-ABI layer (fa_api.cu) and the
+// kernel translation units.  Arguments arrive here already validated.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+struct FwdLaunch {
+    CUtensorMap map_q, map_k, map_v;  // 3-D maps (d, N, B*H), box (64, 128, 1), 128B swizzle
+    void* o;
+    float* lse;
+    int B, H, Nq, Nk, d;
+    float scale;
+    int causal;
+    int num_sms;
+    DevError* err;
+    uint64_t timeout_ns;
+};
+
+struct BwdLaunch {
+    CUtensorMap map_q, map_k, map_v, map_do;  // same geometry as the forward maps
+    const void* q;
+    const void* k;
+    const void* o;
+    const void* dO;
+    const float* lse;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dq_acc;  // fp32 [B,H,Nq,d]
+    float* delta;   // fp32 [B,H,Nq]
+    int B, H, Nq, Nk, d;
+    float scale;
+    int causal;
+    int num_sms;
+    DevError* err;
+    uint64_t timeout_ns;
+};
+
+struct DecodeLaunch {
+    const void* q;
+    const void* kc;
+    const void* vc;
+    void* o;
+    float* lse;      // may be null
+    float* part_o;   // fp32 [B,H,S,d]
+    float* part_lse; // fp32 [B,H,S]
+    int B, H, Nk, d, splits, chunk;
+    float scale;
+};
+
+// Each returns a cudaError_t of the launch (cudaSuccess when queued).
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);
+
+// Rows of the forward's CTA work tile (two 128-row softmax tiles).
+constexpr int kFwdRowsPerCta = 256;
+
+}  // namespace fa

@@ -1,0 +1,129 @@
+/* Exact tiled attention for GB300 (sm_103a): the C ABI.
+ *
+ * What the library computes, for every batch b and head h (all tensors
+ * contiguous, layout (B, H, N, d), d innermost):
+ *
+ *     O = softmax(scale * Q K^T  [+ causal mask]) V,   LSE_i = ln sum_j exp(scale * q_i . k_j)
+ *
+ * the definition of wiki.ai-engineering.at "Flash Attention" (section "Das
+ * Grundproblem") and johe.ru "Flash Attention: ускорить attention в 6 раз без
+ * потери точности" (section "Введение").  It is evaluated tile by tile with the
+ * online-softmax recurrence of the first page (section "Lösung: Online
+ * Softmax"), so the N x N score matrix never exists in device memory.  The
+ * result equals standard attention up to floating-point rounding; only the
+ * order of operations differs (second page, "Почему это точно?").
+ *
+ * Conventions shared by every entry point:
+ *  - q, k, v, o, dO, dq, dk, dv, caches: bf16 (__nv_bfloat16) device pointers,
+ *    16-byte aligned, contiguous (B, H, N, d); d is 64 or 128.
+ *  - lse, D and every workspace: fp32 device pointers, 16-byte aligned.
+ *  - scale is passed explicitly (1/sqrt(d) is the usual choice); it must be
+ *    finite and > 0.
+ *  - causal: 0 or 1.  The mask is aligned bottom-right: query i sees key j iff
+ *    j <= i + (Nk - Nq).  A query that sees no key gets O = 0, LSE = -inf and
+ *    zero gradients.
+ *  - stream: a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Every call is asynchronous on it; nothing is synchronised.
+ *  - Ownership: the caller allocates and owns every buffer, workspaces
+ *    included.  The library allocates no device memory and keeps no state
+ *    besides a cached driver entry point and a device-side error word.
+ *  - Errors: return codes only (fa_status); arguments are validated before
+ *    anything is launched, and an invalid call launches nothing.  No fallback
+ *    implementation exists: an unsupported shape is an error, never a slower
+ *    path.  Device-side waits are bounded; a wait that runs out records
+ *    FA_ERR_TIMEOUT in the error word, the kernel releases what it holds and
+ *    returns, and fa_get_last_device_error() reports it.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, bad scale or flag */
+    FA_ERR_UNSUPPORTED = -2, /* d not in {64, 128}, sizes beyond 32-bit tile indexing */
+    FA_ERR_ALIGNMENT = -3,   /* a pointer not 16-byte aligned */
+    FA_ERR_WORKSPACE = -4,   /* workspace null or smaller than the *_workspace_bytes query */
+    FA_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed (launch, tensor map) */
+    FA_ERR_TIMEOUT = -6      /* a device-side bounded wait ran out (see fa_get_last_device_error) */
+} fa_status;
+
+/* Forward pass (tiled attention with online softmax, one fused kernel).
+ * q [B,H,Nq,d], k/v [B,H,Nk,d] bf16 in; o [B,H,Nq,d] bf16 and lse [B,H,Nq]
+ * fp32 out (natural log of the row's sum of exp(scale * q.k)).  Source: the
+ * "Tiling Algorithm" and "Lösung: Online Softmax" sections of
+ * wiki.ai-engineering.at "Flash Attention"; each output row leaves the chip
+ * exactly once (johe.ru, section "Проблема 2: DRAM bottleneck", the count of
+ * memory round trips).  Requires B, H, Nq, Nk >= 1. */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int H, int Nq, int Nk, int d, float scale, int causal, void *stream);
+
+/* Bytes of fp32 workspace fa_bwd needs: the dQ accumulator [B,H,Nq,d] and the
+ * row terms D [B,H,Nq].  Returns 0 for invalid sizes. */
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+
+/* Backward pass (johe.ru, section "Стадии вычисления", pass 2: gradients are
+ * recomputed from the same tiles, P is rebuilt from the saved LSE instead of
+ * being stored).  Inputs: q, k, v, o (the forward output), lse (the forward's
+ * LSE), dO [B,H,Nq,d] the upstream gradient.  Outputs dq [B,H,Nq,d],
+ * dk/dv [B,H,Nk,d] bf16.  Steps: D_i = sum_c dO_ic O_ic (fp32); per key tile,
+ * S = scale QK^T recomputed, P = exp(S - LSE), dV += P^T dO, dP = dO V^T,
+ * dS = P (dP - D), dK += scale dS^T Q, dQ += scale dS K (fp32 accumulate in the
+ * workspace), then dQ is rounded to bf16.  workspace must hold at least
+ * fa_bwd_workspace_bytes(B,H,Nq,Nk,d) bytes; its contents on entry do not
+ * matter.  dQ's fp32 accumulation order is not fixed, so dq may differ in the
+ * last bits between runs. */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dO, void *dq, void *dk, void *dv,
+           int B, int H, int Nq, int Nk, int d, float scale, int causal,
+           void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of fp32 workspace fa_decode needs for num_splits partials (<= 0:
+ * the number the library would choose for this Nk).  Returns 0 for invalid
+ * sizes. */
+size_t fa_decode_workspace_bytes(int B, int H, int Nk, int d, int num_splits);
+
+/* Split-KV decode: one query token per (b, h) against a KV cache.  The key
+ * cache is streamed, not shrunk (zimaspace.com "Wie reduziert Flash Attention
+ * den Speicherverkehr ...", section "Weniger IO bedeutet nicht, dass der
+ * KV-Cache entfällt").  The Nk keys are cut into num_splits contiguous chunks of
+ * ceil(Nk / num_splits) keys; each chunk yields a partial output and partial
+ * LSE, and the partials are merged with the max-shifted rescaling of the
+ * online-softmax recurrence (wiki.ai-engineering.at "Flash Attention",
+ * "Lösung: Online Softmax").  q [B,H,d], kcache/vcache [B,H,Nk,d] bf16 in;
+ * o [B,H,d] bf16 out; lse [B,H] fp32 out, may be NULL.  num_splits <= 0 lets
+ * the library choose; otherwise 1 <= num_splits <= 256.  workspace: at least
+ * fa_decode_workspace_bytes(B,H,Nk,d,num_splits) bytes. */
+int fa_decode(const void *q, const void *kcache, const void *vcache, void *o, float *lse,
+              int B, int H, int Nk, int d, float scale, int num_splits,
+              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns FA_OK, FA_ERR_TIMEOUT (a bounded wait ran out), or
+ * FA_ERR_CUDA if synchronising or reading failed.  If `detail` is not NULL it
+ * receives 4 ints: code, site (which wait), block index, and an auxiliary
+ * value (the wait's phase), all 0 when no error was recorded. */
+int fa_get_last_device_error(void *stream, int *detail);
+
+/* Sets the limit of every device-side wait, in nanoseconds, for kernels
+ * launched after the call (default 2e9; values below 1e6 are raised to 1e6).
+ * Returns the previous value. */
+uint64_t fa_set_wait_timeout_ns(uint64_t ns);
+
+/* Static description of a status code. */
+const char *fa_status_string(int status);
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,57 @@
+"""Shared comparison helpers for the GPU parity tests (tolerances live here).
+
+Tolerances (stated for bf16 inputs, fp32 accumulation, compared with the fp64
+oracle run on the identical bf16 values widened exactly):
+  forward / decode:  max |O - O_ref| <= 1e-2, mean |O - O_ref| <= 1e-3,
+                     |LSE - LSE_ref| <= 1e-3 on finite entries; -inf where the
+                     oracle has -inf (a row that sees no key), with O = 0 there.
+  backward:          max |dX - dX_ref| <= 2e-2 * max |dX_ref| for dQ, dK, dV.
+These are the stated bounds for the workloads (scale = 1/sqrt(d)).  Off those
+workloads, a sharp softmax (large scale) can exceed the fixed 1e-2: P is
+rounded to bf16 (relative 2^-9) before the value product and O is rounded to
+bf16 at the end, so |O - O_ref| <= 2^-9 max|V| + 2^-9 |O| <= 2^-8 max|V| (plus
+fp32 accumulation noise).  ``derived_o_bound`` gives that bound.
+"""
+import numpy as np
+import torch
+
+FWD_MAX_ABS = 1e-2
+FWD_MEAN_ABS = 1e-3
+LSE_ABS = 1e-3
+GRAD_REL = 2e-2
+
+
+def f64(t):
+    """Exact widening of a (bf16 / fp32) tensor to a float64 numpy array."""
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def derived_o_bound(v):
+    """Max-abs bound from the arithmetic: two bf16 roundings of weight 2^-9 max|V|."""
+    return 2.0 ** -8 * float(np.abs(np.asarray(v, dtype=np.float64)).max()) + 1e-4
+
+
+def check_out(o, lse, o_ref, lse_ref, what="", max_abs=FWD_MAX_ABS):
+    o = np.asarray(o, dtype=np.float64)
+    err = np.abs(o - o_ref)
+    assert np.isfinite(o).all(), "%s: non-finite output" % what
+    assert err.max() <= max_abs, "%s: max |O-O_ref| = %g" % (what, err.max())
+    assert err.mean() <= FWD_MEAN_ABS, "%s: mean |O-O_ref| = %g" % (what, err.mean())
+    if lse is not None:
+        lse = np.asarray(lse, dtype=np.float64)
+        inf_ref = np.isneginf(lse_ref)
+        assert np.array_equal(np.isneginf(lse), inf_ref), "%s: -inf LSE pattern differs" % what
+        fin = ~inf_ref
+        if fin.any():
+            le = np.abs(lse[fin] - lse_ref[fin]).max()
+            assert le <= LSE_ABS, "%s: max |LSE-LSE_ref| = %g" % (what, le)
+    return float(err.max()), float(err.mean())
+
+
+def check_grad(g, g_ref, what=""):
+    g = np.asarray(g, dtype=np.float64)
+    assert np.isfinite(g).all(), "%s: non-finite gradient" % what
+    scale = max(np.abs(g_ref).max(), 1e-30)
+    rel = np.abs(g - g_ref).max() / scale
+    assert rel <= GRAD_REL, "%s: max|dX-ref|/max|ref| = %g" % (what, rel)
+    return float(rel)
