@@ -1,0 +1,413 @@
+#!/usr/bin/env python3
+"""Throughput of the exact tiled attention library on GB300; prints ONE JSON line.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+  forward (causal) and backward (preprocess, dK/dV pass, dQ pass) at
+  B=1, H=32, N=8192, d=128 — the top of the 1k-8k fwd/bwd sweep — and
+  split-KV decode (16 splits + combine) at B=32, H=32, Nk=4096, d=128.
+``value`` is forward+backward TFLOP/s (algorithmic FLOPs: 4 B H Nq Nk d / 2 for
+the causal forward, 2.5x that for the backward) over the device time of those
+kernels; decode KV-read GB/s is reported under ``decode``.  Inputs are resident
+in HBM and larger than L2 (129 MB), so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path shards by head / batch with no exchange): ``value`` sums the ranks'
+work over the slowest rank's time.  ``--impl reference`` times the fp64 CPU
+oracle (the only other implementation there is) on the host cores, on a
+bounded sample of the same workload, in the same metric.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fwd/bwd TFLOP/s (bf16, d=128, N 1k-8k, % of peak); decode KV-read GB/s"
+B, H, N, D = 1, 32, 8192, 128
+DEC_B, DEC_H, DEC_NK, DEC_SPLITS = 32, 32, 4096, 16
+SCALE = 1.0 / math.sqrt(D)
+FWD_FLOPS = 4.0 * B * H * N * N * D / 2          # causal
+BWD_FLOPS = 2.5 * FWD_FLOPS
+DKDV_FLOPS = BWD_FLOPS * 4 / 5                   # S, dP, dV, dK of the five products
+DEC_BYTES = 2.0 * DEC_B * DEC_H * DEC_NK * D * 2  # K and V cache, read once
+CONFIG = {
+    "workload": "fwd+bwd causal B=1 H=32 N=8192 d=128 (top of the 1k-8k sweep); "
+                "decode B=32 H=32 Nk=4096 d=128 16 splits",
+    "fwd_bwd": {"B": B, "H": H, "N": N, "d": D, "causal": True, "scale": "1/sqrt(d)"},
+    "decode": {"B": DEC_B, "H": DEC_H, "Nk": DEC_NK, "d": D, "splits": DEC_SPLITS},
+    "inputs": "iid N(0,1) bf16, resident in HBM",
+    "l2": "inputs larger than L2 (129 MB); no flush",
+}
+SMI_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16": float(m["bf16_tflops"]),
+                "bf16_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while the timed region runs."""
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + SMI_FIELDS, "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        def pump():
+            for line in self.proc.stdout:
+                self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+        self.thread = threading.Thread(target=pump, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [r for t, r in self.rows if t0 - 0.15 <= t <= t1 + 0.15] or [r for _, r in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if len(r) > 9 and num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if len(r) > 9 and num(r[3]) is not None]
+        reasons = set()
+        for r in rows:
+            if len(r) <= 9:
+                continue
+            for name, val in (("hw_slowdown", r[6]), ("hw_thermal_slowdown", r[7]),
+                              ("sw_thermal_slowdown", r[8]), ("sw_power_cap", r[9])):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max([num(r[4]) or 0 for r in rows if len(r) > 4])}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_sample(seconds, max_rows=None, seed=2):
+    """Time the fp64 oracle (naive materialised fwd + bwd) on query rows of head
+    (0, 0) of the fwd/bwd workload, in batches of 256 rows spread over the
+    sequence, until ``seconds`` of CPU time have passed.  Returns (flops, secs, rows)."""
+    import numpy as np
+    from exact_tiled_attention_21_gb300 import synthetic as syn
+    from oracle import naive
+    q = syn.head(seed, syn.TAG_Q, 0, 0, N, D).double().numpy()
+    k = syn.head(seed, syn.TAG_K, 0, 0, N, D).double().numpy()
+    v = syn.head(seed, syn.TAG_V, 0, 0, N, D).double().numpy()
+    do = syn.head(seed, syn.TAG_DO, 0, 0, N, D).double().numpy()
+    order = np.random.default_rng(seed).permutation(N // 256)
+    flops = 0.0
+    done = 0
+    t0 = time.perf_counter()
+    for blk in order:
+        rows = np.arange(blk * 256, blk * 256 + 256)
+        naive.forward(q[rows], k, v, SCALE, True, rows=rows, Nq=N)
+        naive.backward(q[rows], k, v, do[rows], SCALE, True, rows=rows, Nq=N)
+        vis = (rows + 1).sum()  # causal: row i sees i + 1 keys
+        flops += 4.0 * D * vis * 3.5  # forward + 2.5x backward
+        done += 256
+        if time.perf_counter() - t0 >= seconds or (max_rows and done >= max_rows):
+            break
+    return flops, time.perf_counter() - t0, done
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return 0
+    per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(per_step)
+    tot_f, tot_t, tot_r = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        f, t, r = oracle_sample(per_step)
+        tot_f, tot_t, tot_r = tot_f + f, tot_t + t, tot_r + r
+    value = tot_f / tot_t / 1e12
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": CONFIG,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "per step: numpy fp64 naive fwd+bwd of 256-row query blocks of head "
+                                   "(0,0), N=8192 causal, for %.1f s (%d rows in all)" % (per_step, tot_r)},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import exact_tiled_attention_21_gb300 as fa
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    fa.load()
+    stream = torch.cuda.current_stream(dev)
+
+    g = torch.Generator(device=dev).manual_seed(1234 + rank)
+    rnd = lambda *shape: torch.randn(*shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    q, k, v, dO = (rnd(B, H, N, D) for _ in range(4))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty(B, H, N, device=dev, dtype=torch.float32)
+    dq_, kc, vc = rnd(DEC_B, DEC_H, D), rnd(DEC_B, DEC_H, DEC_NK, D), rnd(DEC_B, DEC_H, DEC_NK, D)
+    od = torch.empty_like(dq_)
+    lsed = torch.empty(DEC_B, DEC_H, device=dev, dtype=torch.float32)
+    dws = torch.empty(fa.fa_decode_workspace_bytes(DEC_B, DEC_H, DEC_NK, D, DEC_SPLITS),
+                      dtype=torch.uint8, device=dev)
+    bws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, N, D), dtype=torch.uint8, device=dev)
+    LAUNCHES_PER_STEP = 6  # fwd 1, bwd 3, decode 2
+
+    def step(ev=None):
+        rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
+        rec(0)
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, N, D, SCALE, True, stream)
+        rec(1)
+        fa.fa_bwd_preprocess(o, dO, delta, B, H, N, D, stream)
+        rec(2)
+        fa.fa_bwd_dkdv(q, k, v, lse, delta, dO, dk, dv, B, H, N, N, D, SCALE, True, stream)
+        rec(3)
+        fa.fa_bwd_dq(q, k, v, lse, delta, dO, dq, B, H, N, N, D, SCALE, True, stream)
+        rec(4)
+        fa.fa_decode(dq_, kc, vc, od, lsed, DEC_B, DEC_H, DEC_NK, D, SCALE, DEC_SPLITS, dws,
+                     dws.numel(), stream)
+        rec(5)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    st, detail = fa.fa_get_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError("device error during warm-up: %s" % detail)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    w0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    barrier()
+    w1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    st, detail = fa.fa_get_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError("device error in the timed region: %s" % detail)
+
+    total_ms = t_start.elapsed_time(t_end)
+    comp = [0.0] * 5
+    for e in evs:
+        for j in range(5):
+            comp[j] += e[j].elapsed_time(e[j + 1])
+    K = args.steps
+    fwd_ms, pre_ms, dkdv_ms, dq_ms, dec_ms = (c / K for c in comp)
+    fb_ms = fwd_ms + pre_ms + dkdv_ms + dq_ms
+
+    def maxall(x):
+        if not dist:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    total_ms = maxall(total_ms)
+    fb_ms_max = maxall(fb_ms)
+    dec_ms_max = maxall(dec_ms)
+    value = world * (FWD_FLOPS + BWD_FLOPS) / (fb_ms_max * 1e-3) / 1e12
+
+    # ---- end to end through the public API, host buffers, copies inside the timed region
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    hq, hk, hv, hdO = (pin(t) for t in (q, k, v, dO))
+    for h_, d_ in ((hq, q), (hk, k), (hv, v), (hdO, dO)):
+        h_.copy_(d_)
+    hqd = pin(dq_)
+    hqd.copy_(dq_)
+    ho, hl, hdq, hdk, hdv = pin(o), pin(lse), pin(dq), pin(dk), pin(dv)
+    hod, hld = pin(od), pin(lsed)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdO, hqd))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv, hod, hld))
+    e2e_steps = max(1, min(K, 20))
+
+    def e2e_step(ev):
+        ev[0].record(stream)
+        for d_, h_ in ((q, hq), (k, hk), (v, hv), (dO, hdO)):
+            d_.copy_(h_, non_blocking=True)
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, N, D, SCALE, True, stream)
+        fa.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, D, SCALE, True, bws, bws.numel(), stream)
+        for h_, d_ in ((ho, o), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            h_.copy_(d_, non_blocking=True)
+        ev[1].record(stream)
+        dq_.copy_(hqd, non_blocking=True)
+        fa.fa_decode(dq_, kc, vc, od, lsed, DEC_B, DEC_H, DEC_NK, D, SCALE, DEC_SPLITS, dws,
+                     dws.numel(), stream)
+        hod.copy_(od, non_blocking=True)
+        hld.copy_(lsed, non_blocking=True)
+        ev[2].record(stream)
+
+    for _ in range(2):
+        e2e_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    barrier()
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        e2e_step(eev[i])
+    barrier()
+    e2e_fb = maxall(sum(e[0].elapsed_time(e[1]) for e in eev) / e2e_steps)
+    e2e_dec = maxall(sum(e[1].elapsed_time(e[2]) for e in eev) / e2e_steps)
+    st, detail = fa.fa_get_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError("device error in the end-to-end run: %s" % detail)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    pk = peaks()
+    dkdv_tflops = DKDV_FLOPS / (dkdv_ms * 1e-3) / 1e12
+    clocks = sampler.summary(w0, w1)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": CONFIG,
+        "components": {
+            "fwd_ms": fwd_ms, "fwd_tflops": FWD_FLOPS / (fwd_ms * 1e-3) / 1e12,
+            "bwd_ms": pre_ms + dkdv_ms + dq_ms,
+            "bwd_tflops": BWD_FLOPS / ((pre_ms + dkdv_ms + dq_ms) * 1e-3) / 1e12,
+            "bwd_pre_ms": pre_ms, "bwd_dkdv_ms": dkdv_ms, "bwd_dq_ms": dq_ms,
+            "fwd_frac_of_peak": FWD_FLOPS / (fwd_ms * 1e-3) / 1e12 / pk["bf16_sustained"],
+            "bwd_frac_of_peak": BWD_FLOPS / ((pre_ms + dkdv_ms + dq_ms) * 1e-3) / 1e12 / pk["bf16_sustained"],
+        },
+        "decode": {"value": world * DEC_BYTES / (dec_ms_max * 1e-3) / 1e9, "unit": "GB/s",
+                   "ms": dec_ms, "frac_of_hbm": DEC_BYTES / (dec_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "roofline": {
+            "kernel": "bwd_dkdv_kernel<128>",
+            "bound": "tensor",
+            "achieved": dkdv_tflops,
+            "peak": pk["bf16_sustained"],
+            "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step loop)" % pk["source"],
+            "unit": "TFLOP/s",
+            "frac": dkdv_tflops / pk["bf16_sustained"],
+            "traffic": None,
+            "algorithmic_per_launch": "4 of the 5 backward products: 4 * B*H*N*N*d FLOP (causal half of 8 B H N^2 d)",
+        },
+        "e2e": {"value": world * (FWD_FLOPS + BWD_FLOPS) / (e2e_fb * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "decode_gbs": world * DEC_BYTES / (e2e_dec * 1e-3) / 1e9,
+                "api": "fa_fwd + fa_bwd + fa_decode from pinned host buffers; KV cache resident"},
+        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        f, t, r = oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": f / t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": "numpy fp64 naive fwd+bwd of %d query rows (256-row blocks spread over the "
+                      "sequence) of head (0,0), N=8192 causal, %.1f s" % (r, t)}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank)
+    return run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

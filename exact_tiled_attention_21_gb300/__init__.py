@@ -1,6 +1,7 @@
 """Exact tiled attention on GB300 (sm_103a) — Python binding of the C ABI.
 
-The functions ``fa_fwd``, ``fa_bwd``, ``fa_decode``, ``fa_bwd_workspace_bytes``,
+The functions ``fa_fwd``, ``fa_bwd`` (and its steps ``fa_bwd_preprocess``,
+``fa_bwd_dkdv``, ``fa_bwd_dq``), ``fa_decode``, ``fa_bwd_workspace_bytes``,
 ``fa_decode_workspace_bytes``, ``fa_get_last_device_error``,
 ``fa_set_wait_timeout_ns``, ``fa_status_string`` and ``fa_version`` carry the
 names and arguments of ``include/fa.h`` and only marshal arguments: every step
@@ -68,6 +69,12 @@ def load():
     lib.fa_bwd_workspace_bytes.restype = sz
     lib.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
+    lib.fa_bwd_preprocess.restype = i
+    lib.fa_bwd_dkdv.argtypes = [vp] * 8 + [i, i, i, i, i, f, i, vp]
+    lib.fa_bwd_dkdv.restype = i
+    lib.fa_bwd_dq.argtypes = [vp] * 7 + [i, i, i, i, i, f, i, vp]
+    lib.fa_bwd_dq.restype = i
     lib.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i]
     lib.fa_decode_workspace_bytes.restype = sz
     lib.fa_decode.argtypes = [vp] * 5 + [i, i, i, i, f, i, vp, sz, vp]
@@ -146,6 +153,23 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, work
     _raise(load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
                          _ptr(dk), _ptr(dv), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
                          _ptr(workspace), int(workspace_bytes), _stream(stream)), "fa_bwd")
+
+
+def fa_bwd_preprocess(o, dO, delta, B, H, Nq, d, stream=None):
+    _raise(load().fa_bwd_preprocess(_ptr(o), _ptr(dO), _ptr(delta), B, H, Nq, d, _stream(stream)),
+           "fa_bwd_preprocess")
+
+
+def fa_bwd_dkdv(q, k, v, lse, delta, dO, dk, dv, B, H, Nq, Nk, d, scale, causal, stream=None):
+    _raise(load().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(dO), _ptr(dk),
+                              _ptr(dv), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+                              _stream(stream)), "fa_bwd_dkdv")
+
+
+def fa_bwd_dq(q, k, v, lse, delta, dO, dq, B, H, Nq, Nk, d, scale, causal, stream=None):
+    _raise(load().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(dO), _ptr(dq),
+                            B, H, Nq, Nk, d, float(scale), int(bool(causal)), _stream(stream)),
+           "fa_bwd_dq")
 
 
 def fa_decode(q, kcache, vcache, o, lse, B, H, Nk, d, scale, num_splits, workspace,

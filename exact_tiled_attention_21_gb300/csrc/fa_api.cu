@@ -87,9 +87,12 @@ int check_shape(int B, int H, int Nq, int Nk, int d) {
 
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
 
+// The backward keeps dQ in TMEM (Q-tile-parallel pass), so its only scratch
+// is D = rowsum(dO o O): one fp32 per query row.
 size_t bwd_ws_bytes(int B, int H, int Nq, int d) {
+    (void)d;
     const size_t rows = (size_t)B * H * Nq;
-    return rows * d * 4 + ((rows * 4 + 255) & ~(size_t)255);
+    return (rows * 4 + 255) & ~(size_t)255;
 }
 
 int decode_auto_splits(int Nk) {
@@ -164,45 +167,100 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
     return bwd_ws_bytes(B, H, Nq, d);
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-           void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
-           void* workspace, size_t workspace_bytes, void* stream) {
-    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Shared checks of the backward steps.  Pointers that a step does not use are
+// passed as `used = false` and not checked.
+int bwd_prepare(BwdLaunch* a, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const float* delta, const void* dO, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
+                int d, float scale, int causal, bool need_maps) {
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
     int st = check_shape(B, H, Nq, Nk, d);
     if (st != FA_OK) return st;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-        !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-        return FA_ERR_ALIGNMENT;
+    const void* ptrs[] = {q, k, v, o, lse, delta, dO, dq, dk, dv};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return FA_ERR_ALIGNMENT;
+    st = device_state(&a->err, &a->num_sms);
+    if (st != FA_OK) return st;
+    const int BH = B * H;
+    if (need_maps && (make_map(&a->map_q, q, BH, Nq, d) || make_map(&a->map_k, k, BH, Nk, d) ||
+                      make_map(&a->map_v, v, BH, Nk, d) || make_map(&a->map_do, dO, BH, Nq, d)))
+        return FA_ERR_CUDA;
+    a->q = q;
+    a->k = k;
+    a->o = o;
+    a->dO = dO;
+    a->lse = lse;
+    a->dq = dq;
+    a->dk = dk;
+    a->dv = dv;
+    a->delta = const_cast<float*>(delta);
+    a->B = B;
+    a->H = H;
+    a->Nq = Nq;
+    a->Nk = Nk;
+    a->d = d;
+    a->scale = scale;
+    a->causal = causal;
+    a->timeout_ns = g_timeout_ns.load();
+    return FA_OK;
+}
+
+int launched(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+           void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+           void* workspace, size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, Nq, Nk, d);
+    if (st != FA_OK) return st;
     if (!workspace || workspace_bytes < bwd_ws_bytes(B, H, Nq, d)) return FA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
     BwdLaunch a;
-    st = device_state(&a.err, &a.num_sms);
+    st = bwd_prepare(&a, q, k, v, o, lse, static_cast<float*>(workspace), dO, dq, dk, dv, B, H, Nq, Nk, d,
+                     scale, causal, true);
     if (st != FA_OK) return st;
-    const int BH = B * H;
-    if (make_map(&a.map_q, q, BH, Nq, d) || make_map(&a.map_k, k, BH, Nk, d) ||
-        make_map(&a.map_v, v, BH, Nk, d) || make_map(&a.map_do, dO, BH, Nq, d))
-        return FA_ERR_CUDA;
-    a.q = q;
-    a.k = k;
-    a.o = o;
-    a.dO = dO;
-    a.lse = lse;
-    a.dq = dq;
-    a.dk = dk;
-    a.dv = dv;
-    a.dq_acc = static_cast<float*>(workspace);
-    a.delta = a.dq_acc + (size_t)BH * Nq * d;
-    a.B = B;
-    a.H = H;
-    a.Nq = Nq;
-    a.Nk = Nk;
-    a.d = d;
-    a.scale = scale;
-    a.causal = causal;
-    a.timeout_ns = g_timeout_ns.load();
-    return launch_bwd(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((st = launched(launch_bwd_pre(a, s))) != FA_OK) return st;
+    if ((st = launched(launch_bwd_dkdv(a, s))) != FA_OK) return st;
+    return launched(launch_bwd_dq(a, s));
+}
+
+int fa_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H, int Nq, int d, void* stream) {
+    if (!o || !dO || !delta) return FA_ERR_INVALID_ARG;
+    BwdLaunch a;
+    int st = bwd_prepare(&a, nullptr, nullptr, nullptr, o, nullptr, delta, dO, nullptr, nullptr, nullptr, B, H,
+                         Nq, 1, d, 1.f, 0, false);
+    if (st != FA_OK) return st;
+    return launched(launch_bwd_pre(a, (cudaStream_t)stream));
+}
+
+int fa_bwd_dkdv(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                const void* dO, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                void* stream) {
+    if (!q || !k || !v || !lse || !delta || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
+    BwdLaunch a;
+    int st = bwd_prepare(&a, q, k, v, nullptr, lse, delta, dO, nullptr, dk, dv, B, H, Nq, Nk, d, scale, causal,
+                         true);
+    if (st != FA_OK) return st;
+    return launched(launch_bwd_dkdv(a, (cudaStream_t)stream));
+}
+
+int fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse, const float* delta, const void* dO,
+              void* dq, int B, int H, int Nq, int Nk, int d, float scale, int causal, void* stream) {
+    if (!q || !k || !v || !lse || !delta || !dO || !dq) return FA_ERR_INVALID_ARG;
+    BwdLaunch a;
+    int st = bwd_prepare(&a, q, k, v, nullptr, lse, delta, dO, dq, nullptr, nullptr, B, H, Nq, Nk, d, scale,
+                         causal, true);
+    if (st != FA_OK) return st;
+    return launched(launch_bwd_dq(a, (cudaStream_t)stream));
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int Nk, int d, int num_splits) {

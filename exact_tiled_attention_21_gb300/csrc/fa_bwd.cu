@@ -1,6 +1,585 @@
-// Backward pass (placeholder until the kernels land): reports "not supported".
+// Backward pass: gradients recomputed tile by tile from the saved LSE.
+//
+// Method (johe.ru "Flash Attention: ...", section "Стадии вычисления", pass 2:
+// the gradients are computed from the same tiles without storing the N x N
+// matrix; "Проблема 3": keeping that matrix for the backward would double the
+// memory).  With P = exp(scale S - LSE) rebuilt from the forward's LSE:
+//     dV = P^T dO,   dP = dO V^T,   D_i = sum_c dO_ic O_ic,
+//     dS = P o (dP - D),   dK = scale dS^T Q,   dQ = scale dS K.
+//
+// Three launches on one stream:
+//   bwd_pre   D_i = rowsum(dO o O) in fp32 (one warp per row).
+//   bwd_dkdv  one CTA per 128-key tile (KV-tile parallel): K_j, V_j stay in
+//             shared memory, Q_i / dO_i stream through a 2-stage ring;
+//             tcgen05: S^T = K Q^T and dP^T = V dO^T into TMEM, dV += P^T dO
+//             and dK += dS^T Q with P^T / dS^T read from TMEM; dK, dV
+//             accumulate in TMEM over all query tiles.
+//   bwd_dq    one CTA per 128-query tile (Q-tile parallel): Q_i, dO_i stay,
+//             K_j / V_j stream; S = Q K^T, dP = dO V^T, dQ += dS K with dS
+//             from TMEM.  dQ is accumulated in fp32 TMEM and written once, so
+//             the backward needs no atomics and is deterministic.
+// In both, one thread per TMEM lane (the 128 rows of the tile) computes P
+// and dS; P stays in registers (packed bf16) so the next score MMA can be
+// issued while dS is being formed.
 #include "fa_internal.h"
 
 namespace fa {
-cudaError_t launch_bwd(const BwdLaunch&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+template <int D>
+struct Bwd {
+    static constexpr int KCH = D / 64;
+    static constexpr int TILE = 128 * D * 2;  // one 128-row bf16 tile
+    static constexpr int CHUNK = 128 * 128;   // 128 rows x 128 bytes (one swizzle column block)
+    static constexpr int OFF_FIXED = 0;       // two resident tiles
+    static constexpr int OFF_STAGE = 2 * TILE;  // 2 stages x 2 streamed tiles
+    static constexpr int OFF_VEC = OFF_STAGE + 4 * TILE;  // dkdv: lse2/delta per stage (2 x 1 KB)
+    static constexpr int OFF_BAR = OFF_VEC + 2048;
+    static constexpr int NBAR = 12;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 16 + 1024;
+    static constexpr int THREADS = 192;  // warps 0-3 compute, 4 producer, 5 MMA
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_A = 0;      // S / S^T fp32; P^T bf16 over its first 64 columns
+    static constexpr uint32_t COL_B = 128;    // dP / dP^T fp32; dS / dS^T bf16 over its first 64
+    static constexpr uint32_t COL_ACC0 = 256; // dV (dkdv) or dQ (dq)
+    static constexpr uint32_t COL_ACC1 = 256 + D;  // dK (dkdv)
+    static constexpr uint32_t IDESC_SS = idesc_bf16(128, 128, 0, 0);
+    static constexpr uint32_t IDESC_TS = idesc_bf16(128, D, 0, 1);
+};
+
+struct BwdParams {
+    __nv_bfloat16* dq;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    const float* lse;
+    const float* delta;
+    int BH, Nq, Nk, causal, n_qt, n_kt;
+    float scale, scale_log2;
+    DevError* err;
+    uint64_t timeout_ns;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------ D = rowsum(dO o O)
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
+               float* __restrict__ delta, long long rows) {
+    constexpr int PER = D / 32;
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const __nv_bfloat16* a = o + row * D + lane * PER;
+    const __nv_bfloat16* b = dO + row * D + lane * PER;
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; i += 2) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(a + i));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(b + i));
+        s = fmaf(x.x, y.x, s);
+        s = fmaf(x.y, y.y, s);
+    }
+    for (int w = 16; w >= 1; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+    if (lane == 0) delta[row] = s;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Issue C[tmem] = A B^T over K = D with both operands K-major 128-row tiles.
+template <int D>
+__device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t sA, uint32_t sB) {
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * Bwd<D>::CHUNK + (k & 3) * 32;
+        mma_ss(d_tmem, sdesc_sw128(sA + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024),
+               Bwd<D>::IDESC_SS, k > 0);
+    }
+}
+
+// Issue C[tmem] (+)= A[tmem, 128 x 128 bf16] B[smem, 128 x D, MN-major].
+template <int D>
+__device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, bool acc) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        mma_ts(d_tmem, a_tmem + k * 8, sdesc_sw128(sB + k * 2048, Bwd<D>::CHUNK, 1024),
+               Bwd<D>::IDESC_TS, (acc || k > 0) ? 1u : 0u);
+}
+
+// Writes a 128-row accumulator row (thread = row) scaled by `mul` as bf16.
+template <int D>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, __nv_bfloat16* dst, float mul, bool valid,
+                                              bool zero) {
+#pragma unroll 1
+    for (int q4 = 0; q4 < D / 32; ++q4) {
+        uint32_t v[32];
+        if (!zero) {
+            tmem_ld32(taddr + q4 * 32, v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+        if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+    }
+}
+
+// Shared prologue: barriers, TMEM.  Returns the TMEM base.
+template <int D>
+__device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t bar0, const WaitCtl& ctl,
+                                              const uint32_t* counts, int nbar) {
+    const int tid = threadIdx.x, warp = tid >> 5;
+    uint32_t* tmem_slot = (uint32_t*)(smem + Bwd<D>::OFF_MISC);
+    if (tid == 0) {
+        *ctl.abort = 0;
+        for (int b = 0; b < nbar; ++b) mbar_init(bar0 + 8 * b, counts[b]);
+        fence_mbar_init();
+        if ((smem_u32(smem) & 1023u) != 0) record_error(ctl, kErrTimeout, kSiteAlign, 0);
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), Bwd<D>::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    return *tmem_slot;
+}
+
+template <int D>
+__device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if ((threadIdx.x >> 5) == 5) {
+        __syncwarp();
+        tmem_dealloc(tmem, Bwd<D>::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ dK, dV (KV-tile parallel)
+template <int D>
+__global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
+bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                const BwdParams p) {
+    using C = Bwd<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t bar0 = s_base + C::OFF_BAR;
+    // barriers
+    const uint32_t B_KV = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_DP = bar0 + 48,
+                   B_P = bar0 + 56, B_DS = bar0 + 64, B_ACC = bar0 + 72, B_TD = bar0 + 80;
+    const uint32_t counts[11] = {1, 32, 32, 1, 1, 1, 1, 128, 128, 1, 1};
+    volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
+    const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
+    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 11);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kt = blockIdx.x / p.BH;  // causal: small key tiles see the most queries: heavy first
+    const int bh = blockIdx.x - kt * p.BH;
+    const int off = p.Nk - p.Nq;
+    int i0 = 0;
+    if (p.causal) {
+        const int first_q = kt * 128 - off;  // smallest query that sees key kt*128
+        i0 = first_q <= 0 ? 0 : first_q / 128;
+    }
+    const int n = i0 < p.n_qt ? p.n_qt - i0 : 0;
+    const uint32_t sK = s_base + C::OFF_FIXED, sV = sK + C::TILE;
+    auto sQ = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
+    auto sDO = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
+    float* vec = (float*)(smem + C::OFF_VEC);  // stage s: lse2 at [s*256], delta at [s*256 + 128]
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer (whole warp)
+        if (!*abort_flag && n > 0) {
+            const uint64_t pol = l2_policy_evict_last();
+            if (lane == 0) {
+                tma_prefetch_desc(&map_q);
+                tma_prefetch_desc(&map_do);
+                mbar_arrive_expect_tx(B_KV, 2 * C::TILE);
+                for (int c = 0; c < C::KCH; ++c) {
+                    tma_load_3d(sK + c * C::CHUNK, &map_k, B_KV, c * 64, kt * 128, bh, pol);
+                    tma_load_3d(sV + c * C::CHUNK, &map_v, B_KV, c * 64, kt * 128, bh, pol);
+                }
+            }
+            uint32_t issued = 0, issued_par = 0;
+            for (int ii = 0; ii < n; ++ii) {
+                const int st = ii & 1, i = i0 + ii;
+                if (!mbar_wait(B_STE + 8 * st, ((ii >> 1) & 1) ^ 1, ctl, kSiteBwdQEmpty)) break;
+                for (int e = lane; e < 128; e += 32) {
+                    const int q = i * 128 + e;
+                    float l2 = INFINITY, dl = 0.f;
+                    if (q < p.Nq) {
+                        const float L = p.lse[(size_t)bh * p.Nq + q];
+                        l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
+                        dl = p.delta[(size_t)bh * p.Nq + q];
+                    }
+                    vec[st * 256 + e] = l2;
+                    vec[st * 256 + 128 + e] = dl;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(B_STF + 8 * st, 2 * C::TILE);
+                    for (int c = 0; c < C::KCH; ++c) {
+                        tma_load_3d(sQ(st) + c * C::CHUNK, &map_q, B_STF + 8 * st, c * 64, i * 128, bh, pol);
+                        tma_load_3d(sDO(st) + c * C::CHUNK, &map_do, B_STF + 8 * st, c * 64, i * 128, bh, pol);
+                    }
+                } else {
+                    mbar_arrive(B_STF + 8 * st);
+                }
+                issued |= 1u << st;
+                issued_par = (issued_par & ~(1u << st)) | ((uint32_t)((ii >> 1) & 1) << st);
+            }
+            if (*abort_flag && lane == 0) {  // let the loads in flight land before exit
+                mbar_drain(B_KV, 0, ctl, kSiteTeardown);
+                for (int st = 0; st < 2; ++st)
+                    if (issued & (1u << st)) mbar_drain(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && !*abort_flag && n > 0) {
+            bool ok = mbar_wait(B_KV, 0, ctl, kSiteBwdKvFull);
+            if (ok) ok = mbar_wait(B_STF, 0, ctl, kSiteBwdQFull);
+            if (ok) {
+                tc_fence_after();
+                issue_ss<D>(tmem + C::COL_A, sK, sQ(0));
+                mma_commit(B_S);
+                issue_ss<D>(tmem + C::COL_B, sV, sDO(0));
+                mma_commit(B_DP);
+            }
+            for (int ii = 0; ii < n && ok; ++ii) {
+                const int st = ii & 1;
+                if (!(ok = mbar_wait(B_P, ii & 1, ctl, kSiteBwdP))) break;
+                tc_fence_after();
+                issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_A, sDO(st), ii > 0);  // dV += P^T dO
+                const bool more = ii + 1 < n;
+                if (more) {
+                    if (!(ok = mbar_wait(B_STF + 8 * (st ^ 1), ((ii + 1) >> 1) & 1, ctl, kSiteBwdQFull))) break;
+                    tc_fence_after();
+                    issue_ss<D>(tmem + C::COL_A, sK, sQ(st ^ 1));  // S^T of the next query tile
+                    mma_commit(B_S);
+                }
+                if (!(ok = mbar_wait(B_DS, ii & 1, ctl, kSiteBwdDS))) break;
+                tc_fence_after();
+                issue_ts<D>(tmem + C::COL_ACC1, tmem + C::COL_B, sQ(st), ii > 0);  // dK += dS^T Q
+                mma_commit(B_STE + 8 * st);
+                if (more) {
+                    issue_ss<D>(tmem + C::COL_B, sV, sDO(st ^ 1));  // dP^T of the next query tile
+                    mma_commit(B_DP);
+                }
+            }
+            if (ok) mma_commit(B_ACC);
+            if (*abort_flag) {
+                mma_commit(B_TD);
+                mbar_drain(B_TD, 0, ctl, kSiteTeardown);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ P^T, dS^T, epilogue
+        const int r = ((warp & 3) << 5) + lane;  // key row within the tile = TMEM lane
+        const int kg = kt * 128 + r;
+        const bool row_ok = kg < p.Nk;
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const float sc = p.scale_log2;
+        bool ok = true;
+        for (int ii = 0; ii < n; ++ii) {
+            const int st = ii & 1, i = i0 + ii;
+            const float* l2 = vec + st * 256;
+            const float* dl = l2 + 128;
+            // key kg is visible to query q iff kg <= q + off, i.e. column c >= cmin
+            const int cmin = p.causal ? kg - off - i * 128 : -1;
+            if (!(ok = mbar_wait(B_S, ii & 1, ctl, kSiteBwdS))) break;
+            tc_fence_after();
+            uint32_t pp[64];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t v[32];
+                tmem_ld32(lane_addr + C::COL_A + q4 * 32, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int c0 = q4 * 32 + 2 * e;
+                    float a = ex2(fmaf(__uint_as_float(v[2 * e]), sc, -l2[c0]));
+                    float b = ex2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -l2[c0 + 1]));
+                    if (!row_ok || c0 < cmin) a = 0.f;
+                    if (!row_ok || c0 + 1 < cmin) b = 0.f;
+                    pk[e] = pack_bf16(a, b);
+                    pp[q4 * 16 + e] = pk[e];
+                }
+                tmem_st16(lane_addr + C::COL_A + q4 * 16, pk);
+            }
+            tc_fence_before();
+            mbar_arrive(B_P);
+            if (!(ok = mbar_wait(B_DP, ii & 1, ctl, kSiteBwdDP))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t v[32];
+                tmem_ld32(lane_addr + C::COL_B + q4 * 32, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int c0 = q4 * 32 + 2 * e;
+                    const uint32_t pr = pp[q4 * 16 + e];
+                    const float a = bf_lo(pr) * (__uint_as_float(v[2 * e]) - dl[c0]);
+                    const float b = bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dl[c0 + 1]);
+                    pk[e] = pack_bf16(a, b);
+                }
+                tmem_st16(lane_addr + C::COL_B + q4 * 16, pk);
+            }
+            tc_fence_before();
+            mbar_arrive(B_DS);
+        }
+        if (ok) {
+            bool have = n > 0;
+            if (have) {
+                ok = mbar_wait(B_ACC, 0, ctl, kSiteBwdDone);
+                tc_fence_after();
+            }
+            if (ok) {
+                const size_t base = ((size_t)bh * p.Nk + (row_ok ? kg : 0)) * D;
+                store_acc_row<D>(lane_addr + C::COL_ACC0, p.dv + base, 1.f, row_ok, !have);
+                store_acc_row<D>(lane_addr + C::COL_ACC1, p.dk + base, p.scale, row_ok, !have);
+            }
+        }
+    }
+    bwd_teardown<D>(tmem);
+}
+
+// ------------------------------------------------------------------ dQ (Q-tile parallel)
+template <int D>
+__global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+              const BwdParams p) {
+    using C = Bwd<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t bar0 = s_base + C::OFF_BAR;
+    const uint32_t B_Q = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_SF = bar0 + 48,
+                   B_DP = bar0 + 56, B_DS = bar0 + 64, B_ACC = bar0 + 72, B_TD = bar0 + 80;
+    const uint32_t counts[11] = {1, 1, 1, 1, 1, 1, 128, 1, 128, 1, 1};
+    volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
+    const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
+    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 11);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int mr = blockIdx.x / p.BH;
+    const int bh = blockIdx.x - mr * p.BH;
+    const int it = p.causal ? p.n_qt - 1 - mr : mr;  // causal: late query tiles (most keys) first
+    const int off = p.Nk - p.Nq;
+    int n = p.n_kt;
+    if (p.causal) {
+        const int qmax = min(it * 128 + 127, p.Nq - 1);
+        const long long lim = (long long)qmax + off;
+        n = lim < 0 ? 0 : min(p.n_kt, (int)(lim / 128) + 1);
+    }
+    const uint32_t sQ = s_base + C::OFF_FIXED, sDO = sQ + C::TILE;
+    auto sK = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
+    auto sV = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
+
+    if (warp == 4) {
+        if (lane == 0 && !*abort_flag && n > 0) {
+            const uint64_t pol = l2_policy_evict_last();
+            tma_prefetch_desc(&map_k);
+            tma_prefetch_desc(&map_v);
+            mbar_arrive_expect_tx(B_Q, 2 * C::TILE);
+            for (int c = 0; c < C::KCH; ++c) {
+                tma_load_3d(sQ + c * C::CHUNK, &map_q, B_Q, c * 64, it * 128, bh, pol);
+                tma_load_3d(sDO + c * C::CHUNK, &map_do, B_Q, c * 64, it * 128, bh, pol);
+            }
+            uint32_t issued = 0, issued_par = 0;
+            for (int jj = 0; jj < n; ++jj) {
+                const int st = jj & 1;
+                if (!mbar_wait(B_STE + 8 * st, ((jj >> 1) & 1) ^ 1, ctl, kSiteBwdQEmpty)) break;
+                mbar_arrive_expect_tx(B_STF + 8 * st, 2 * C::TILE);
+                for (int c = 0; c < C::KCH; ++c) {
+                    tma_load_3d(sK(st) + c * C::CHUNK, &map_k, B_STF + 8 * st, c * 64, jj * 128, bh, pol);
+                    tma_load_3d(sV(st) + c * C::CHUNK, &map_v, B_STF + 8 * st, c * 64, jj * 128, bh, pol);
+                }
+                issued |= 1u << st;
+                issued_par = (issued_par & ~(1u << st)) | ((uint32_t)((jj >> 1) & 1) << st);
+            }
+            if (*abort_flag) {
+                mbar_drain(B_Q, 0, ctl, kSiteTeardown);
+                for (int st = 0; st < 2; ++st)
+                    if (issued & (1u << st)) mbar_drain(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0 && !*abort_flag && n > 0) {
+            bool ok = mbar_wait(B_Q, 0, ctl, kSiteBwdQFull);
+            if (ok) ok = mbar_wait(B_STF, 0, ctl, kSiteBwdKvFull);
+            if (ok) {
+                tc_fence_after();
+                issue_ss<D>(tmem + C::COL_A, sQ, sK(0));
+                mma_commit(B_S);
+                issue_ss<D>(tmem + C::COL_B, sDO, sV(0));
+                mma_commit(B_DP);
+            }
+            for (int jj = 0; jj < n && ok; ++jj) {
+                const int st = jj & 1;
+                const bool more = jj + 1 < n;
+                if (more) {
+                    if (!(ok = mbar_wait(B_SF, jj & 1, ctl, kSiteBwdP))) break;
+                    if (!(ok = mbar_wait(B_STF + 8 * (st ^ 1), ((jj + 1) >> 1) & 1, ctl, kSiteBwdKvFull))) break;
+                    tc_fence_after();
+                    issue_ss<D>(tmem + C::COL_A, sQ, sK(st ^ 1));
+                    mma_commit(B_S);
+                }
+                if (!(ok = mbar_wait(B_DS, jj & 1, ctl, kSiteBwdDS))) break;
+                tc_fence_after();
+                issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sK(st), jj > 0);  // dQ += dS K
+                mma_commit(B_STE + 8 * st);
+                if (more) {
+                    issue_ss<D>(tmem + C::COL_B, sDO, sV(st ^ 1));
+                    mma_commit(B_DP);
+                }
+            }
+            if (ok) mma_commit(B_ACC);
+            if (*abort_flag) {
+                mma_commit(B_TD);
+                mbar_drain(B_TD, 0, ctl, kSiteTeardown);
+            }
+        }
+    } else {
+        const int r = ((warp & 3) << 5) + lane;  // query row within the tile = TMEM lane
+        const int qg = it * 128 + r;
+        const bool row_ok = qg < p.Nq;
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        float l2 = INFINITY, dl = 0.f;
+        if (row_ok) {
+            const float L = p.lse[(size_t)bh * p.Nq + qg];
+            l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
+            dl = p.delta[(size_t)bh * p.Nq + qg];
+        }
+        const float sc = p.scale_log2;
+        const int lim_row = p.causal ? min(qg + off, p.Nk - 1) : p.Nk - 1;  // last key this row sees
+        bool ok = true;
+        for (int jj = 0; jj < n; ++jj) {
+            const int cmax = lim_row - jj * 128;  // columns > cmax are masked
+            if (!(ok = mbar_wait(B_S, jj & 1, ctl, kSiteBwdS))) break;
+            tc_fence_after();
+            uint32_t pp[64];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t v[32];
+                tmem_ld32(lane_addr + C::COL_A + q4 * 32, v);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int c0 = q4 * 32 + 2 * e;
+                    float a = ex2(fmaf(__uint_as_float(v[2 * e]), sc, -l2));
+                    float b = ex2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -l2));
+                    if (c0 > cmax) a = 0.f;
+                    if (c0 + 1 > cmax) b = 0.f;
+                    pp[q4 * 16 + e] = pack_bf16(a, b);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(B_SF);
+            if (!(ok = mbar_wait(B_DP, jj & 1, ctl, kSiteBwdDP))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t v[32];
+                tmem_ld32(lane_addr + C::COL_B + q4 * 32, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const uint32_t pr = pp[q4 * 16 + e];
+                    pk[e] = pack_bf16(bf_lo(pr) * (__uint_as_float(v[2 * e]) - dl),
+                                      bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dl));
+                }
+                tmem_st16(lane_addr + C::COL_B + q4 * 16, pk);
+            }
+            tc_fence_before();
+            mbar_arrive(B_DS);
+        }
+        if (ok) {
+            const bool have = n > 0;
+            if (have) {
+                ok = mbar_wait(B_ACC, 0, ctl, kSiteBwdDone);
+                tc_fence_after();
+            }
+            if (ok)
+                store_acc_row<D>(lane_addr + C::COL_ACC0, p.dq + ((size_t)bh * p.Nq + (row_ok ? qg : 0)) * D,
+                                 p.scale, row_ok, !have);
+        }
+    }
+    bwd_teardown<D>(tmem);
+}
+
+BwdParams make_params(const BwdLaunch& a) {
+    BwdParams p;
+    p.dq = (__nv_bfloat16*)a.dq;
+    p.dk = (__nv_bfloat16*)a.dk;
+    p.dv = (__nv_bfloat16*)a.dv;
+    p.lse = a.lse;
+    p.delta = a.delta;
+    p.BH = a.B * a.H;
+    p.Nq = a.Nq;
+    p.Nk = a.Nk;
+    p.causal = a.causal;
+    p.n_qt = (a.Nq + 127) / 128;
+    p.n_kt = (a.Nk + 127) / 128;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * kLog2e;
+    p.err = a.err;
+    p.timeout_ns = a.timeout_ns;
+    return p;
+}
+
+template <int D>
+cudaError_t launch_pre_d(const BwdLaunch& a, cudaStream_t s) {
+    const long long rows = (long long)a.B * a.H * a.Nq;
+    bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+        (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, a.delta, rows);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t s) {
+    using C = Bwd<D>;
+    static_assert(C::SMEM <= 232448, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    const BwdParams p = make_params(a);
+    bwd_dkdv_kernel<D><<<p.n_kt * p.BH, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, a.map_do, p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dq_d(const BwdLaunch& a, cudaStream_t s) {
+    using C = Bwd<D>;
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    const BwdParams p = make_params(a);
+    bwd_dq_kernel<D><<<p.n_qt * p.BH, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, a.map_do, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s) {
+    return a.d == 128 ? launch_pre_d<128>(a, s) : launch_pre_d<64>(a, s);
+}
+cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s) {
+    return a.d == 128 ? launch_dkdv_d<128>(a, s) : launch_dkdv_d<64>(a, s);
+}
+cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s) {
+    return a.d == 128 ? launch_dq_d<128>(a, s) : launch_dq_d<64>(a, s);
+}
+
 }  // namespace fa

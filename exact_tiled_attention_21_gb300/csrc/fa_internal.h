@@ -32,8 +32,7 @@ struct BwdLaunch {
     void* dq;
     void* dk;
     void* dv;
-    float* dq_acc;  // fp32 [B,H,Nq,d]
-    float* delta;   // fp32 [B,H,Nq]
+    float* delta;   // fp32 [B,H,Nq] (the workspace)
     int B, H, Nq, Nk, d;
     float scale;
     int causal;
@@ -56,7 +55,9 @@ struct DecodeLaunch {
 
 // Each returns a cudaError_t of the launch (cudaSuccess when queued).
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
-cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t s);
+cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s);   // D = rowsum(dO o O)
+cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s);  // dK, dV
+cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s);    // dQ
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);
 
 // Rows of the forward's CTA work tile (two 128-row softmax tiles).

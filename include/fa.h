@@ -64,8 +64,8 @@ typedef enum {
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int Nq, int Nk, int d, float scale, int causal, void *stream);
 
-/* Bytes of fp32 workspace fa_bwd needs: the dQ accumulator [B,H,Nq,d] and the
- * row terms D [B,H,Nq].  Returns 0 for invalid sizes. */
+/* Bytes of fp32 workspace fa_bwd needs: the row terms D [B,H,Nq] (dQ is
+ * accumulated on chip, in a pass of its own).  Returns 0 for invalid sizes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
 
 /* Backward pass (johe.ru, section "Стадии вычисления", pass 2: gradients are
@@ -74,15 +74,33 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
  * LSE), dO [B,H,Nq,d] the upstream gradient.  Outputs dq [B,H,Nq,d],
  * dk/dv [B,H,Nk,d] bf16.  Steps: D_i = sum_c dO_ic O_ic (fp32); per key tile,
  * S = scale QK^T recomputed, P = exp(S - LSE), dV += P^T dO, dP = dO V^T,
- * dS = P (dP - D), dK += scale dS^T Q, dQ += scale dS K (fp32 accumulate in the
- * workspace), then dQ is rounded to bf16.  workspace must hold at least
+ * dS = P (dP - D), dK += scale dS^T Q; per query tile, dQ += scale dS K.  All
+ * accumulation is fp32 on chip; each gradient is rounded to bf16 once.  The
+ * result is deterministic (no atomics).  workspace must hold at least
  * fa_bwd_workspace_bytes(B,H,Nq,Nk,d) bytes; its contents on entry do not
- * matter.  dQ's fp32 accumulation order is not fixed, so dq may differ in the
- * last bits between runs. */
+ * matter. */
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
            const void *dO, void *dq, void *dk, void *dv,
            int B, int H, int Nq, int Nk, int d, float scale, int causal,
            void *workspace, size_t workspace_bytes, void *stream);
+
+/* The three steps of fa_bwd, for callers that schedule them (or time them)
+ * separately; fa_bwd is exactly these three launches in this order.
+ *  fa_bwd_preprocess: delta [B,H,Nq] fp32 = rowsum(dO o O).
+ *  fa_bwd_dkdv: dk, dv [B,H,Nk,d] from q, k, v, lse, delta, dO; one CTA per
+ *    128-key tile, P and dS rebuilt on chip for every query tile it sees.
+ *  fa_bwd_dq: dq [B,H,Nq,d] from q, k, v, lse, delta, dO; one CTA per
+ *    128-query tile.  dkdv and dq only read delta, so they may run in any
+ *    order (or concurrently) after the preprocess.
+ * Same conventions and errors as fa_bwd. */
+int fa_bwd_preprocess(const void *o, const void *dO, float *delta, int B, int H, int Nq, int d,
+                      void *stream);
+int fa_bwd_dkdv(const void *q, const void *k, const void *v, const float *lse, const float *delta,
+                const void *dO, void *dk, void *dv, int B, int H, int Nq, int Nk, int d, float scale,
+                int causal, void *stream);
+int fa_bwd_dq(const void *q, const void *k, const void *v, const float *lse, const float *delta,
+              const void *dO, void *dq, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+              void *stream);
 
 /* Bytes of fp32 workspace fa_decode needs for num_splits partials (<= 0:
  * the number the library would choose for this Nk).  Returns 0 for invalid

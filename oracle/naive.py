@@ -81,10 +81,16 @@ def forward(q, k, v, scale, causal=False, rows=None, Nq=None, return_p=False):
     return o, lse
 
 
-def backward(q, k, v, do, scale, causal=False):
-    """Gradients (dQ, dK, dV) of O = softmax(scale Q K^T [masked]) V for upstream dO."""
+def backward(q, k, v, do, scale, causal=False, rows=None, Nq=None):
+    """Gradients (dQ, dK, dV) of O = softmax(scale Q K^T [masked]) V for upstream dO.
+
+    With ``rows`` (query indices of the given q / dO rows, ``Nq`` the total query
+    count) the result is the contribution of those query rows only: dQ of those
+    rows, and their share of dK and dV (the full dK, dV are the sums of the
+    shares over any partition of the queries).
+    """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
-    _, _, p = forward(q, k, v, scale, causal, return_p=True)
+    _, _, p = forward(q, k, v, scale, causal, rows=rows, Nq=Nq, return_p=True)
     dv = np.swapaxes(p, -1, -2) @ do
     dp = do @ np.swapaxes(v, -1, -2)
     ds = p * (dp - (p * dp).sum(axis=-1, keepdims=True))

@@ -48,10 +48,20 @@ def check_out(o, lse, o_ref, lse_ref, what="", max_abs=FWD_MAX_ABS):
     return float(err.max()), float(err.mean())
 
 
-def check_grad(g, g_ref, what=""):
+def check_grad(g, g_ref, what="", cancel_scale=None):
+    """max |g - g_ref| <= GRAD_REL * max |g_ref|.
+
+    Where the exact gradient vanishes identically (every query sees a single
+    key, so dS = P (dP - D) = 0 by cancellation), max |g_ref| is 0 and the
+    kernel's result is pure rounding of the cancelling terms; there the error is
+    measured against ``cancel_scale`` = scale * max|dP| * max|K or Q|, the size
+    of those terms.
+    """
     g = np.asarray(g, dtype=np.float64)
     assert np.isfinite(g).all(), "%s: non-finite gradient" % what
-    scale = max(np.abs(g_ref).max(), 1e-30)
-    rel = np.abs(g - g_ref).max() / scale
+    denom = np.abs(g_ref).max()
+    if cancel_scale is not None and denom <= 1e-9 * cancel_scale:
+        denom = cancel_scale
+    rel = np.abs(g - g_ref).max() / max(denom, 1e-30)
     assert rel <= GRAD_REL, "%s: max|dX-ref|/max|ref| = %g" % (what, rel)
     return float(rel)

@@ -31,7 +31,7 @@ def test_status_strings(lib):
 def test_workspace_queries(lib):
     B, H, N, d = 2, 3, 1000, 128
     ws = fa.fa_bwd_workspace_bytes(B, H, N, N, d)
-    assert ws >= B * H * N * d * 4 + B * H * N * 4
+    assert ws >= B * H * N * 4
     assert fa.fa_bwd_workspace_bytes(B, H, N, N, 96) == 0
     assert fa.fa_bwd_workspace_bytes(0, H, N, N, d) == 0
     assert fa.fa_decode_workspace_bytes(32, 32, 4096, 128, 16) >= 32 * 32 * 16 * (128 + 1) * 4

@@ -1,0 +1,88 @@
+"""Backward parity: dQ, dK, dV from the CUDA path (fed with the CUDA forward's
+O and LSE) against the fp64 oracle's exact gradients of the same inputs."""
+import math
+
+import numpy as np
+
+import pytest
+import torch
+
+from exact_tiled_attention_21_gb300 import synthetic as syn
+from oracle import naive
+from tests.parity import check_grad, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(seed, B, H, Nq, Nk, d):
+    return (syn.bhnd(seed, syn.TAG_Q, B, H, Nq, d), syn.bhnd(seed, syn.TAG_K, B, H, Nk, d),
+            syn.bhnd(seed, syn.TAG_V, B, H, Nk, d), syn.bhnd(seed, syn.TAG_DO, B, H, Nq, d))
+
+
+def _run(fa, q, k, v, dO, scale, causal):
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dOd = (t.to(dev) for t in (q, k, v, dO))
+    o, lse = fa.forward(qd, kd, vd, scale=scale, causal=causal)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dOd, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_get_last_device_error()
+    assert st == 0, detail
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+CASES = [
+    (1, 2, 128, 128, 64, False),
+    (1, 2, 128, 128, 64, True),
+    (1, 2, 300, 300, 128, True),
+    (1, 2, 1000, 1000, 128, False),
+    (1, 2, 1000, 1000, 64, True),
+    (2, 2, 513, 257, 128, False),
+    (1, 2, 257, 513, 128, True),
+    (1, 2, 200, 700, 128, True),     # every query sees a prefix of >= 500 keys
+    (1, 2, 700, 200, 128, True),     # the first 500 queries see no key: zero dQ rows
+    (1, 1, 1, 1, 64, False),
+    (1, 2, 1, 300, 128, False),
+    (1, 2, 300, 1, 64, True),
+    (2, 3, 77, 1031, 64, True),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", CASES)
+def test_backward_parity(cuda_lib, B, H, Nq, Nk, d, causal):
+    seed = 500 + Nq * 3 + Nk + d + causal
+    q, k, v, dO = _inputs(seed, B, H, Nq, Nk, d)
+    scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = _run(cuda_lib, q, k, v, dO, scale, causal)
+    rq, rk, rv = naive.backward(f64(q), f64(k), f64(v), f64(dO), scale, causal)
+    tag = "B%d H%d Nq%d Nk%d d%d c%d" % (B, H, Nq, Nk, d, causal)
+    dp_max = np.abs(f64(dO) @ np.swapaxes(f64(v), -1, -2)).max()
+    cancel = scale * dp_max * max(np.abs(f64(k)).max(), np.abs(f64(q)).max())
+    check_grad(f64(dq), rq, "dQ " + tag, cancel_scale=cancel)
+    check_grad(f64(dk), rk, "dK " + tag, cancel_scale=cancel)
+    check_grad(f64(dv), rv, "dV " + tag)
+
+
+def test_backward_deterministic(cuda_lib):
+    """No atomics anywhere: two runs give identical bits."""
+    q, k, v, dO = _inputs(9, 1, 4, 640, 640, 128)
+    a = _run(cuda_lib, q, k, v, dO, 0.088, True)
+    b = _run(cuda_lib, q, k, v, dO, 0.088, True)
+    assert all(torch.equal(x, y) for x, y in zip(a, b))
+
+
+@pytest.mark.parametrize("N", [1024, 2048, 4096, 8192])
+def test_backward_full_size_sweep(cuda_lib, N):
+    """B=1, H=32, d=128, causal, N in the 1k-8k sweep: heads 0 and 31 against the oracle."""
+    cfg = syn.CONFIGS["fwd_bwd_sweep"]
+    B, H, d = cfg["B"], cfg["H"], cfg["d"]
+    seed = cfg["seed"] + N
+    q, k, v, dO = _inputs(seed, B, H, N, N, d)
+    scale = syn.default_scale(d)
+    dq, dk, dv = _run(cuda_lib, q, k, v, dO, scale, True)
+    for h in (0, H - 1):
+        rq, rk, rv = naive.backward(f64(q[0, h]), f64(k[0, h]), f64(v[0, h]), f64(dO[0, h]), scale, True)
+        check_grad(f64(dq[0, h]), rq, "dQ N%d h%d" % (N, h))
+        check_grad(f64(dk[0, h]), rk, "dK N%d h%d" % (N, h))
+        check_grad(f64(dv[0, h]), rv, "dV N%d h%d" % (N, h))
+    for g in (dq, dk, dv):
+        assert torch.isfinite(g.float()).all()

@@ -294,6 +294,23 @@ def test_sampled_rows_match_full():
         np.testing.assert_allclose(ll, lse[:, rows], atol=1e-12)
 
 
+def test_backward_row_shares_add_up():
+    """dK, dV are sums over queries: the shares of a partition of the query
+    rows add up to the full gradient, and each share's dQ rows are the full dQ rows."""
+    Nq, Nk = 23, 17
+    q, k, v, do = (RNG.standard_normal(s) for s in [(2, Nq, 6), (2, Nk, 6), (2, Nk, 6), (2, Nq, 6)])
+    for causal in (False, True):
+        dq, dk, dv = naive.backward(q, k, v, do, 0.7, causal)
+        sk, sv = np.zeros_like(dk), np.zeros_like(dv)
+        for part in ([0, 5, 9], list(range(1, 5)), list(range(10, 23)), [6, 7, 8]):
+            pq, pk, pv = naive.backward(q[:, part], k, v, do[:, part], 0.7, causal, rows=part, Nq=Nq)
+            np.testing.assert_allclose(pq, dq[:, part], atol=1e-12)
+            sk += pk
+            sv += pv
+        np.testing.assert_allclose(sk, dk, atol=1e-12)
+        np.testing.assert_allclose(sv, dv, atol=1e-12)
+
+
 # ---------------------------------------------------------------- mutation check
 def _mutant_forward(kind):
     def fwd(q, k, v, scale, causal=False, return_p=False):
