@@ -123,32 +123,60 @@ class ClockSampler:
                 "power_w_max": max([num(r[4]) or 0 for r in rows if len(r) > 4])}
 
 
+def profiled_traffic(profile, source):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel's source has changed since the capture (its hash no longer matches)."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
+        fields = dict(l.split(":", 1) for l in text.splitlines() if l.startswith(("traffic_bytes", "source_sha")))
+        want = fields["source_sha256_16"].split()[0]
+        src = os.path.join(ROOT, "exact_tiled_attention_21_gb300", "csrc", source)
+        have = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return int(fields["traffic_bytes_per_launch"]) if want == have else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def reduce_max(x, dist=None, device=None):
+    """Max of a host float over all ranks (identity without a process group).
+    The tensor lives on ``device`` (a CUDA device for NCCL, the CPU for gloo)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(work_per_rank, seconds_per_rank, world, dist=None, device=None):
+    """Weak scaling over independent replicas: all ranks' work over the slowest rank's time."""
+    return world * work_per_rank / reduce_max(seconds_per_rank, dist, device)
+
+
 # ------------------------------------------------------------------ CPU oracle timing
 def oracle_sample(seconds, max_rows=None, seed=2):
-    """Time the fp64 oracle (naive materialised fwd + bwd) on query rows of head
-    (0, 0) of the fwd/bwd workload, in batches of 256 rows spread over the
-    sequence, until ``seconds`` of CPU time have passed.  Returns (flops, secs, rows)."""
+    """Time the fp64 oracle (naive materialised fwd + bwd) on 256-row query
+    blocks of the fwd/bwd workload — head (0, 0), then (0, 1), ... — until
+    ``seconds`` of CPU time have passed.  Returns (flops, secs, rows)."""
     import numpy as np
     from exact_tiled_attention_21_gb300 import synthetic as syn
     from oracle import naive
-    q = syn.head(seed, syn.TAG_Q, 0, 0, N, D).double().numpy()
-    k = syn.head(seed, syn.TAG_K, 0, 0, N, D).double().numpy()
-    v = syn.head(seed, syn.TAG_V, 0, 0, N, D).double().numpy()
-    do = syn.head(seed, syn.TAG_DO, 0, 0, N, D).double().numpy()
-    order = np.random.default_rng(seed).permutation(N // 256)
-    flops = 0.0
-    done = 0
-    t0 = time.perf_counter()
-    for blk in order:
-        rows = np.arange(blk * 256, blk * 256 + 256)
-        naive.forward(q[rows], k, v, SCALE, True, rows=rows, Nq=N)
-        naive.backward(q[rows], k, v, do[rows], SCALE, True, rows=rows, Nq=N)
-        vis = (rows + 1).sum()  # causal: row i sees i + 1 keys
-        flops += 4.0 * D * vis * 3.5  # forward + 2.5x backward
-        done += 256
-        if time.perf_counter() - t0 >= seconds or (max_rows and done >= max_rows):
-            break
-    return flops, time.perf_counter() - t0, done
+    flops, done, secs = 0.0, 0, 0.0
+    for h in range(H):
+        q, k, v, do = (syn.head(seed, tag, 0, h, N, D).double().numpy()
+                       for tag in (syn.TAG_Q, syn.TAG_K, syn.TAG_V, syn.TAG_DO))
+        t0 = time.perf_counter()
+        for blk in np.random.default_rng(seed + h).permutation(N // 256):
+            rows = np.arange(blk * 256, blk * 256 + 256)
+            naive.forward(q[rows], k, v, SCALE, True, rows=rows, Nq=N)
+            naive.backward(q[rows], k, v, do[rows], SCALE, True, rows=rows, Nq=N)
+            flops += 4.0 * D * float((rows + 1).sum()) * 3.5  # causal row i sees i+1 keys; fwd + 2.5x bwd
+            done += 256
+            if secs + time.perf_counter() - t0 >= seconds or (max_rows and done >= max_rows):
+                return flops, secs + time.perf_counter() - t0, done
+        secs += time.perf_counter() - t0
+    return flops, secs, done
 
 
 def blas_threads():
@@ -180,8 +208,8 @@ def run_reference(args, rank):
         "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": CONFIG,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "per step: numpy fp64 naive fwd+bwd of 256-row query blocks of head "
-                                   "(0,0), N=8192 causal, for %.1f s (%d rows in all)" % (per_step, tot_r)},
+                         "sample": "per step: numpy fp64 naive fwd+bwd of 256-row query blocks of heads "
+                                   "(0,0), (0,1), ..., N=8192 causal, for %.1f s (%d rows in all)" % (per_step, tot_r)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -274,17 +302,10 @@ def run_ours(args, rank, world, local_rank):
     fwd_ms, pre_ms, dkdv_ms, dq_ms, dec_ms = (c / K for c in comp)
     fb_ms = fwd_ms + pre_ms + dkdv_ms + dq_ms
 
-    def maxall(x):
-        if not dist:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
+    maxall = lambda x: reduce_max(x, dist, dev)
     total_ms = maxall(total_ms)
-    fb_ms_max = maxall(fb_ms)
     dec_ms_max = maxall(dec_ms)
-    value = world * (FWD_FLOPS + BWD_FLOPS) / (fb_ms_max * 1e-3) / 1e12
+    value = replica_throughput(FWD_FLOPS + BWD_FLOPS, fb_ms * 1e-3, world, dist, dev) / 1e12
 
     # ---- end to end through the public API, host buffers, copies inside the timed region
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
@@ -368,7 +389,9 @@ def run_ours(args, rank, world, local_rank):
             "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step loop)" % pk["source"],
             "unit": "TFLOP/s",
             "frac": dkdv_tflops / pk["bf16_sustained"],
-            "traffic": None,
+            "traffic": profiled_traffic("bwd_dkdv_kernel_causal_B1H32N8192.md", "fa_bwd.cu"),
+            "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch; algorithmic "
+                            "bytes are 4 x 64 MiB read (Q, K, V, dO) + 2 x 64 MiB written (dK, dV)",
             "algorithmic_per_launch": "4 of the 5 backward products: 4 * B*H*N*N*d FLOP (causal half of 8 B H N^2 d)",
         },
         "e2e": {"value": world * (FWD_FLOPS + BWD_FLOPS) / (e2e_fb * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -382,8 +405,8 @@ def run_ours(args, rank, world, local_rank):
         f, t, r = oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": f / t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": "numpy fp64 naive fwd+bwd of %d query rows (256-row blocks spread over the "
-                      "sequence) of head (0,0), N=8192 causal, %.1f s" % (r, t)}
+            "sample": "numpy fp64 naive fwd+bwd of %d query rows (256-row blocks of heads (0,0), "
+                      "(0,1), ...), N=8192 causal, %.1f s" % (r, t)}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
