@@ -179,6 +179,18 @@ def fa_decode(q, kcache, vcache, o, lse, B, H, Nk, d, scale, num_splits, workspa
                             int(workspace_bytes), _stream(stream)), "fa_decode")
 
 
+def fa_decode_noalloc(q, kcache, vcache, o, lse, B, H, Nk, d, scale, num_splits, stream=None):
+    """fa_decode without a workspace: the partials go to the library's fixed
+    scratch array (for callers that may not allocate; see include/fa.h)."""
+    fn = load().fa_decode_noalloc
+    if fn.argtypes is None:
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        fn.argtypes = [vp] * 5 + [i, i, i, i, ctypes.c_float, i, vp]
+        fn.restype = ctypes.c_int
+    _raise(fn(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(o), _ptr(lse), B, H, Nk, d, float(scale),
+              int(num_splits), _stream(stream)), "fa_decode_noalloc")
+
+
 # ------------------------------------------------------------------ conveniences
 def _check(t, name, shape):
     if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):

@@ -324,3 +324,57 @@ int fa_get_last_device_error(void* stream, int* detail) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- decode without a workspace
+// fa_decode_noalloc: the split partials live in one fixed array compiled into
+// the library, for callers that may not allocate device memory (see fa.h).
+// In host code the name of the array is only a stand-in; its device address
+// comes from cudaGetSymbolAddress, looked up once per device with that device
+// current, and is what the kernels receive.
+static __device__ __align__(256) unsigned char g_fa_decode_scratch[FA_DECODE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_addr[fa::kMaxDevices] = {};
+}  // namespace
+
+extern "C" int fa_decode_noalloc(const void* q, const void* kcache, const void* vcache, void* o, float* lse,
+                                 int B, int H, int Nk, int d, float scale, int num_splits, void* stream) {
+    if (!q || !kcache || !vcache || !o) return FA_ERR_INVALID_ARG;
+    if (!scale_ok(scale) || num_splits > 256) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, 1, Nk, d);
+    if (st != FA_OK) return st;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+        (lse && !aligned16(lse)))
+        return FA_ERR_ALIGNMENT;
+    const int splits = num_splits <= 0 ? decode_auto_splits(Nk) : num_splits;
+    if (decode_ws_bytes(B, H, d, splits) > FA_DECODE_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (!g_scratch_addr[dev]) {
+            void* addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_fa_decode_scratch) != cudaSuccess || !addr) return FA_ERR_CUDA;
+            g_scratch_addr[dev] = addr;
+        }
+        scratch = g_scratch_addr[dev];
+    }
+    DecodeLaunch a;
+    a.q = q;
+    a.kc = kcache;
+    a.vc = vcache;
+    a.o = o;
+    a.lse = lse;
+    a.part_o = static_cast<float*>(scratch);
+    a.part_lse = a.part_o + (size_t)B * H * splits * d;  // same layout as the fa_decode workspace
+    a.B = B;
+    a.H = H;
+    a.Nk = Nk;
+    a.d = d;
+    a.splits = splits;
+    a.chunk = (Nk + splits - 1) / splits;
+    a.scale = scale;
+    return launch_decode(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

@@ -122,6 +122,34 @@ int fa_decode(const void *q, const void *kcache, const void *vcache, void *o, fl
               int B, int H, int Nk, int d, float scale, int num_splits,
               void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the scratch array that fa_decode_noalloc uses instead of a workspace. */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* Split-KV decode exactly like fa_decode, for callers that cannot allocate
+ * device memory when they need a decode step.  Examples: a serving loop or
+ * plugin host that hands this library only its input and output buffers and
+ * owns every other byte of device memory; a real-time path that must never
+ * call the allocator, because cudaMalloc/cudaFree may synchronise the whole
+ * device and may fail once memory is fragmented; C callers with no access to
+ * the framework allocator that owns the tensors.
+ * Not a step of the method: the pages have no counterpart; it only changes
+ * where the split partials live.  Instead of a caller workspace, the partials
+ * go to one fixed array of FA_DECODE_NOALLOC_SCRATCH_BYTES compiled into the
+ * library (every GPU that loads the library holds it until the process exits).
+ * Arguments mean what they mean for fa_decode; the caller still passes q, the
+ * caches, o and (optionally) lse.  A problem whose partials would need more
+ * than the array (fa_decode_workspace_bytes(B,H,Nk,d,num_splits) >
+ * FA_DECODE_NOALLOC_SCRATCH_BYTES) is rejected with FA_ERR_WORKSPACE before
+ * anything is launched.  The call allocates nothing.  The first call on each
+ * device looks up the array's device address (with that device current) and
+ * caches it; make that first call before any stream capture.  All calls share
+ * the one array: calls that may overlap on the GPU (different streams, no
+ * ordering between them) race on it, so order them.  Nothing in the array has
+ * to start at zero (every partial is written before it is read), and it keeps
+ * the last call's partials. */
+int fa_decode_noalloc(const void *q, const void *kcache, const void *vcache, void *o, float *lse,
+                      int B, int H, int Nk, int d, float scale, int num_splits, void *stream);
+
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device.  Returns FA_OK, FA_ERR_TIMEOUT (a bounded wait ran out), or
  * FA_ERR_CUDA if synchronising or reading failed.  If `detail` is not NULL it
