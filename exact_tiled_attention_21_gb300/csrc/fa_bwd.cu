@@ -38,7 +38,8 @@ struct Bwd {
     static constexpr int NBAR = 12;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;
-    static constexpr int THREADS = 192;  // warps 0-3 compute, 4 producer, 5 MMA
+    static constexpr int THREADS = 320;  // warps 0-7 compute (two warpgroups), 8 producer, 9 MMA
+    static constexpr int PRODUCER = 8, MMA = 9;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_A = 0;      // S / S^T fp32; P^T bf16 over its first 64 columns
     static constexpr uint32_t COL_B = 128;    // dP / dP^T fp32; dS / dS^T bf16 over its first 64
@@ -99,21 +100,27 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t sA, uint32_t 
     }
 }
 
-// Issue C[tmem] (+)= A[tmem, 128 x 128 bf16] B[smem, 128 x D, MN-major].
+// Issue C[tmem] (+)= A[tmem, 128 x 128 bf16] B[smem, 128 x D, MN-major].  The
+// two compute warpgroups write the bf16 A operand in two halves, K = 0..63 at
+// columns a_tmem + [0, 32) and K = 64..127 at a_tmem + [64, 96), each over the
+// fp32 columns that warpgroup has itself already read.
 template <int D>
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, bool acc) {
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-        mma_ts(d_tmem, a_tmem + k * 8, sdesc_sw128(sB + k * 2048, Bwd<D>::CHUNK, 1024),
+        mma_ts(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), sdesc_sw128(sB + k * 2048, Bwd<D>::CHUNK, 1024),
                Bwd<D>::IDESC_TS, (acc || k > 0) ? 1u : 0u);
 }
 
-// Writes a 128-row accumulator row (thread = row) scaled by `mul` as bf16.
+// Writes columns [c0, c0 + D/2) of a 128-row accumulator row (thread = row)
+// scaled by `mul` as bf16; each compute warpgroup stores its half.
 template <int D>
 __device__ __forceinline__ void store_acc_row(uint32_t taddr, __nv_bfloat16* dst, float mul, bool valid,
-                                              bool zero) {
+                                              bool zero, int c0) {
+    taddr += c0;
+    dst += c0;
 #pragma unroll 1
-    for (int q4 = 0; q4 < D / 32; ++q4) {
+    for (int q4 = 0; q4 < D / 64; ++q4) {
         uint32_t v[32];
         if (!zero) {
             tmem_ld32(taddr + q4 * 32, v);
@@ -145,7 +152,7 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t bar0, cons
         fence_mbar_init();
         if ((smem_u32(smem) & 1023u) != 0) record_error(ctl, kErrTimeout, kSiteAlign, 0);
     }
-    if (warp == 5) {
+    if (warp == Bwd<D>::MMA) {
         tmem_alloc(smem_u32(tmem_slot), Bwd<D>::TMEM_COLS);
         tmem_relinquish();
     }
@@ -160,7 +167,7 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if ((threadIdx.x >> 5) == 5) {
+    if ((threadIdx.x >> 5) == Bwd<D>::MMA) {
         __syncwarp();
         tmem_dealloc(tmem, Bwd<D>::TMEM_COLS);
     }
@@ -180,14 +187,16 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // barriers
     const uint32_t B_KV = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_DP = bar0 + 48,
                    B_P = bar0 + 56, B_DS = bar0 + 64, B_ACC = bar0 + 72, B_TD = bar0 + 80;
-    const uint32_t counts[11] = {1, 32, 32, 1, 1, 1, 1, 128, 128, 1, 1};
+    const uint32_t counts[11] = {1, 32, 32, 1, 1, 1, 1, 256, 256, 1, 1};
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
     const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 11);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kt = blockIdx.x / p.BH;  // causal: small key tiles see the most queries: heavy first
-    const int bh = blockIdx.x - kt * p.BH;
+    // head-major, so the CTAs in flight share one head's Q / dO in L2; within a
+    // head, key tile 0 (the most query tiles when causal) first
+    const int bh = blockIdx.x / p.n_kt;
+    const int kt = blockIdx.x - bh * p.n_kt;
     const int off = p.Nk - p.Nq;
     int i0 = 0;
     if (p.causal) {
@@ -200,7 +209,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     auto sDO = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
     float* vec = (float*)(smem + C::OFF_VEC);  // stage s: lse2 at [s*256], delta at [s*256 + 128]
 
-    if (warp == 4) {
+    if (warp == C::PRODUCER) {
         // ------------------------------------------------------------ producer (whole warp)
         if (!*abort_flag && n > 0) {
             const uint64_t pol = l2_policy_evict_last();
@@ -246,7 +255,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     if (issued & (1u << st)) mbar_drain(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == C::MMA) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && !*abort_flag && n > 0) {
             bool ok = mbar_wait(B_KV, 0, ctl, kSiteBwdKvFull);
@@ -287,25 +296,28 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
     } else {
         // ------------------------------------------------------------ P^T, dS^T, epilogue
+        // Two warpgroups: warpgroup h handles query columns [64h, 64h + 64) of every key row.
+        const int h = warp >> 2;
         const int r = ((warp & 3) << 5) + lane;  // key row within the tile = TMEM lane
         const int kg = kt * 128 + r;
         const bool row_ok = kg < p.Nk;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t colA = C::COL_A + 64 * h, colB = C::COL_B + 64 * h;
         const float sc = p.scale_log2;
         bool ok = true;
         for (int ii = 0; ii < n; ++ii) {
             const int st = ii & 1, i = i0 + ii;
-            const float* l2 = vec + st * 256;
+            const float* l2 = vec + st * 256 + 64 * h;
             const float* dl = l2 + 128;
             // key kg is visible to query q iff kg <= q + off, i.e. column c >= cmin
-            const int cmin = p.causal ? kg - off - i * 128 : -1;
+            const int cmin = p.causal ? kg - off - i * 128 - 64 * h : -1;
             if (!(ok = mbar_wait(B_S, ii & 1, ctl, kSiteBwdS))) break;
             tc_fence_after();
-            uint32_t pp[64];
+            uint32_t pp[32];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q4 = 0; q4 < 2; ++q4) {
                 uint32_t v[32];
-                tmem_ld32(lane_addr + C::COL_A + q4 * 32, v);
+                tmem_ld32(lane_addr + colA + q4 * 32, v);
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -317,16 +329,16 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     pk[e] = pack_bf16(a, b);
                     pp[q4 * 16 + e] = pk[e];
                 }
-                tmem_st16(lane_addr + C::COL_A + q4 * 16, pk);
+                tmem_st16(lane_addr + colA + q4 * 16, pk);
             }
             tc_fence_before();
             mbar_arrive(B_P);
             if (!(ok = mbar_wait(B_DP, ii & 1, ctl, kSiteBwdDP))) break;
             tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q4 = 0; q4 < 2; ++q4) {
                 uint32_t v[32];
-                tmem_ld32(lane_addr + C::COL_B + q4 * 32, v);
+                tmem_ld32(lane_addr + colB + q4 * 32, v);
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -336,7 +348,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     const float b = bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dl[c0 + 1]);
                     pk[e] = pack_bf16(a, b);
                 }
-                tmem_st16(lane_addr + C::COL_B + q4 * 16, pk);
+                tmem_st16(lane_addr + colB + q4 * 16, pk);
             }
             tc_fence_before();
             mbar_arrive(B_DS);
@@ -349,8 +361,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
             if (ok) {
                 const size_t base = ((size_t)bh * p.Nk + (row_ok ? kg : 0)) * D;
-                store_acc_row<D>(lane_addr + C::COL_ACC0, p.dv + base, 1.f, row_ok, !have);
-                store_acc_row<D>(lane_addr + C::COL_ACC1, p.dk + base, p.scale, row_ok, !have);
+                store_acc_row<D>(lane_addr + C::COL_ACC0, p.dv + base, 1.f, row_ok, !have, h * (D / 2));
+                store_acc_row<D>(lane_addr + C::COL_ACC1, p.dk + base, p.scale, row_ok, !have, h * (D / 2));
             }
         }
     }
@@ -370,14 +382,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const uint32_t bar0 = s_base + C::OFF_BAR;
     const uint32_t B_Q = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_SF = bar0 + 48,
                    B_DP = bar0 + 56, B_DS = bar0 + 64, B_ACC = bar0 + 72, B_TD = bar0 + 80;
-    const uint32_t counts[11] = {1, 1, 1, 1, 1, 1, 128, 1, 128, 1, 1};
+    const uint32_t counts[11] = {1, 1, 1, 1, 1, 1, 256, 1, 256, 1, 1};
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
     const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 11);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int mr = blockIdx.x / p.BH;
-    const int bh = blockIdx.x - mr * p.BH;
+    const int bh = blockIdx.x / p.n_qt;  // head-major (K / V of one head shared in L2)
+    const int mr = blockIdx.x - bh * p.n_qt;
     const int it = p.causal ? p.n_qt - 1 - mr : mr;  // causal: late query tiles (most keys) first
     const int off = p.Nk - p.Nq;
     int n = p.n_kt;
@@ -390,7 +402,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     auto sK = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
     auto sV = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
 
-    if (warp == 4) {
+    if (warp == C::PRODUCER) {
         if (lane == 0 && !*abort_flag && n > 0) {
             const uint64_t pol = l2_policy_evict_last();
             tma_prefetch_desc(&map_k);
@@ -418,7 +430,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                     if (issued & (1u << st)) mbar_drain(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == C::MMA) {
         if (lane == 0 && !*abort_flag && n > 0) {
             bool ok = mbar_wait(B_Q, 0, ctl, kSiteBwdQFull);
             if (ok) ok = mbar_wait(B_STF, 0, ctl, kSiteBwdKvFull);
@@ -455,10 +467,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             }
         }
     } else {
+        // Two warpgroups: warpgroup h handles key columns [64h, 64h + 64) of every query row.
+        const int h = warp >> 2;
         const int r = ((warp & 3) << 5) + lane;  // query row within the tile = TMEM lane
         const int qg = it * 128 + r;
         const bool row_ok = qg < p.Nq;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t colA = C::COL_A + 64 * h, colB = C::COL_B + 64 * h;
         float l2 = INFINITY, dl = 0.f;
         if (row_ok) {
             const float L = p.lse[(size_t)bh * p.Nq + qg];
@@ -469,14 +484,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const int lim_row = p.causal ? min(qg + off, p.Nk - 1) : p.Nk - 1;  // last key this row sees
         bool ok = true;
         for (int jj = 0; jj < n; ++jj) {
-            const int cmax = lim_row - jj * 128;  // columns > cmax are masked
+            const int cmax = lim_row - jj * 128 - 64 * h;  // columns > cmax are masked
             if (!(ok = mbar_wait(B_S, jj & 1, ctl, kSiteBwdS))) break;
             tc_fence_after();
-            uint32_t pp[64];
+            uint32_t pp[32];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q4 = 0; q4 < 2; ++q4) {
                 uint32_t v[32];
-                tmem_ld32(lane_addr + C::COL_A + q4 * 32, v);
+                tmem_ld32(lane_addr + colA + q4 * 32, v);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int c0 = q4 * 32 + 2 * e;
@@ -492,9 +507,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             if (!(ok = mbar_wait(B_DP, jj & 1, ctl, kSiteBwdDP))) break;
             tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q4 = 0; q4 < 2; ++q4) {
                 uint32_t v[32];
-                tmem_ld32(lane_addr + C::COL_B + q4 * 32, v);
+                tmem_ld32(lane_addr + colB + q4 * 32, v);
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -502,7 +517,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                     pk[e] = pack_bf16(bf_lo(pr) * (__uint_as_float(v[2 * e]) - dl),
                                       bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dl));
                 }
-                tmem_st16(lane_addr + C::COL_B + q4 * 16, pk);
+                tmem_st16(lane_addr + colB + q4 * 16, pk);
             }
             tc_fence_before();
             mbar_arrive(B_DS);
@@ -515,7 +530,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             }
             if (ok)
                 store_acc_row<D>(lane_addr + C::COL_ACC0, p.dq + ((size_t)bh * p.Nq + (row_ok ? qg : 0)) * D,
-                                 p.scale, row_ok, !have);
+                                 p.scale, row_ok, !have, h * (D / 2));
         }
     }
     bwd_teardown<D>(tmem);

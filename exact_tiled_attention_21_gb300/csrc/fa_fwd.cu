@@ -297,10 +297,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     uint32_t v[32];
                     tmem_ld32(lane_addr + col_s + q4 * 32, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x = __uint_as_float(v[i]);
-                        if (masked && kbase + q4 * 32 + i > lim) x = -INFINITY;
-                        mraw = fmaxf(mraw, x);
+                    for (int i = 0; i < 32; i += 2) {
+                        float x0 = __uint_as_float(v[i]), x1 = __uint_as_float(v[i + 1]);
+                        if (masked) {
+                            if (kbase + q4 * 32 + i > lim) x0 = -INFINITY;
+                            if (kbase + q4 * 32 + i + 1 > lim) x1 = -INFINITY;
+                        }
+                        mraw = fmax3(mraw, x0, x1);
                     }
                 }
                 const float m_new = fmaxf(m_use, mraw * c);
@@ -322,7 +325,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 }
                 const float msub = (m_use == -INFINITY) ? 0.f : m_use;
                 // pass 2: p = 2^(s*c - m), row sum, bf16 P over the S columns already read
-                float rs0 = 0.f, rs1 = 0.f;
+                float2 rs = make_float2(0.f, 0.f);
+                const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
 #pragma unroll 1
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t v[32];
@@ -335,14 +339,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                             if (kbase + q4 * 32 + 2 * i > lim) s0 = -INFINITY;
                             if (kbase + q4 * 32 + 2 * i + 1 > lim) s1 = -INFINITY;
                         }
-                        const float a = ex2(fmaf(s0, c, -msub));
-                        const float b = ex2(fmaf(s1, c, -msub));
-                        rs0 += a;
-                        rs1 += b;
-                        pk[i] = pack_bf16(a, b);
+                        const float2 x = ffma2(make_float2(s0, s1), c2, nm2);  // s*c - m, two lanes
+                        const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                        rs = fadd2(rs, e);
+                        pk[i] = pack_bf16(e.x, e.y);
                     }
                     tmem_st16(lane_addr + col_s + q4 * 16, pk);
                 }
+                const float rs0 = rs.x, rs1 = rs.y;
                 l += rs0 + rs1;
                 tc_fence_before();
                 mbar_arrive(bar_p);

@@ -268,6 +268,30 @@ __device__ __forceinline__ float lg2(float x) {
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// max(a, b, c) in one instruction (sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Two fp32 lanes per instruction (sm_100 family): {a.x*b.x + c.x, a.y*b.y + c.y}.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    const uint64_t A = ((uint64_t)__float_as_uint(a.y) << 32) | __float_as_uint(a.x);
+    const uint64_t B = ((uint64_t)__float_as_uint(b.y) << 32) | __float_as_uint(b.x);
+    const uint64_t C = ((uint64_t)__float_as_uint(c.y) << 32) | __float_as_uint(c.x);
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(A), "l"(B), "l"(C));
+    return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    const uint64_t A = ((uint64_t)__float_as_uint(a.y) << 32) | __float_as_uint(a.x);
+    const uint64_t B = ((uint64_t)__float_as_uint(b.y) << 32) | __float_as_uint(b.x);
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(A), "l"(B));
+    return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
