@@ -21,6 +21,8 @@
 // In both, one thread per TMEM lane (the 128 rows of the tile) computes P
 // and dS; P stays in registers (packed bf16) so the next score MMA can be
 // issued while dS is being formed.
+#include <type_traits>
+
 #include "fa_internal.h"
 
 namespace fa {
@@ -314,42 +316,74 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             if (!(ok = mbar_wait(B_S, ii & 1, ctl, kSiteBwdS))) break;
             tc_fence_after();
             uint32_t pp[32];
+            uint32_t va[32], vb[32];  // chunk 1 loads while chunk 0 is processed
+            // masked entries: rows past Nk (whole row) and, causal, columns c < cmin.
+            // Tiles with none in the warp take the instantiation without the test.
+            const int cmin_eff = row_ok ? cmin : (1 << 30);
+            auto p_phase = [&](auto MASK) {
+            tmem_ld32_async(lane_addr + colA, va);
+            tmem_wait_ld(va);
+            tmem_ld32_async(lane_addr + colA + 32, vb);
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + colA + q4 * 32, v);
+                uint32_t(&v)[32] = q4 ? vb : va;
+                if (q4) tmem_wait_ld(vb);
+                float lv[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 t = reinterpret_cast<const float4*>(l2 + q4 * 32)[e];
+                    lv[4 * e] = t.x, lv[4 * e + 1] = t.y, lv[4 * e + 2] = t.z, lv[4 * e + 3] = t.w;
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int c0 = q4 * 32 + 2 * e;
-                    float a = ex2(fmaf(__uint_as_float(v[2 * e]), sc, -l2[c0]));
-                    float b = ex2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -l2[c0 + 1]));
-                    if (!row_ok || c0 < cmin) a = 0.f;
-                    if (!row_ok || c0 + 1 < cmin) b = 0.f;
+                    const float2 x = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                           make_float2(sc, sc), make_float2(-lv[2 * e], -lv[2 * e + 1]));
+                    float a = ex2(x.x), b = ex2(x.y);
+                    if constexpr (decltype(MASK)::value) {
+                        if (c0 < cmin_eff) a = 0.f;
+                        if (c0 + 1 < cmin_eff) b = 0.f;
+                    }
                     pk[e] = pack_bf16(a, b);
                     pp[q4 * 16 + e] = pk[e];
                 }
-                tmem_st16(lane_addr + colA + q4 * 16, pk);
+                tmem_st16_async(lane_addr + colA + q4 * 16, pk);
             }
+            tmem_wait_st();
+            };
+            if (__any_sync(0xffffffffu, cmin_eff > 0))
+                p_phase(std::true_type{});
+            else
+                p_phase(std::false_type{});
             tc_fence_before();
             mbar_arrive(B_P);
             if (!(ok = mbar_wait(B_DP, ii & 1, ctl, kSiteBwdDP))) break;
             tc_fence_after();
+            tmem_ld32_async(lane_addr + colB, va);
+            tmem_wait_ld(va);
+            tmem_ld32_async(lane_addr + colB + 32, vb);
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + colB + q4 * 32, v);
+                uint32_t(&v)[32] = q4 ? vb : va;
+                if (q4) tmem_wait_ld(vb);
+                float dv[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 t = reinterpret_cast<const float4*>(dl + q4 * 32)[e];
+                    dv[4 * e] = t.x, dv[4 * e + 1] = t.y, dv[4 * e + 2] = t.z, dv[4 * e + 3] = t.w;
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int c0 = q4 * 32 + 2 * e;
                     const uint32_t pr = pp[q4 * 16 + e];
-                    const float a = bf_lo(pr) * (__uint_as_float(v[2 * e]) - dl[c0]);
-                    const float b = bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dl[c0 + 1]);
+                    const float a = bf_lo(pr) * (__uint_as_float(v[2 * e]) - dv[2 * e]);
+                    const float b = bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dv[2 * e + 1]);
                     pk[e] = pack_bf16(a, b);
                 }
-                tmem_st16(lane_addr + colB + q4 * 16, pk);
+                tmem_st16_async(lane_addr + colB + q4 * 16, pk);
             }
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(B_DS);
         }
@@ -488,28 +522,46 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             if (!(ok = mbar_wait(B_S, jj & 1, ctl, kSiteBwdS))) break;
             tc_fence_after();
             uint32_t pp[32];
+            uint32_t va[32], vb[32];  // chunk 1 loads while chunk 0 is processed
+            // masked entries: columns c > cmax (keys past Nk or, causal, past the
+            // row's limit); tiles with none in the warp skip the test.
+            auto p_phase = [&](auto MASK) {
+            tmem_ld32_async(lane_addr + colA, va);
+            tmem_wait_ld(va);
+            tmem_ld32_async(lane_addr + colA + 32, vb);
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + colA + q4 * 32, v);
+                uint32_t(&v)[32] = q4 ? vb : va;
+                if (q4) tmem_wait_ld(vb);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int c0 = q4 * 32 + 2 * e;
-                    float a = ex2(fmaf(__uint_as_float(v[2 * e]), sc, -l2));
-                    float b = ex2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -l2));
-                    if (c0 > cmax) a = 0.f;
-                    if (c0 + 1 > cmax) b = 0.f;
+                    const float2 x = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                           make_float2(sc, sc), make_float2(-l2, -l2));
+                    float a = ex2(x.x), b = ex2(x.y);
+                    if constexpr (decltype(MASK)::value) {
+                        if (c0 > cmax) a = 0.f;
+                        if (c0 + 1 > cmax) b = 0.f;
+                    }
                     pp[q4 * 16 + e] = pack_bf16(a, b);
                 }
             }
+            };
+            if (__any_sync(0xffffffffu, cmax < 63))
+                p_phase(std::true_type{});
+            else
+                p_phase(std::false_type{});
             tc_fence_before();
             mbar_arrive(B_SF);
             if (!(ok = mbar_wait(B_DP, jj & 1, ctl, kSiteBwdDP))) break;
             tc_fence_after();
+            tmem_ld32_async(lane_addr + colB, va);
+            tmem_wait_ld(va);
+            tmem_ld32_async(lane_addr + colB + 32, vb);
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + colB + q4 * 32, v);
+                uint32_t(&v)[32] = q4 ? vb : va;
+                if (q4) tmem_wait_ld(vb);
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -517,8 +569,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                     pk[e] = pack_bf16(bf_lo(pr) * (__uint_as_float(v[2 * e]) - dl),
                                       bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dl));
                 }
-                tmem_st16(lane_addr + colB + q4 * 16, pk);
+                tmem_st16_async(lane_addr + colB + q4 * 16, pk);
             }
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(B_DS);
         }

@@ -80,6 +80,70 @@ __device__ __forceinline__ void fwd_decode(const FwdParams& p, int w, int& bh, i
     row0 = m * kFwdRowsPerCta;
 }
 
+// Pass 1 over one 128-column S row in TMEM (thread = row): the maximum of the
+// raw scores.  Chunks of 32 columns are double-buffered (the next loads while
+// this one is scanned).  MASKED: columns c > lim2 are excluded; instantiated
+// only for the blocks that hold a masked column.
+template <bool MASKED>
+__device__ __forceinline__ float row_max_pass(uint32_t taddr, int lim2) {
+    float mraw = -INFINITY;
+    uint32_t va[32], vb[32];
+    tmem_ld32_async(taddr, va);
+    tmem_wait_ld(va);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t(&v)[32] = (q4 & 1) ? vb : va;
+        uint32_t(&nx)[32] = (q4 & 1) ? va : vb;
+        if (q4 + 1 < 4) tmem_ld32_async(taddr + (q4 + 1) * 32, nx);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            float x0 = __uint_as_float(v[i]), x1 = __uint_as_float(v[i + 1]);
+            if constexpr (MASKED) {
+                if (q4 * 32 + i > lim2) x0 = -INFINITY;
+                if (q4 * 32 + i + 1 > lim2) x1 = -INFINITY;
+            }
+            mraw = fmax3(mraw, x0, x1);
+        }
+        if (q4 + 1 < 4) tmem_wait_ld(nx);
+    }
+    return mraw;
+}
+
+// Pass 2: p = 2^(s c - m) for the 128 columns, their sum, and bf16 P written
+// over the S columns already read (keys [32 q, 32 q + 32) to columns
+// [16 q, 16 q + 16); the load in flight is always of columns >= 32 (q + 1)).
+template <bool MASKED>
+__device__ __forceinline__ float exp_pass(uint32_t taddr, int lim2, float c, float msub) {
+    float2 rs = make_float2(0.f, 0.f);
+    const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
+    uint32_t va[32], vb[32];
+    tmem_ld32_async(taddr, va);
+    tmem_wait_ld(va);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t(&v)[32] = (q4 & 1) ? vb : va;
+        uint32_t(&nx)[32] = (q4 & 1) ? va : vb;
+        if (q4 + 1 < 4) tmem_ld32_async(taddr + (q4 + 1) * 32, nx);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float s0 = __uint_as_float(v[2 * i]), s1 = __uint_as_float(v[2 * i + 1]);
+            if constexpr (MASKED) {
+                if (q4 * 32 + 2 * i > lim2) s0 = -INFINITY;
+                if (q4 * 32 + 2 * i + 1 > lim2) s1 = -INFINITY;
+            }
+            const float2 x = ffma2(make_float2(s0, s1), c2, nm2);  // s*c - m, two lanes
+            const float2 e = make_float2(ex2(x.x), ex2(x.y));
+            rs = fadd2(rs, e);
+            pk[i] = pack_bf16(e.x, e.y);
+        }
+        tmem_st16_async(taddr + q4 * 16, pk);
+        if (q4 + 1 < 4) tmem_wait_ld(nx);
+    }
+    tmem_wait_st();
+    return rs.x + rs.y;
+}
+
 template <int D>
 __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -291,21 +355,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 const int kbase = j * 128;
                 const bool masked = kbase + 128 > p.Nk || (p.causal && kbase + 127 > tile_row0 + off);
                 const int lim = p.causal ? min(row + off, p.Nk - 1) : p.Nk - 1;
-                float mraw = -INFINITY;
-#pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t v[32];
-                    tmem_ld32(lane_addr + col_s + q4 * 32, v);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float x0 = __uint_as_float(v[i]), x1 = __uint_as_float(v[i + 1]);
-                        if (masked) {
-                            if (kbase + q4 * 32 + i > lim) x0 = -INFINITY;
-                            if (kbase + q4 * 32 + i + 1 > lim) x1 = -INFINITY;
-                        }
-                        mraw = fmax3(mraw, x0, x1);
-                    }
-                }
+                const int lim2 = lim - kbase;  // last visible column of this block
+                // uniform over the warpgroup: masked blocks take the instantiation with the mask
+                const float mraw = masked ? row_max_pass<true>(lane_addr + col_s, lim2)
+                                          : row_max_pass<false>(lane_addr + col_s, lim2);
                 const float m_new = fmaxf(m_use, mraw * c);
                 if (j == 0) {
                     m_use = m_new;
@@ -325,29 +378,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 }
                 const float msub = (m_use == -INFINITY) ? 0.f : m_use;
                 // pass 2: p = 2^(s*c - m), row sum, bf16 P over the S columns already read
-                float2 rs = make_float2(0.f, 0.f);
-                const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
-#pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t v[32];
-                    tmem_ld32(lane_addr + col_s + q4 * 32, v);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float s0 = __uint_as_float(v[2 * i]), s1 = __uint_as_float(v[2 * i + 1]);
-                        if (masked) {
-                            if (kbase + q4 * 32 + 2 * i > lim) s0 = -INFINITY;
-                            if (kbase + q4 * 32 + 2 * i + 1 > lim) s1 = -INFINITY;
-                        }
-                        const float2 x = ffma2(make_float2(s0, s1), c2, nm2);  // s*c - m, two lanes
-                        const float2 e = make_float2(ex2(x.x), ex2(x.y));
-                        rs = fadd2(rs, e);
-                        pk[i] = pack_bf16(e.x, e.y);
-                    }
-                    tmem_st16(lane_addr + col_s + q4 * 16, pk);
-                }
-                const float rs0 = rs.x, rs1 = rs.y;
-                l += rs0 + rs1;
+                const float rsum = masked ? exp_pass<true>(lane_addr + col_s, lim2, c, msub)
+                                          : exp_pass<false>(lane_addr + col_s, lim2, c, msub);
+                l += rsum;
                 tc_fence_before();
                 mbar_arrive(bar_p);
             }
