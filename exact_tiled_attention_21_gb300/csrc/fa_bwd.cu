@@ -225,31 +225,43 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 }
             }
             uint32_t issued = 0, issued_par = 0;
+            // per-column LSE*log2(e) and D of query tile i (4 values of each per lane),
+            // read from global memory one tile ahead so the load latency is off the
+            // path from "stage free" to "TMA issued"
+            float nl2[4], ndl[4];
+            auto fetch_vec = [&](int i) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int q = i * 128 + lane + 32 * t;
+                    nl2[t] = INFINITY;
+                    ndl[t] = 0.f;
+                    if (q < p.Nq) {
+                        const float L = p.lse[(size_t)bh * p.Nq + q];
+                        nl2[t] = (L == -INFINITY) ? INFINITY : L * kLog2e;
+                        ndl[t] = p.delta[(size_t)bh * p.Nq + q];
+                    }
+                }
+            };
+            fetch_vec(i0);
             for (int ii = 0; ii < n; ++ii) {
                 const int st = ii & 1, i = i0 + ii;
                 if (!mbar_wait(B_STE + 8 * st, ((ii >> 1) & 1) ^ 1, ctl, kSiteBwdQEmpty)) break;
-                for (int e = lane; e < 128; e += 32) {
-                    const int q = i * 128 + e;
-                    float l2 = INFINITY, dl = 0.f;
-                    if (q < p.Nq) {
-                        const float L = p.lse[(size_t)bh * p.Nq + q];
-                        l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
-                        dl = p.delta[(size_t)bh * p.Nq + q];
-                    }
-                    vec[st * 256 + e] = l2;
-                    vec[st * 256 + 128 + e] = dl;
-                }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(B_STF + 8 * st, 2 * C::TILE);
+                if (lane == 0) {  // byte count first (no arrival), then the copies
+                    mbar_expect_tx(B_STF + 8 * st, 2 * C::TILE);
                     for (int c = 0; c < C::KCH; ++c) {
                         tma_load_3d(sQ(st) + c * C::CHUNK, &map_q, B_STF + 8 * st, c * 64, i * 128, bh, pol);
                         tma_load_3d(sDO(st) + c * C::CHUNK, &map_do, B_STF + 8 * st, c * 64, i * 128, bh, pol);
                     }
-                } else {
-                    mbar_arrive(B_STF + 8 * st);
                 }
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    vec[st * 256 + lane + 32 * t] = nl2[t];
+                    vec[st * 256 + 128 + lane + 32 * t] = ndl[t];
+                }
+                mbar_arrive(B_STF + 8 * st);  // all 32 lanes, after their writes
                 issued |= 1u << st;
                 issued_par = (issued_par & ~(1u << st)) | ((uint32_t)((ii >> 1) & 1) << st);
+                if (ii + 1 < n) fetch_vec(i + 1);
             }
             if (*abort_flag && lane == 0) {  // let the loads in flight land before exit
                 mbar_drain(B_KV, 0, ctl, kSiteTeardown);
