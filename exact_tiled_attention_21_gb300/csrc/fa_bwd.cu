@@ -36,19 +36,21 @@ struct Bwd {
     static constexpr int OFF_FIXED = 0;       // two resident tiles
     static constexpr int OFF_STAGE = 2 * TILE;  // 2 stages x 2 streamed tiles
     static constexpr int OFF_VEC = OFF_STAGE + 4 * TILE;  // dkdv: lse2/delta per stage (2 x 1 KB)
-    static constexpr int OFF_BAR = OFF_VEC + 2048;
-    static constexpr int NBAR = 12;
+    static constexpr int OFF_PT = OFF_VEC + 2048;         // dkdv: P^T bf16, 128 keys x 128 queries, K-major
+    static constexpr int OFF_BAR = OFF_PT + 128 * 128 * 2;
+    static constexpr int NBAR = 16;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_MISC + 16 + 1024;
+    static constexpr int SMEM = OFF_MISC + 16;  // the dynamic shared array is declared 1024-aligned
     static constexpr int THREADS = 320;  // warps 0-7 compute (two warpgroups), 8 producer, 9 MMA
     static constexpr int PRODUCER = 8, MMA = 9;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_A = 0;      // S / S^T fp32; P^T bf16 over its first 64 columns
+    static constexpr uint32_t COL_A = 0;      // S / S^T fp32 (the dK/dV pass keeps P^T in shared memory)
     static constexpr uint32_t COL_B = 128;    // dP / dP^T fp32; dS / dS^T bf16 over its first 64
     static constexpr uint32_t COL_ACC0 = 256; // dV (dkdv) or dQ (dq)
     static constexpr uint32_t COL_ACC1 = 256 + D;  // dK (dkdv)
     static constexpr uint32_t IDESC_SS = idesc_bf16(128, 128, 0, 0);
     static constexpr uint32_t IDESC_TS = idesc_bf16(128, D, 0, 1);
+    static constexpr uint32_t IDESC_SM = idesc_bf16(128, D, 0, 1);  // A K-major smem, B MN-major
 };
 
 struct BwdParams {
@@ -182,17 +184,20 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                 const BwdParams p) {
     using C = Bwd<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw;  // 1024-aligned (checked in bwd_setup)
     const uint32_t s_base = smem_u32(smem);
     const uint32_t bar0 = s_base + C::OFF_BAR;
     // barriers
+    // S: S^T ready; SF: S^T read out of TMEM (the next S^T may overwrite it); P: P^T written
+    // to shared memory; PV: dV product done (P^T buffer free again); DP, DS: dP^T ready, dS^T written
     const uint32_t B_KV = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_DP = bar0 + 48,
-                   B_P = bar0 + 56, B_DS = bar0 + 64, B_ACC = bar0 + 72, B_TD = bar0 + 80;
-    const uint32_t counts[11] = {1, 32, 32, 1, 1, 1, 1, 256, 256, 1, 1};
+                   B_P = bar0 + 56, B_DS = bar0 + 64, B_ACC = bar0 + 72, B_TD = bar0 + 80, B_SF = bar0 + 88,
+                   B_PV = bar0 + 96;
+    const uint32_t counts[13] = {1, 32, 32, 1, 1, 1, 1, 256, 256, 1, 1, 256, 1};
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
-    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 11);
+    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 13);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // head-major, so the CTAs in flight share one head's Q / dO in L2; within a
@@ -210,6 +215,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     auto sQ = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
     auto sDO = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
     float* vec = (float*)(smem + C::OFF_VEC);  // stage s: lse2 at [s*256], delta at [s*256 + 128]
+    const uint32_t sPT = s_base + C::OFF_PT;    // P^T: query chunk c at c * CHUNK, key row r at r * 128
 
     if (warp == C::PRODUCER) {
         // ------------------------------------------------------------ producer (whole warp)
@@ -281,18 +287,25 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 issue_ss<D>(tmem + C::COL_B, sV, sDO(0));
                 mma_commit(B_DP);
             }
+            // order per query tile: S^T(i+1) as soon as S^T(i) has been read out of TMEM,
+            // dV(i) once P^T(i) is in shared memory, dK(i) once dS^T(i) is in TMEM, dP^T(i+1)
             for (int ii = 0; ii < n && ok; ++ii) {
                 const int st = ii & 1;
-                if (!(ok = mbar_wait(B_P, ii & 1, ctl, kSiteBwdP))) break;
-                tc_fence_after();
-                issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_A, sDO(st), ii > 0);  // dV += P^T dO
                 const bool more = ii + 1 < n;
                 if (more) {
+                    if (!(ok = mbar_wait(B_SF, ii & 1, ctl, kSiteBwdS))) break;
                     if (!(ok = mbar_wait(B_STF + 8 * (st ^ 1), ((ii + 1) >> 1) & 1, ctl, kSiteBwdQFull))) break;
                     tc_fence_after();
                     issue_ss<D>(tmem + C::COL_A, sK, sQ(st ^ 1));  // S^T of the next query tile
                     mma_commit(B_S);
                 }
+                if (!(ok = mbar_wait(B_P, ii & 1, ctl, kSiteBwdP))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)  // dV += P^T dO: A = P^T (smem, K-major), B = dO (MN-major)
+                    mma_ss(tmem + C::COL_ACC0, sdesc_sw128(sPT + (k >> 2) * C::CHUNK + (k & 3) * 32, 16, 1024),
+                           sdesc_sw128(sDO(st) + k * 2048, C::CHUNK, 1024), C::IDESC_SM, (ii > 0 || k > 0) ? 1u : 0u);
+                mma_commit(B_PV);
                 if (!(ok = mbar_wait(B_DS, ii & 1, ctl, kSiteBwdDS))) break;
                 tc_fence_after();
                 issue_ts<D>(tmem + C::COL_ACC1, tmem + C::COL_B, sQ(st), ii > 0);  // dK += dS^T Q
@@ -328,25 +341,27 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             if (!(ok = mbar_wait(B_S, ii & 1, ctl, kSiteBwdS))) break;
             tc_fence_after();
             uint32_t pp[32];
-            uint32_t va[32], vb[32];  // chunk 1 loads while chunk 0 is processed
+            uint32_t va[32], vb[32];
+            // read this warpgroup's 64 S^T columns, then release them: the next S^T may overwrite
+            tmem_ld32_async(lane_addr + colA, va);
+            tmem_ld32_async(lane_addr + colA + 32, vb);
+            tmem_wait_ld(va);
+            tmem_wait_ld(vb);
+            tc_fence_before();
+            mbar_arrive(B_SF);
             // masked entries: rows past Nk (whole row) and, causal, columns c < cmin.
             // Tiles with none in the warp take the instantiation without the test.
             const int cmin_eff = row_ok ? cmin : (1 << 30);
             auto p_phase = [&](auto MASK) {
-            tmem_ld32_async(lane_addr + colA, va);
-            tmem_wait_ld(va);
-            tmem_ld32_async(lane_addr + colA + 32, vb);
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
                 uint32_t(&v)[32] = q4 ? vb : va;
-                if (q4) tmem_wait_ld(vb);
                 float lv[32];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float4 t = reinterpret_cast<const float4*>(l2 + q4 * 32)[e];
                     lv[4 * e] = t.x, lv[4 * e + 1] = t.y, lv[4 * e + 2] = t.z, lv[4 * e + 3] = t.w;
                 }
-                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int c0 = q4 * 32 + 2 * e;
@@ -357,18 +372,25 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                         if (c0 < cmin_eff) a = 0.f;
                         if (c0 + 1 < cmin_eff) b = 0.f;
                     }
-                    pk[e] = pack_bf16(a, b);
-                    pp[q4 * 16 + e] = pk[e];
+                    pp[q4 * 16 + e] = pack_bf16(a, b);
                 }
-                tmem_st16_async(lane_addr + colA + q4 * 16, pk);
             }
-            tmem_wait_st();
             };
             if (__any_sync(0xffffffffu, cmin_eff > 0))
                 p_phase(std::true_type{});
             else
                 p_phase(std::false_type{});
-            tc_fence_before();
+            // P^T row r, queries [64h, 64h + 64): query chunk h, 16-byte granule g stored at
+            // g ^ (r & 7) (128-byte swizzle, matching the K-major operand descriptor)
+            if (ii > 0 && !(ok = mbar_wait(B_PV, (ii - 1) & 1, ctl, kSiteBwdP))) break;  // dV(i-1) has read it
+            {
+                uint8_t* prow = smem + C::OFF_PT + h * C::CHUNK + r * 128;
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    *reinterpret_cast<uint4*>(prow + ((g ^ (r & 7)) << 4)) =
+                        make_uint4(pp[4 * g], pp[4 * g + 1], pp[4 * g + 2], pp[4 * g + 3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
             mbar_arrive(B_P);
             if (!(ok = mbar_wait(B_DP, ii & 1, ctl, kSiteBwdDP))) break;
             tc_fence_after();
@@ -422,8 +444,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
               const BwdParams p) {
     using C = Bwd<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw;  // 1024-aligned (checked in bwd_setup)
     const uint32_t s_base = smem_u32(smem);
     const uint32_t bar0 = s_base + C::OFF_BAR;
     const uint32_t B_Q = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_SF = bar0 + 48,
