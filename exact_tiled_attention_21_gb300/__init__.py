@@ -135,6 +135,15 @@ def fa_get_last_device_error(stream=None):
     return st, list(detail)
 
 
+def fa_selftest_wait_timeout(timeout_ns, stream=None):
+    """Launch the watchdog self-test kernel (a wait that must run out)."""
+    fn = load().fa_selftest_wait_timeout
+    if fn.argtypes is None:
+        fn.argtypes = [ctypes.c_uint64, ctypes.c_void_p]
+        fn.restype = ctypes.c_int
+    _raise(fn(int(timeout_ns), _stream(stream)), "fa_selftest_wait_timeout")
+
+
 def fa_bwd_workspace_bytes(B, H, Nq, Nk, d):
     return int(load().fa_bwd_workspace_bytes(B, H, Nq, Nk, d))
 

@@ -106,6 +106,21 @@ size_t decode_ws_bytes(int B, int H, int d, int splits) {
     return parts * d * 4 + ((parts * 4 + 255) & ~(size_t)255);
 }
 
+// Watchdog self-test: one thread waits on an mbarrier that nothing ever
+// arrives on.  The bounded wait gives up after `timeout_ns`, records
+// FA_ERR_TIMEOUT at kSiteProbe in the error word and the kernel returns.
+__global__ void selftest_wait_kernel(DevError* err, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    const WaitCtl ctl{err, timeout_ns, &abort_flag};
+    mbar_wait(b, 0, ctl, kSiteProbe);
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -300,6 +315,15 @@ int fa_decode(const void* q, const void* kcache, const void* vcache, void* o, fl
     a.chunk = (Nk + splits - 1) / splits;
     a.scale = scale;
     return launch_decode(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
+    if (timeout_ns < 1000ull || timeout_ns > 1000000000ull) return FA_ERR_INVALID_ARG;
+    DevError* err = nullptr;
+    int st = device_state(&err, nullptr);
+    if (st != FA_OK) return st;
+    selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err, timeout_ns);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_get_last_device_error(void* stream, int* detail) {

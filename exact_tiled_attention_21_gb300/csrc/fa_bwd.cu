@@ -54,6 +54,8 @@ struct Bwd {
 };
 
 struct BwdParams {
+    const __nv_bfloat16* q;   // the dQ pass loads its Q and dO rows straight into TMEM
+    const __nv_bfloat16* dO;
     __nv_bfloat16* dq;
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
@@ -114,6 +116,16 @@ __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint3
     for (int k = 0; k < 8; ++k)
         mma_ts(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), sdesc_sw128(sB + k * 2048, Bwd<D>::CHUNK, 1024),
                Bwd<D>::IDESC_TS, (acc || k > 0) ? 1u : 0u);
+}
+
+// Issue C[tmem] = A[tmem, 128 x D bf16] B^T with B a K-major 128-row tile in
+// shared memory (the score products of the dQ pass: Q or dO from TMEM).
+template <int D>
+__device__ __forceinline__ void issue_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB) {
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k)
+        mma_ts(d_tmem, a_tmem + k * 8, sdesc_sw128(sB + (k >> 2) * Bwd<D>::CHUNK + (k & 3) * 32, 16, 1024),
+               Bwd<D>::IDESC_SS, k > 0);
 }
 
 // Writes columns [c0, c0 + D/2) of a 128-row accumulator row (thread = row)
@@ -448,12 +460,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     uint8_t* smem = smem_raw;  // 1024-aligned (checked in bwd_setup)
     const uint32_t s_base = smem_u32(smem);
     const uint32_t bar0 = s_base + C::OFF_BAR;
-    const uint32_t B_Q = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_SF = bar0 + 48,
-                   B_DP = bar0 + 56, B_DS = bar0 + 64, B_ACC = bar0 + 72, B_TD = bar0 + 80;
-    const uint32_t counts[11] = {1, 1, 1, 1, 1, 1, 256, 1, 256, 1, 1};
+    // QA: Q_i and dO_i written to TMEM by the compute threads; K/V ring of NST stages
+    constexpr int NST = 3;
+    const uint32_t B_QA = bar0, B_STF = bar0 + 8, B_STE = bar0 + 32, B_S = bar0 + 56, B_SF = bar0 + 64,
+                   B_DP = bar0 + 72, B_DS = bar0 + 80, B_ACC = bar0 + 88, B_TD = bar0 + 96;
+    const uint32_t counts[13] = {256, 1, 1, 1, 1, 1, 1, 1, 256, 1, 256, 1, 1};
+    // TMEM: S at 0, dP at 128 (dS bf16 over it), dQ at 256, Q_i at 384, dO_i after it (bf16 pairs)
+    constexpr uint32_t COL_QA = 384, COL_DOA = 384 + D / 2;
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
-    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 11);
+    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 13);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x / p.n_qt;  // head-major (K / V of one head shared in L2)
@@ -466,57 +482,52 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const long long lim = (long long)qmax + off;
         n = lim < 0 ? 0 : min(p.n_kt, (int)(lim / 128) + 1);
     }
-    const uint32_t sQ = s_base + C::OFF_FIXED, sDO = sQ + C::TILE;
-    auto sK = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
-    auto sV = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
+    static_assert(NST * 2 * C::TILE <= C::OFF_VEC, "K/V stages fit below the vector region");
+    auto sK = [&](int st) { return s_base + st * 2 * C::TILE; };
+    auto sV = [&](int st) { return s_base + st * 2 * C::TILE + C::TILE; };
 
     if (warp == C::PRODUCER) {
         if (lane == 0 && !*abort_flag && n > 0) {
             const uint64_t pol = l2_policy_evict_last();
             tma_prefetch_desc(&map_k);
             tma_prefetch_desc(&map_v);
-            mbar_arrive_expect_tx(B_Q, 2 * C::TILE);
-            for (int c = 0; c < C::KCH; ++c) {
-                tma_load_3d(sQ + c * C::CHUNK, &map_q, B_Q, c * 64, it * 128, bh, pol);
-                tma_load_3d(sDO + c * C::CHUNK, &map_do, B_Q, c * 64, it * 128, bh, pol);
-            }
             uint32_t issued = 0, issued_par = 0;
             for (int jj = 0; jj < n; ++jj) {
-                const int st = jj & 1;
-                if (!mbar_wait(B_STE + 8 * st, ((jj >> 1) & 1) ^ 1, ctl, kSiteBwdQEmpty)) break;
+                const int st = jj % NST;
+                const uint32_t ph = (uint32_t)((jj / NST) & 1);
+                if (!mbar_wait(B_STE + 8 * st, ph ^ 1, ctl, kSiteBwdQEmpty)) break;
                 mbar_arrive_expect_tx(B_STF + 8 * st, 2 * C::TILE);
                 for (int c = 0; c < C::KCH; ++c) {
                     tma_load_3d(sK(st) + c * C::CHUNK, &map_k, B_STF + 8 * st, c * 64, jj * 128, bh, pol);
                     tma_load_3d(sV(st) + c * C::CHUNK, &map_v, B_STF + 8 * st, c * 64, jj * 128, bh, pol);
                 }
                 issued |= 1u << st;
-                issued_par = (issued_par & ~(1u << st)) | ((uint32_t)((jj >> 1) & 1) << st);
+                issued_par = (issued_par & ~(1u << st)) | (ph << st);
             }
             if (*abort_flag) {
-                mbar_drain(B_Q, 0, ctl, kSiteTeardown);
-                for (int st = 0; st < 2; ++st)
+                for (int st = 0; st < NST; ++st)
                     if (issued & (1u << st)) mbar_drain(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
             }
         }
     } else if (warp == C::MMA) {
         if (lane == 0 && !*abort_flag && n > 0) {
-            bool ok = mbar_wait(B_Q, 0, ctl, kSiteBwdQFull);
+            bool ok = mbar_wait(B_QA, 0, ctl, kSiteBwdQFull);
             if (ok) ok = mbar_wait(B_STF, 0, ctl, kSiteBwdKvFull);
             if (ok) {
                 tc_fence_after();
-                issue_ss<D>(tmem + C::COL_A, sQ, sK(0));
+                issue_ts_k<D>(tmem + C::COL_A, tmem + COL_QA, sK(0));   // S = Q K^T, Q from TMEM
                 mma_commit(B_S);
-                issue_ss<D>(tmem + C::COL_B, sDO, sV(0));
+                issue_ts_k<D>(tmem + C::COL_B, tmem + COL_DOA, sV(0));  // dP = dO V^T, dO from TMEM
                 mma_commit(B_DP);
             }
             for (int jj = 0; jj < n && ok; ++jj) {
-                const int st = jj & 1;
+                const int st = jj % NST, stn = (jj + 1) % NST;
                 const bool more = jj + 1 < n;
                 if (more) {
                     if (!(ok = mbar_wait(B_SF, jj & 1, ctl, kSiteBwdP))) break;
-                    if (!(ok = mbar_wait(B_STF + 8 * (st ^ 1), ((jj + 1) >> 1) & 1, ctl, kSiteBwdKvFull))) break;
+                    if (!(ok = mbar_wait(B_STF + 8 * stn, ((jj + 1) / NST) & 1, ctl, kSiteBwdKvFull))) break;
                     tc_fence_after();
-                    issue_ss<D>(tmem + C::COL_A, sQ, sK(st ^ 1));
+                    issue_ts_k<D>(tmem + C::COL_A, tmem + COL_QA, sK(stn));
                     mma_commit(B_S);
                 }
                 if (!(ok = mbar_wait(B_DS, jj & 1, ctl, kSiteBwdDS))) break;
@@ -524,7 +535,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                 issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sK(st), jj > 0);  // dQ += dS K
                 mma_commit(B_STE + 8 * st);
                 if (more) {
-                    issue_ss<D>(tmem + C::COL_B, sDO, sV(st ^ 1));
+                    issue_ts_k<D>(tmem + C::COL_B, tmem + COL_DOA, sV(stn));
                     mma_commit(B_DP);
                 }
             }
@@ -550,6 +561,29 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
         const float sc = p.scale_log2;
         const int lim_row = p.causal ? min(qg + off, p.Nk - 1) : p.Nk - 1;  // last key this row sees
+        // Q_i and dO_i into TMEM as the A operands of the score products: row = lane,
+        // bf16 pairs in column order; warpgroup h writes d-columns [h D/2, (h+1) D/2)
+        if (n > 0) {
+            constexpr int W = D / 4;  // 32-bit words per half row
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const __nv_bfloat16* src = (t ? p.dO : p.q) + ((size_t)bh * p.Nq + (row_ok ? qg : 0)) * D + h * (D / 2);
+                uint32_t w[W];
+#pragma unroll
+                for (int e = 0; e < W / 4; ++e) {
+                    const uint4 x = row_ok ? __ldg(reinterpret_cast<const uint4*>(src) + e) : make_uint4(0, 0, 0, 0);
+                    w[4 * e] = x.x, w[4 * e + 1] = x.y, w[4 * e + 2] = x.z, w[4 * e + 3] = x.w;
+                }
+                const uint32_t col = (t ? COL_DOA : COL_QA) + h * (D / 4);
+                if constexpr (W == 32) {
+                    tmem_st32(lane_addr + col, w);
+                } else {
+                    tmem_st16(lane_addr + col, w);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(B_QA);
+        }
         bool ok = true;
         for (int jj = 0; jj < n; ++jj) {
             const int cmax = lim_row - jj * 128 - 64 * h;  // columns > cmax are masked
@@ -625,6 +659,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 
 BwdParams make_params(const BwdLaunch& a) {
     BwdParams p;
+    p.q = (const __nv_bfloat16*)a.q;
+    p.dO = (const __nv_bfloat16*)a.dO;
     p.dq = (__nv_bfloat16*)a.dq;
     p.dk = (__nv_bfloat16*)a.dk;
     p.dv = (__nv_bfloat16*)a.dv;

@@ -157,6 +157,14 @@ int fa_decode_noalloc(const void *q, const void *kcache, const void *vcache, voi
  * value (the wait's phase), all 0 when no error was recorded. */
 int fa_get_last_device_error(void *stream, int *detail);
 
+/* Watchdog self-test (failure detection without a GPU fault): launches one
+ * thread that waits on a barrier nothing ever arrives on, with a limit of
+ * timeout_ns (1e3 .. 1e9).  The wait runs out, the kernel records
+ * FA_ERR_TIMEOUT (site 19, the self-test site) in the error word and returns;
+ * fa_get_last_device_error(stream, ...) then reports it and clears the word.
+ * The device stays usable.  Returns the launch status. */
+int fa_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
 /* Sets the limit of every device-side wait, in nanoseconds, for kernels
  * launched after the call (default 2e9; values below 1e6 are raised to 1e6).
  * Returns the previous value. */

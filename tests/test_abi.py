@@ -76,6 +76,14 @@ def test_backward_and_decode_validation(lib):
     assert lib.fa_decode(*q[:4], vp(20), 2, 2, 100, 128, 0.1, 16, vp(16), d_need, None) == fa.FA_ERR_ALIGNMENT
 
 
+def test_selftest_argument_checks(lib):
+    fn = lib.fa_selftest_wait_timeout
+    fn.argtypes = [ctypes.c_uint64, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    assert fn(10, None) == fa.FA_ERR_INVALID_ARG              # below 1 us
+    assert fn(5_000_000_000, None) == fa.FA_ERR_INVALID_ARG   # above 1 s
+
+
 def test_wait_timeout_setting(lib):
     old = fa.fa_set_wait_timeout_ns(5_000_000)
     assert fa.fa_set_wait_timeout_ns(10) == 5_000_000    # raised to the 1 ms floor next
