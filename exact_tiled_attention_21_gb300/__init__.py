@@ -135,6 +135,44 @@ def fa_get_last_device_error(stream=None):
     return st, list(detail)
 
 
+def fa_decode_paged_workspace_bytes(B, Hq, d, num_splits):
+    fn = load().fa_decode_paged_workspace_bytes
+    fn.argtypes = [ctypes.c_int] * 4
+    fn.restype = ctypes.c_size_t
+    return int(fn(B, Hq, d, num_splits))
+
+
+def fa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, B, Hq, Hkv, page_size,
+                    max_pages, num_pages, d, scale, num_splits, workspace, workspace_bytes, stream=None):
+    fn = load().fa_decode_paged
+    if fn.argtypes is None:
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        fn.argtypes = [vp] * 7 + [i] * 7 + [ctypes.c_float, i, vp, ctypes.c_size_t, vp]
+        fn.restype = ctypes.c_int
+    _raise(fn(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), _ptr(o), _ptr(lse),
+              B, Hq, Hkv, page_size, max_pages, num_pages, d, float(scale), int(num_splits),
+              _ptr(workspace), int(workspace_bytes), _stream(stream)), "fa_decode_paged")
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale=None, num_splits=16, stream=None):
+    """O [B,Hq,d] bf16 and LSE [B,Hq] fp32 against a paged cache (int32 table and lengths on the device)."""
+    B, Hq, d = q.shape
+    num_pages, Hkv, page_size = k_pages.shape[:3]
+    max_pages = block_table.shape[1]
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+            raise ValueError("%s must be a contiguous bf16 CUDA tensor" % n)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_table and seq_lens must be int32")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    ws = torch.empty(fa_decode_paged_workspace_bytes(B, Hq, d, num_splits), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    fa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, B, Hq, Hkv, page_size, max_pages,
+                    num_pages, d, scale, num_splits, ws, ws.numel(), stream)
+    return o, lse
+
+
 def fa_selftest_wait_timeout(timeout_ns, stream=None):
     """Launch the watchdog self-test kernel (a wait that must run out)."""
     fn = load().fa_selftest_wait_timeout

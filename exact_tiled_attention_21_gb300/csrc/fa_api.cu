@@ -317,6 +317,50 @@ int fa_decode(const void* q, const void* kcache, const void* vcache, void* o, fl
     return launch_decode(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+size_t fa_decode_paged_workspace_bytes(int B, int Hq, int d, int num_splits) {
+    if (B < 1 || Hq < 1 || (d != 64 && d != 128) || num_splits < 1 || num_splits > 256) return 0;
+    return decode_ws_bytes(B, Hq, d, num_splits);
+}
+
+int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                    const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int page_size,
+                    int max_pages, int num_pages, int d, float scale, int num_splits, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
+    if (!scale_ok(scale) || num_splits < 1 || num_splits > 256) return FA_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || page_size < 1 || max_pages < 1 || num_pages < 1) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if ((long long)max_pages * page_size > 0x7FFFFFFFll || (long long)B * Hq > (1ll << 24)) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || (lse && !aligned16(lse)) ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return FA_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < decode_ws_bytes(B, Hq, d, num_splits)) return FA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
+    PagedDecodeLaunch a;
+    int st = device_state(&a.err, nullptr);
+    if (st != FA_OK) return st;
+    a.q = q;
+    a.kp = k_pages;
+    a.vp = v_pages;
+    a.table = block_table;
+    a.lens = seq_lens;
+    a.o = o;
+    a.lse = lse;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = a.part_o + (size_t)B * Hq * num_splits * d;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.page = page_size;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.d = d;
+    a.splits = num_splits;
+    a.scale = scale;
+    return launch_decode_paged(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
     if (timeout_ns < 1000ull || timeout_ns > 1000000000ull) return FA_ERR_INVALID_ARG;
     DevError* err = nullptr;
@@ -344,7 +388,7 @@ int fa_get_last_device_error(void* stream, int* detail) {
         detail[2] = h.block;
         detail[3] = h.aux;
     }
-    return h.code == 0 ? FA_OK : FA_ERR_TIMEOUT;
+    return h.code;  // FA_OK, or the first code a kernel recorded
 }
 
 }  // extern "C"

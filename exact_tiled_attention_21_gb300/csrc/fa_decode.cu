@@ -210,10 +210,244 @@ cudaError_t launch_decode_d(const DecodeLaunch& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+
+// ------------------------------------------------------------------ paged, grouped-query decode
+// One CTA per (b, kv head, split, group of G <= 4 query heads).  The split's keys
+// are the logical tokens [split * chunk, min(len, (split + 1) * chunk)) of the
+// sequence, chunk = ceil(len / splits), found through the block table one
+// key at a time; each K and V row is read once and used for all G query heads
+// of the group (they share the kv head).  Same online pieces, partials and
+// combine as the contiguous decode.  A page index outside [0, num_pages) or
+// a length outside [1, max_pages * page] is recorded as FA_ERR_INVALID_ARG in
+// the error word and read as zeros, never dereferenced.
+template <int D, int G>
+__global__ void __launch_bounds__(kDecThreads)
+decode_paged_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kp,
+                          const __nv_bfloat16* __restrict__ vp, const int* __restrict__ table,
+                          const int* __restrict__ lens, float* __restrict__ part_o,
+                          float* __restrict__ part_lse, int Hq, int Hkv, int page, int max_pages,
+                          int num_pages, int splits, int groups, float scale_log2, DevError* err) {
+    constexpr int LPK = D / 8, KPW = 32 / LPK, KPC = KPW * (kDecThreads / 32), STEPS = kDecPiece / KPC;
+    __shared__ float s_p[G][kDecPiece];
+    __shared__ float s_red[kDecThreads / 32][G];
+    __shared__ float s_acc[KPC][D + 4];
+    __shared__ int s_bad;
+
+    int idx = blockIdx.x;
+    const int grp = idx % groups; idx /= groups;
+    const int split = idx % splits; idx /= splits;
+    const int kvh = idx % Hkv;
+    const int b = idx / Hkv;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slice = lane % LPK, group = warp * KPW + lane / LPK;
+    const int g = Hq / Hkv;
+    const int h0 = kvh * g + grp * G;  // first query head of this CTA
+
+    if (tid == 0) s_bad = 0;
+    int len = lens[b];
+    const int cap = max_pages * page;
+    if (len < 1 || len > cap) {
+        if (tid == 0 && atomicCAS(&err->code, 0, kErrInvalid) == 0) {
+            err->site = kSitePagedTable; err->block = blockIdx.x; err->aux = len;
+        }
+        len = len < 1 ? 0 : cap;
+    }
+    const int chunk = (len + splits - 1) / splits;
+    const int k0 = split * chunk, k1 = min(k0 + chunk, len);
+    if (k0 >= k1) {
+        for (int hh = 0; hh < G; ++hh) {
+            float* po = part_o + ((size_t)(b * Hq + h0 + hh) * splits + split) * D;
+            if (tid < D / 4) reinterpret_cast<float4*>(po)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (tid == 0) part_lse[(size_t)(b * Hq + h0 + hh) * splits + split] = -INFINITY;
+        }
+        return;
+    }
+    float qf[G][8];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        const uint4 qv = *reinterpret_cast<const uint4*>(q + (size_t)(b * Hq + h0 + hh) * D + slice * 8);
+        const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(q2[i]);
+            qf[hh][2 * i] = f.x * scale_log2;
+            qf[hh][2 * i + 1] = f.y * scale_log2;
+        }
+    }
+    const int* trow = table + (size_t)b * max_pages;
+    // element offset of logical token t's row for this kv head, or -1 if its page is invalid
+    auto row_off = [&](int t) -> long long {
+        const int pg = trow[t / page];
+        if (pg < 0 || pg >= num_pages) return -1;
+        return (((long long)pg * Hkv + kvh) * page + (t % page)) * D + slice * 8;
+    };
+    float m_run[G], l_run[G], acc[G][8];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        m_run[hh] = -INFINITY;
+        l_run[hh] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[hh][i] = 0.f;
+    }
+    bool bad = false;
+    for (int p0 = k0; p0 < k1; p0 += kDecPiece) {
+        uint4 kr[STEPS];
+#pragma unroll
+        for (int s2 = 0; s2 < STEPS; ++s2) {
+            const int key = p0 + s2 * KPC + group;
+            kr[s2] = make_uint4(0, 0, 0, 0);
+            if (key < k1) {
+                const long long off = row_off(key);
+                if (off >= 0) kr[s2] = __ldg(reinterpret_cast<const uint4*>(kp + off));
+                else bad = true;
+            }
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < STEPS; ++s2) {
+            const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kr[s2]);
+            float kf[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(k2[i]);
+                kf[2 * i] = f.x, kf[2 * i + 1] = f.y;
+            }
+            const int kl = s2 * KPC + group;
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                float dot = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dot = fmaf(qf[hh][i], kf[i], dot);
+#pragma unroll
+                for (int w = LPK / 2; w >= 1; w >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, w);
+                if (slice == 0) s_p[hh][kl] = (p0 + kl < k1) ? dot : -INFINITY;
+            }
+        }
+        __syncthreads();
+        float mx[G];
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            float m = s_p[hh][tid];
+            for (int w = 16; w >= 1; w >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, w));
+            mx[hh] = m;
+        }
+        if (lane == 0)
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) s_red[warp][hh] = mx[hh];
+        __syncthreads();
+        float alpha[G], pv[G], ps[G];
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            float m = s_red[0][hh];
+#pragma unroll
+            for (int w = 1; w < kDecThreads / 32; ++w) m = fmaxf(m, s_red[w][hh]);
+            const float m_new = fmaxf(m_run[hh], m);
+            alpha[hh] = ex2(m_run[hh] - m_new);
+            m_run[hh] = m_new;
+            pv[hh] = ex2(s_p[hh][tid] - m_new);
+            float t = pv[hh];
+            for (int w = 16; w >= 1; w >>= 1) t += __shfl_xor_sync(0xffffffffu, t, w);
+            ps[hh] = t;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            s_p[hh][tid] = pv[hh];
+            if (lane == 0) s_red[warp][hh] = ps[hh];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            float psum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecThreads / 32; ++w) psum += s_red[w][hh];
+            l_run[hh] = l_run[hh] * alpha[hh] + psum;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[hh][i] *= alpha[hh];
+        }
+        uint4 vr[STEPS];
+#pragma unroll
+        for (int s2 = 0; s2 < STEPS; ++s2) {
+            const int key = p0 + s2 * KPC + group;
+            vr[s2] = make_uint4(0, 0, 0, 0);
+            if (key < k1) {
+                const long long off = row_off(key);
+                if (off >= 0) vr[s2] = __ldg(reinterpret_cast<const uint4*>(vp + off));
+            }
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < STEPS; ++s2) {
+            const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&vr[s2]);
+            float vf[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(v2[i]);
+                vf[2 * i] = f.x, vf[2 * i + 1] = f.y;
+            }
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                const float pj = s_p[hh][s2 * KPC + group];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[hh][i] = fmaf(pj, vf[i], acc[hh][i]);
+            }
+        }
+        __syncthreads();
+    }
+    if (bad) s_bad = 1;
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s_acc[group][slice * 8 + i] = acc[hh][i];
+        __syncthreads();
+        float* po = part_o + ((size_t)(b * Hq + h0 + hh) * splits + split) * D;
+        const float inv = 1.f / l_run[hh];
+        for (int c = tid; c < D; c += kDecThreads) {
+            float sum = 0.f;
+#pragma unroll
+            for (int gg = 0; gg < KPC; ++gg) sum += s_acc[gg][c];
+            po[c] = sum * inv;
+        }
+        if (tid == 0)
+            part_lse[(size_t)(b * Hq + h0 + hh) * splits + split] = (m_run[hh] + lg2(l_run[hh])) * 0.69314718055994531f;
+        __syncthreads();
+    }
+    if (tid == 0 && s_bad && atomicCAS(&err->code, 0, kErrInvalid) == 0) {
+        err->site = kSitePagedTable; err->block = blockIdx.x; err->aux = -1;
+    }
+}
+
+template <int D, int G>
+cudaError_t launch_paged_dg(const PagedDecodeLaunch& a, cudaStream_t s) {
+    const int groups = (a.Hq / a.Hkv) / G;
+    const long long ctas = (long long)a.B * a.Hkv * a.splits * groups;
+    if (ctas > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+    decode_paged_split_kernel<D, G><<<(unsigned)ctas, kDecThreads, 0, s>>>(
+        (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kp, (const __nv_bfloat16*)a.vp, a.table, a.lens,
+        a.part_o, a.part_lse, a.Hq, a.Hkv, a.page, a.max_pages, a.num_pages, a.splits, groups,
+        a.scale * 1.4426950408889634f, a.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int BH = a.B * a.Hq;
+    decode_combine_kernel<D><<<(BH + 3) / 4, 128, 0, s>>>(a.part_o, a.part_lse, (__nv_bfloat16*)a.o, a.lse, BH,
+                                                          a.splits);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_paged_d(const PagedDecodeLaunch& a, cudaStream_t s) {
+    const int g = a.Hq / a.Hkv;  // up to 4 query heads per CTA (registers); larger groups use several CTAs
+    if (g % 4 == 0) return launch_paged_dg<D, 4>(a, s);
+    if (g % 2 == 0) return launch_paged_dg<D, 2>(a, s);
+    return launch_paged_dg<D, 1>(a, s);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
     return a.d == 128 ? launch_decode_d<128>(a, s) : launch_decode_d<64>(a, s);
+}
+
+cudaError_t launch_decode_paged(const PagedDecodeLaunch& a, cudaStream_t s) {
+    return a.d == 128 ? launch_paged_d<128>(a, s) : launch_paged_d<64>(a, s);
 }
 
 }  // namespace fa

@@ -53,12 +53,28 @@ struct DecodeLaunch {
     float scale;
 };
 
+struct PagedDecodeLaunch {
+    const void* q;        // bf16 [B, Hq, d]
+    const void* kp;       // bf16 [num_pages, Hkv, page, d]
+    const void* vp;
+    const int* table;     // int32 [B, max_pages]
+    const int* lens;      // int32 [B]
+    void* o;
+    float* lse;           // may be null
+    float* part_o;        // fp32 [B, Hq, S, d]
+    float* part_lse;      // fp32 [B, Hq, S]
+    int B, Hq, Hkv, page, max_pages, num_pages, d, splits;
+    float scale;
+    DevError* err;
+};
+
 // Each returns a cudaError_t of the launch (cudaSuccess when queued).
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s);   // D = rowsum(dO o O)
 cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s);  // dK, dV
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s);    // dQ
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);
+cudaError_t launch_decode_paged(const PagedDecodeLaunch& a, cudaStream_t s);
 
 // Rows of the forward's CTA work tile (two 128-row softmax tiles).
 constexpr int kFwdRowsPerCta = 256;

@@ -24,10 +24,11 @@ struct DevError {
 enum : int {
     kSiteQFull = 1, kSiteQEmpty, kSiteKvFull, kSiteKvEmpty, kSiteSFull, kSitePFull, kSiteOFinal,
     kSiteTeardown, kSiteBwdQFull, kSiteBwdQEmpty, kSiteBwdKvFull, kSiteBwdS, kSiteBwdP, kSiteBwdDP,
-    kSiteBwdDS, kSiteBwdDQ, kSiteBwdDone, kSiteAlign, kSiteProbe
+    kSiteBwdDS, kSiteBwdDQ, kSiteBwdDone, kSiteAlign, kSiteProbe, kSitePagedTable
 };
 
 constexpr int kErrTimeout = -6;
+constexpr int kErrInvalid = -1;  // a device-side argument check failed (e.g. a page index)
 
 struct WaitCtl {
     DevError* err;          // device error word

@@ -122,6 +122,33 @@ int fa_decode(const void *q, const void *kcache, const void *vcache, void *o, fl
               int B, int H, int Nk, int d, float scale, int num_splits,
               void *workspace, size_t workspace_bytes, void *stream);
 
+/* Bytes of fp32 workspace fa_decode_paged needs (partials of B*Hq heads). */
+size_t fa_decode_paged_workspace_bytes(int B, int Hq, int d, int num_splits);
+
+/* Decode against a paged KV cache with grouped-query heads (the serving
+ * layout: johe.ru "Flash Attention: ...", section "Альтернативы",
+ * PagedAttention keeps the cache in fixed-size pages; grouped-query heads
+ * share one kv head).  For every sequence b and query head h it computes the
+ * same result as fa_decode against the sequence's first seq_lens[b] tokens
+ * in logical order, with query head h reading kv head h / (Hq / Hkv).
+ *  q [B, Hq, d] bf16; k_pages, v_pages [num_pages, Hkv, page_size, d] bf16
+ *  (a page holds page_size consecutive tokens of one kv head);
+ *  block_table [B, max_pages] int32: physical page of each logical page;
+ *  seq_lens [B] int32, 1 <= seq_lens[b] <= max_pages * page_size;
+ *  o [B, Hq, d] bf16; lse [B, Hq] fp32 or NULL.
+ * Each sequence is cut into num_splits (1..256) contiguous chunks of
+ * ceil(seq_lens[b] / num_splits) tokens, merged as in fa_decode.  Every K/V
+ * row is read once per group of up to 4 query heads.  Host checks: Hq % Hkv
+ * == 0, d in {64, 128}, alignment, workspace.  The table and lengths live in
+ * device memory and are checked by the kernel: a page index outside
+ * [0, num_pages) or a length out of range is never dereferenced; it is read
+ * as zeros and recorded as FA_ERR_INVALID_ARG in the device error word
+ * (fa_get_last_device_error). */
+int fa_decode_paged(const void *q, const void *k_pages, const void *v_pages, const int *block_table,
+                    const int *seq_lens, void *o, float *lse, int B, int Hq, int Hkv, int page_size,
+                    int max_pages, int num_pages, int d, float scale, int num_splits, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
 /* Size of the scratch array that fa_decode_noalloc uses instead of a workspace. */
 #define FA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
@@ -151,8 +178,10 @@ int fa_decode_noalloc(const void *q, const void *kcache, const void *vcache, voi
                       int B, int H, int Nk, int d, float scale, int num_splits, void *stream);
 
 /* Synchronises `stream`, then reads and clears the device error word of the
- * current device.  Returns FA_OK, FA_ERR_TIMEOUT (a bounded wait ran out), or
- * FA_ERR_CUDA if synchronising or reading failed.  If `detail` is not NULL it
+ * current device.  Returns FA_OK, the first code a kernel recorded
+ * (FA_ERR_TIMEOUT: a bounded wait ran out; FA_ERR_INVALID_ARG: a device-side
+ * argument check failed, e.g. a page index), or FA_ERR_CUDA if synchronising
+ * or reading failed.  If `detail` is not NULL it
  * receives 4 ints: code, site (which wait), block index, and an auxiliary
  * value (the wait's phase), all 0 when no error was recorded. */
 int fa_get_last_device_error(void *stream, int *detail);

@@ -141,3 +141,43 @@ def decode_split(q, kcache, vcache, scale, num_splits):
     lse = m[..., 0] + np.log(w.sum(axis=-1))
     o = (np.exp(pl - lse[..., None])[..., None] * po).sum(axis=-2)
     return o, lse, po, pl
+
+
+def gather_pages(pages, block_table_row, length):
+    """The first ``length`` tokens of one sequence from a paged cache.
+
+    pages: [num_pages, page_size, dv] (one kv head); block_table_row: physical
+    page of each logical page of the sequence, in order.
+    """
+    P = pages.shape[1]
+    n = -(-length // P)
+    rows = np.concatenate([pages[int(block_table_row[p])] for p in range(n)], axis=0) if n else pages[:0, 0]
+    return rows[:length]
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale):
+    """Decode against a paged KV cache with grouped-query heads.
+
+    q [B, Hq, d]; k_pages / v_pages [num_pages, Hkv, page_size, d];
+    block_table [B, max_pages] (physical page of each logical page);
+    seq_lens [B] (tokens in each sequence, >= 1).  Query head h reads kv head
+    h // (Hq // Hkv).  Each (b, h) is the plain decode of its query against the
+    sequence's tokens gathered in logical order (the cache is paged storage,
+    not a different computation: PagedAttention in johe.ru "Flash Attention:
+    ...", section "Альтернативы").  Returns O [B, Hq, dv], LSE [B, Hq].
+    """
+    q, kp, vp = _f64(q), _f64(k_pages), _f64(v_pages)
+    B, Hq, _ = q.shape
+    Hkv = kp.shape[1]
+    g = Hq // Hkv
+    o = np.zeros((B, Hq, vp.shape[-1]))
+    lse = np.zeros((B, Hq))
+    for b in range(B):
+        L = int(seq_lens[b])
+        for kvh in range(Hkv):
+            K = gather_pages(kp[:, kvh], block_table[b], L)
+            V = gather_pages(vp[:, kvh], block_table[b], L)
+            oo, ll = forward(q[b, kvh * g:(kvh + 1) * g], K, V, scale)
+            o[b, kvh * g:(kvh + 1) * g] = oo
+            lse[b, kvh * g:(kvh + 1) * g] = ll
+    return o, lse

@@ -1,0 +1,93 @@
+"""Paged, grouped-query decode (fa_decode_paged) against the fp64 oracle
+(oracle.naive.decode_paged: the plain decode of each query head against its
+sequence's tokens gathered through the block table)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_tiled_attention_21_gb300 as fa_mod
+from exact_tiled_attention_21_gb300 import synthetic as syn
+from oracle import naive
+from tests.parity import check_out, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(seed, B, Hq, Hkv, P, lens, d, extra_pages=5):
+    rng = np.random.default_rng(seed)
+    maxp = max(-(-L // P) for L in lens)
+    npages = B * maxp + extra_pages
+    q = syn.bhd(seed, syn.TAG_Q, B, Hq, d)
+    kp = syn.bhnd(seed, syn.TAG_K, npages, Hkv, P, d)   # [num_pages, Hkv, P, d]
+    vp = syn.bhnd(seed, syn.TAG_V, npages, Hkv, P, d)
+    table = rng.permutation(npages)[:B * maxp].reshape(B, maxp).astype(np.int32)
+    return q, kp, vp, table, np.array(lens, dtype=np.int32)
+
+
+def _run(fa, q, kp, vp, table, lens, splits):
+    dev = torch.device("cuda", 0)
+    o, lse = fa.decode_paged(q.to(dev), kp.to(dev), vp.to(dev), torch.from_numpy(table).to(dev),
+                             torch.from_numpy(lens).to(dev), num_splits=splits)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_get_last_device_error()
+    assert st == 0, detail
+    return o.cpu(), lse.cpu()
+
+
+# (B, Hq, Hkv, page, lens, d, splits)
+CASES = [
+    (3, 8, 2, 16, [1, 37, 200], 128, 4),        # group of 4
+    (2, 6, 2, 64, [64, 1000], 64, 16),          # group of 3 (one head per CTA)
+    (2, 16, 2, 32, [4096, 513], 128, 16),       # group of 8 (two CTAs per kv head)
+    (2, 8, 1, 16, [300, 17], 128, 8),           # multi-query (one kv head)
+    (2, 4, 4, 8, [129, 1], 64, 3),              # one query head per kv head
+    (1, 4, 2, 1, [77], 128, 16),                # single-token pages
+    (2, 4, 2, 16, [5, 3], 128, 16),             # more splits than tokens: empty splits
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,P,lens,d,splits", CASES)
+def test_paged_decode_parity(cuda_lib, B, Hq, Hkv, P, lens, d, splits):
+    q, kp, vp, table, L = _case(900 + P + d + Hq, B, Hq, Hkv, P, lens, d)
+    o, lse = _run(cuda_lib, q, kp, vp, table, L, splits)
+    o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(d))
+    check_out(f64(o), f64(lse), o_ref, lse_ref, "B%d Hq%d Hkv%d P%d d%d" % (B, Hq, Hkv, P, d))
+
+
+def test_paged_decode_full_size(cuda_lib):
+    """B=32, Hq=32, Hkv=8 (groups of 4), 16-token pages, lengths up to 4096."""
+    rng = np.random.default_rng(77)
+    lens = [4096, 1] + list(rng.integers(1, 4097, size=30))
+    q, kp, vp, table, L = _case(78, 32, 32, 8, 16, lens, 128)
+    o, lse = _run(cuda_lib, q, kp, vp, table, L, 16)
+    o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(128))
+    check_out(f64(o), f64(lse), o_ref, lse_ref, "paged full size")
+
+
+def test_paged_decode_matches_contiguous_decode(cuda_lib):
+    """Identity table, full lengths, Hq == Hkv: the same as fa_decode."""
+    B, H, P, npg, d = 2, 4, 64, 8, 128
+    q = syn.bhd(5, syn.TAG_Q, B, H, d)
+    kc, vc = syn.bhnd(5, syn.TAG_K, B, H, P * npg, d), syn.bhnd(5, syn.TAG_V, B, H, P * npg, d)
+    kp = kc.reshape(B, H, npg, P, d).permute(0, 2, 1, 3, 4).reshape(B * npg, H, P, d).contiguous()
+    vp = vc.reshape(B, H, npg, P, d).permute(0, 2, 1, 3, 4).reshape(B * npg, H, P, d).contiguous()
+    table = np.arange(B * npg, dtype=np.int32).reshape(B, npg)
+    o, lse = _run(cuda_lib, q, kp, vp, table, np.full(B, P * npg, dtype=np.int32), 16)
+    dev = torch.device("cuda", 0)
+    o2, lse2 = cuda_lib.decode(q.to(dev), kc.to(dev), vc.to(dev), num_splits=16)
+    check_out(f64(o), f64(lse), f64(o2.cpu()), f64(lse2.cpu()), "paged vs contiguous")
+
+
+def test_paged_decode_rejects_bad_page_index_on_device(cuda_lib):
+    """A page index outside the cache is never dereferenced: it reads as zeros
+    and the kernel records FA_ERR_INVALID_ARG."""
+    q, kp, vp, table, L = _case(5, 1, 4, 2, 16, [40], 128)
+    table[0, 1] = kp.shape[0] + 1000
+    dev = torch.device("cuda", 0)
+    cuda_lib.decode_paged(q.to(dev), kp.to(dev), vp.to(dev), torch.from_numpy(table).to(dev),
+                          torch.from_numpy(L).to(dev), num_splits=4)
+    st, detail = cuda_lib.fa_get_last_device_error()
+    assert st == fa_mod.FA_ERR_INVALID_ARG, detail
+    assert cuda_lib.fa_get_last_device_error()[0] == 0

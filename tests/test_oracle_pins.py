@@ -311,6 +311,56 @@ def test_backward_row_shares_add_up():
         np.testing.assert_allclose(sv, dv, atol=1e-12)
 
 
+def _paged_case(B, Hkv, g, P, lens, d, pages_extra=3, seed=7):
+    rng = np.random.default_rng(seed)
+    maxp = max(-(-L // P) for L in lens)
+    npages = B * maxp + pages_extra
+    kp, vp = rng.standard_normal((npages, Hkv, P, d)), rng.standard_normal((npages, Hkv, P, d))
+    table = rng.permutation(npages)[:B * maxp].reshape(B, maxp)
+    q = rng.standard_normal((B, Hkv * g, d))
+    return q, kp, vp, table, np.array(lens)
+
+
+def test_paged_decode_equals_contiguous_decode():
+    """Identity page table, full lengths, one query head per kv head: the
+    plain contiguous decode."""
+    B, H, P, d, npg = 2, 3, 8, 16, 5
+    q = RNG.standard_normal((B, H, d))
+    kc, vc = RNG.standard_normal((B, H, P * npg, d)), RNG.standard_normal((B, H, P * npg, d))
+    # pages [B*npg, H, P, d]: sequence b's logical page p is physical page b*npg + p
+    kp = kc.reshape(B, H, npg, P, d).transpose(0, 2, 1, 3, 4).reshape(B * npg, H, P, d)
+    vp = vc.reshape(B, H, npg, P, d).transpose(0, 2, 1, 3, 4).reshape(B * npg, H, P, d)
+    table = np.arange(B * npg).reshape(B, npg)
+    o, lse = naive.decode_paged(q, kp, vp, table, [P * npg] * B, 0.3)
+    o2, lse2 = naive.decode(q, kc, vc, 0.3)
+    np.testing.assert_allclose(o, o2, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, atol=1e-12)
+
+
+def test_paged_decode_invariances():
+    """Moving pages to other physical slots (table updated) changes nothing;
+    a sequence of length L equals decode against its first L tokens; the
+    query heads of a group all read the same kv head."""
+    q, kp, vp, table, lens = _paged_case(3, 2, 4, 8, [1, 13, 24], 16)
+    o, lse = naive.decode_paged(q, kp, vp, table, lens, 0.25)
+    perm = RNG.permutation(kp.shape[0])
+    inv = np.argsort(perm)
+    o2, lse2 = naive.decode_paged(q, kp[perm], vp[perm], inv[table], lens, 0.25)
+    np.testing.assert_allclose(o2, o, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, atol=1e-12)
+    for b in range(3):
+        for h in range(8):
+            K = np.concatenate([kp[table[b, p], h // 4] for p in range(table.shape[1])])[:lens[b]]
+            V = np.concatenate([vp[table[b, p], h // 4] for p in range(table.shape[1])])[:lens[b]]
+            oo, ll = naive.forward(q[b, h][None], K, V, 0.25)
+            np.testing.assert_allclose(o[b, h], oo[0], atol=1e-12)
+            np.testing.assert_allclose(lse[b, h], ll[0], atol=1e-12)
+    # a single-token sequence returns that token's value, LSE = its score
+    K0, V0 = kp[table[0, 0], 0, 0], vp[table[0, 0], 0, 0]
+    np.testing.assert_allclose(o[0, 0], V0, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], 0.25 * q[0, 0] @ K0, atol=1e-12)
+
+
 # ---------------------------------------------------------------- mutation check
 def _mutant_forward(kind):
     def fwd(q, k, v, scale, causal=False, return_p=False):
