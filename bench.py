@@ -349,6 +349,33 @@ def run_ours(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError("device error in the end-to-end run: %s" % detail)
 
+    # ---- paged grouped-query decode (next-row feature; timed separately, not part of the step)
+    PG_HKV, PG_PAGE = 8, 16
+    npages = DEC_B * (DEC_NK // PG_PAGE)
+    kpg = rnd(npages, PG_HKV, PG_PAGE, D)
+    vpg = rnd(npages, PG_HKV, PG_PAGE, D)
+    perm = torch.randperm(npages, generator=torch.Generator().manual_seed(5)).to(torch.int32)
+    table = perm.reshape(DEC_B, DEC_NK // PG_PAGE).to(dev)
+    lens = torch.full((DEC_B,), DEC_NK, dtype=torch.int32, device=dev)
+    pws = torch.empty(fa.fa_decode_paged_workspace_bytes(DEC_B, DEC_H, D, DEC_SPLITS), dtype=torch.uint8,
+                      device=dev)
+    pg_call = lambda: fa.fa_decode_paged(dq_, kpg, vpg, table, lens, od, lsed, DEC_B, DEC_H, PG_HKV, PG_PAGE,
+                                         DEC_NK // PG_PAGE, npages, D, SCALE, DEC_SPLITS, pws, pws.numel(), stream)
+    for _ in range(3):
+        pg_call()
+    barrier()
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pe0.record(stream)
+    for _ in range(20):
+        pg_call()
+    pe1.record(stream)
+    barrier()
+    pg_ms = pe0.elapsed_time(pe1) / 20
+    pg_bytes = 2.0 * DEC_B * PG_HKV * DEC_NK * D * 2
+    st, detail = fa.fa_get_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError("device error in the paged decode run: %s" % detail)
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -381,6 +408,9 @@ def run_ours(args, rank, world, local_rank):
         },
         "decode": {"value": world * DEC_BYTES / (dec_ms_max * 1e-3) / 1e9, "unit": "GB/s",
                    "ms": dec_ms, "frac_of_hbm": DEC_BYTES / (dec_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "decode_paged": {"value": pg_bytes / (pg_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": pg_ms,
+                         "config": "B=32 Hq=32 Hkv=8 page=16 Nk=4096 d=128 16 splits (grouped-query, paged)",
+                         "frac_of_hbm": pg_bytes / (pg_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
         "roofline": {
             "kernel": "bwd_dkdv_kernel<128>",
             "bound": "tensor",

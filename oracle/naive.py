@@ -39,20 +39,28 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def allowed(Nq, Nk, causal, rows=None):
+def allowed(Nq, Nk, causal, rows=None, window=0):
     """Boolean [len(rows), Nk]: which keys each query row may attend to.
 
     ``rows`` are query indices in [0, Nq) (default: all).  Causal alignment is
-    bottom-right (key j visible to query i iff j <= i + Nk - Nq).
+    bottom-right (key j visible to query i iff j <= i + Nk - Nq).  A sliding
+    window of w >= 1 keys (causal only; the local attention with a fixed
+    window that johe.ru "Flash Attention: ...", section "Альтернативы",
+    describes) also hides the keys j <= i + Nk - Nq - w: each query sees at most
+    the w keys ending at its diagonal.
     """
     rows = np.arange(Nq) if rows is None else np.asarray(rows)
     cols = np.arange(Nk)
     if not causal:
         return np.ones((rows.size, Nk), dtype=bool)
-    return cols[None, :] <= (rows[:, None] + (Nk - Nq))
+    hi = rows[:, None] + (Nk - Nq)
+    ok = cols[None, :] <= hi
+    if window:
+        ok &= cols[None, :] > hi - window
+    return ok
 
 
-def forward(q, k, v, scale, causal=False, rows=None, Nq=None, return_p=False):
+def forward(q, k, v, scale, causal=False, rows=None, Nq=None, return_p=False, window=0):
     """Materialised forward.
 
     q: [..., R, d] query rows (R = Nq, or the sampled rows when ``rows`` given)
@@ -65,7 +73,7 @@ def forward(q, k, v, scale, causal=False, rows=None, Nq=None, return_p=False):
     R, Nk = q.shape[-2], k.shape[-2]
     if rows is None:
         Nq = R
-    mask = allowed(Nq, Nk, causal, rows)
+    mask = allowed(Nq, Nk, causal, rows, window)
     s = scale * (q @ np.swapaxes(k, -1, -2))
     s = np.where(mask, s, -np.inf)
     m = s.max(axis=-1, keepdims=True)
@@ -81,7 +89,7 @@ def forward(q, k, v, scale, causal=False, rows=None, Nq=None, return_p=False):
     return o, lse
 
 
-def backward(q, k, v, do, scale, causal=False, rows=None, Nq=None):
+def backward(q, k, v, do, scale, causal=False, rows=None, Nq=None, window=0):
     """Gradients (dQ, dK, dV) of O = softmax(scale Q K^T [masked]) V for upstream dO.
 
     With ``rows`` (query indices of the given q / dO rows, ``Nq`` the total query
@@ -90,7 +98,7 @@ def backward(q, k, v, do, scale, causal=False, rows=None, Nq=None):
     shares over any partition of the queries).
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
-    _, _, p = forward(q, k, v, scale, causal, rows=rows, Nq=Nq, return_p=True)
+    _, _, p = forward(q, k, v, scale, causal, rows=rows, Nq=Nq, return_p=True, window=window)
     dv = np.swapaxes(p, -1, -2) @ do
     dp = do @ np.swapaxes(v, -1, -2)
     ds = p * (dp - (p * dp).sum(axis=-1, keepdims=True))

@@ -361,6 +361,44 @@ def test_paged_decode_invariances():
     np.testing.assert_allclose(lse[0, 0], 0.25 * q[0, 0] @ K0, atol=1e-12)
 
 
+@pytest.mark.parametrize("Nq,Nk", [(9, 9), (5, 12), (12, 5)])
+def test_sliding_window_pins(Nq, Nk):
+    """A window of >= Nk keys is plain causal; a window of 1 key gives
+    O_i = V[i + Nk - Nq] and LSE_i = its score; any window equals torch SDPA
+    with the explicit band mask; rows sum to one over the band."""
+    q, k, v = RNG.standard_normal((2, Nq, 6)), RNG.standard_normal((2, Nk, 6)), RNG.standard_normal((2, Nk, 5))
+    off = Nk - Nq
+    o_c, l_c = naive.forward(q, k, v, 0.4, True)
+    o_w, l_w = naive.forward(q, k, v, 0.4, True, window=Nk + 3)
+    np.testing.assert_allclose(o_w, o_c, atol=1e-12)
+    np.testing.assert_allclose(l_w, l_c, atol=1e-12)
+    o1, l1 = naive.forward(q, k, v, 0.4, True, window=1)
+    for i in range(Nq):
+        j = i + off
+        if 0 <= j < Nk:
+            np.testing.assert_allclose(o1[:, i], v[:, j], atol=1e-12)
+            np.testing.assert_allclose(l1[:, i], 0.4 * (q[:, i] * k[:, j]).sum(-1), atol=1e-12)
+        else:
+            assert np.all(o1[:, i] == 0) and np.all(np.isneginf(l1[:, i]))
+    for w in (2, 3, 5):
+        o, lse, p = naive.forward(q, k, v, 0.4, True, window=w, return_p=True)
+        band = torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=off) & ~torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=off - w)
+        has = band.any(-1).numpy()
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[:, has]), torch.from_numpy(k), torch.from_numpy(v), attn_mask=band[has], scale=0.4)
+        np.testing.assert_allclose(o[:, has], ref.numpy(), atol=1e-12)
+        np.testing.assert_allclose(p[:, has].sum(-1), 1.0, atol=1e-12)
+        assert (p[:, ~has] == 0).all()
+
+
+def test_sliding_window_backward_finite_differences():
+    def fwd_w(q, k, v, s, c):
+        return naive.forward(q, k, v, s, c, window=3)
+    def bwd_w(q, k, v, do, s, c):
+        return naive.backward(q, k, v, do, s, c, window=3)
+    check_finite_differences(bwd_w, fwd_w)
+
+
 # ---------------------------------------------------------------- mutation check
 def _mutant_forward(kind):
     def fwd(q, k, v, scale, causal=False, return_p=False):
