@@ -173,6 +173,28 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale=None, num_spl
     return o, lse
 
 
+def fa_fwd_window(q, k, v, o, lse, B, H, Nq, Nk, d, scale, window, stream=None):
+    fn = load().fa_fwd_window
+    if fn.argtypes is None:
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        fn.argtypes = [vp] * 5 + [i] * 5 + [ctypes.c_float, i, vp]
+        fn.restype = i
+    _raise(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(scale), int(window),
+              _stream(stream)), "fa_fwd_window")
+
+
+def fa_bwd_window(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, window, workspace,
+                  workspace_bytes, stream=None):
+    fn = load().fa_bwd_window
+    if fn.argtypes is None:
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        fn.argtypes = [vp] * 9 + [i] * 5 + [ctypes.c_float, i, vp, ctypes.c_size_t, vp]
+        fn.restype = i
+    _raise(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Nq,
+              Nk, d, float(scale), int(window), _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "fa_bwd_window")
+
+
 def fa_selftest_wait_timeout(timeout_ns, stream=None):
     """Launch the watchdog self-test kernel (a wait that must run out)."""
     fn = load().fa_selftest_wait_timeout

@@ -148,8 +148,11 @@ const char* fa_status_string(int st) {
     }
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
-           int Nk, int d, float scale, int causal, void* stream) {
+}  // extern "C"
+
+namespace {
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+             int d, float scale, int causal, int window, void* stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
@@ -173,8 +176,23 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     a.d = d;
     a.scale = scale;
     a.causal = causal;
+    a.window = window;
     a.timeout_ns = g_timeout_ns.load();
     return launch_fwd(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+           int Nk, int d, float scale, int causal, void* stream) {
+    return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 0, stream);
+}
+
+int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                  int Nk, int d, float scale, int window, void* stream) {
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, 1, window, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
@@ -220,19 +238,16 @@ int bwd_prepare(BwdLaunch* a, const void* q, const void* k, const void* v, const
     a->d = d;
     a->scale = scale;
     a->causal = causal;
+    a->window = 0;
     a->timeout_ns = g_timeout_ns.load();
     return FA_OK;
 }
 
 int launched(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
-}  // namespace
-
-extern "C" {
-
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-           void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
-           void* workspace, size_t workspace_bytes, void* stream) {
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+             void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+             int window, void* workspace, size_t workspace_bytes, void* stream) {
     if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     int st = check_shape(B, H, Nq, Nk, d);
     if (st != FA_OK) return st;
@@ -242,10 +257,30 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     st = bwd_prepare(&a, q, k, v, o, lse, static_cast<float*>(workspace), dO, dq, dk, dv, B, H, Nq, Nk, d,
                      scale, causal, true);
     if (st != FA_OK) return st;
+    a.window = window;
     cudaStream_t s = (cudaStream_t)stream;
     if ((st = launched(launch_bwd_pre(a, s))) != FA_OK) return st;
     if ((st = launched(launch_bwd_dkdv(a, s))) != FA_OK) return st;
     return launched(launch_bwd_dq(a, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+           void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+           void* workspace, size_t workspace_bytes, void* stream) {
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, 0, workspace,
+                    workspace_bytes, stream);
+}
+
+int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int window,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, 1, window, workspace,
+                    workspace_bytes, stream);
 }
 
 int fa_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H, int Nq, int d, void* stream) {

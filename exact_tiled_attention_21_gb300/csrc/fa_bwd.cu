@@ -62,6 +62,7 @@ struct BwdParams {
     const float* lse;
     const float* delta;
     int BH, Nq, Nk, causal, n_qt, n_kt;
+    int window;  // > 0: causal sliding window of this many keys
     float scale, scale_log2;
     DevError* err;
     uint64_t timeout_ns;
@@ -222,7 +223,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const int first_q = kt * 128 - off;  // smallest query that sees key kt*128
         i0 = first_q <= 0 ? 0 : first_q / 128;
     }
-    const int n = i0 < p.n_qt ? p.n_qt - i0 : 0;
+    int i_end = p.n_qt;
+    if (p.window > 0) {  // the last query that sees the tile's last key
+        const long long qlast = (long long)kt * 128 + 127 - off + p.window - 1;
+        i_end = qlast < 0 ? 0 : (int)min((long long)p.n_qt, qlast / 128 + 1);
+    }
+    const int n = i0 < i_end ? i_end - i0 : 0;
     const uint32_t sK = s_base + C::OFF_FIXED, sV = sK + C::TILE;
     auto sQ = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
     auto sDO = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
@@ -364,6 +370,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             // masked entries: rows past Nk (whole row) and, causal, columns c < cmin.
             // Tiles with none in the warp take the instantiation without the test.
             const int cmin_eff = row_ok ? cmin : (1 << 30);
+            // sliding window: queries c > cmax_w no longer see key kg
+            const int cmax_w = p.window > 0 ? kg - off + p.window - 1 - i * 128 - 64 * h : (1 << 30);
             auto p_phase = [&](auto MASK) {
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
@@ -381,14 +389,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                                            make_float2(sc, sc), make_float2(-lv[2 * e], -lv[2 * e + 1]));
                     float a = ex2(x.x), b = ex2(x.y);
                     if constexpr (decltype(MASK)::value) {
-                        if (c0 < cmin_eff) a = 0.f;
-                        if (c0 + 1 < cmin_eff) b = 0.f;
+                        if (c0 < cmin_eff || c0 > cmax_w) a = 0.f;
+                        if (c0 + 1 < cmin_eff || c0 + 1 > cmax_w) b = 0.f;
                     }
                     pp[q4 * 16 + e] = pack_bf16(a, b);
                 }
             }
             };
-            if (__any_sync(0xffffffffu, cmin_eff > 0))
+            if (__any_sync(0xffffffffu, cmin_eff > 0 || cmax_w < 63))
                 p_phase(std::true_type{});
             else
                 p_phase(std::false_type{});
@@ -482,6 +490,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const long long lim = (long long)qmax + off;
         n = lim < 0 ? 0 : min(p.n_kt, (int)(lim / 128) + 1);
     }
+    int jlo = 0;  // sliding window: first key tile the tile's first query sees
+    if (p.window > 0) {
+        const long long lo = (long long)it * 128 + off - p.window + 1;
+        jlo = lo <= 0 ? 0 : (int)min((long long)n, lo / 128);
+    }
+    n -= jlo;
     static_assert(NST * 2 * C::TILE <= C::OFF_VEC, "K/V stages fit below the vector region");
     auto sK = [&](int st) { return s_base + st * 2 * C::TILE; };
     auto sV = [&](int st) { return s_base + st * 2 * C::TILE + C::TILE; };
@@ -498,8 +512,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                 if (!mbar_wait(B_STE + 8 * st, ph ^ 1, ctl, kSiteBwdQEmpty)) break;
                 mbar_arrive_expect_tx(B_STF + 8 * st, 2 * C::TILE);
                 for (int c = 0; c < C::KCH; ++c) {
-                    tma_load_3d(sK(st) + c * C::CHUNK, &map_k, B_STF + 8 * st, c * 64, jj * 128, bh, pol);
-                    tma_load_3d(sV(st) + c * C::CHUNK, &map_v, B_STF + 8 * st, c * 64, jj * 128, bh, pol);
+                    tma_load_3d(sK(st) + c * C::CHUNK, &map_k, B_STF + 8 * st, c * 64, (jlo + jj) * 128, bh, pol);
+                    tma_load_3d(sV(st) + c * C::CHUNK, &map_v, B_STF + 8 * st, c * 64, (jlo + jj) * 128, bh, pol);
                 }
                 issued |= 1u << st;
                 issued_par = (issued_par & ~(1u << st)) | (ph << st);
@@ -586,7 +600,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
         bool ok = true;
         for (int jj = 0; jj < n; ++jj) {
-            const int cmax = lim_row - jj * 128 - 64 * h;  // columns > cmax are masked
+            const int kb = (jlo + jj) * 128 + 64 * h;           // key of this warpgroup's column 0
+            const int cmax = lim_row - kb;                       // columns > cmax are masked
+            const int cmin_w = p.window > 0 ? qg + off - p.window + 1 - kb : -(1 << 30);  // and < cmin_w
             if (!(ok = mbar_wait(B_S, jj & 1, ctl, kSiteBwdS))) break;
             tc_fence_after();
             uint32_t pp[32];
@@ -608,14 +624,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                                            make_float2(sc, sc), make_float2(-l2, -l2));
                     float a = ex2(x.x), b = ex2(x.y);
                     if constexpr (decltype(MASK)::value) {
-                        if (c0 > cmax) a = 0.f;
-                        if (c0 + 1 > cmax) b = 0.f;
+                        if (c0 > cmax || c0 < cmin_w) a = 0.f;
+                        if (c0 + 1 > cmax || c0 + 1 < cmin_w) b = 0.f;
                     }
                     pp[q4 * 16 + e] = pack_bf16(a, b);
                 }
             }
             };
-            if (__any_sync(0xffffffffu, cmax < 63))
+            if (__any_sync(0xffffffffu, cmax < 63 || cmin_w > 0))
                 p_phase(std::true_type{});
             else
                 p_phase(std::false_type{});
@@ -670,6 +686,7 @@ BwdParams make_params(const BwdLaunch& a) {
     p.Nq = a.Nq;
     p.Nk = a.Nk;
     p.causal = a.causal;
+    p.window = a.window;
     p.n_qt = (a.Nq + 127) / 128;
     p.n_kt = (a.Nk + 127) / 128;
     p.scale = a.scale;

@@ -231,6 +231,7 @@ decode_paged_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
     __shared__ float s_p[G][kDecPiece];
     __shared__ float s_red[kDecThreads / 32][G];
     __shared__ float s_acc[KPC][D + 4];
+    __shared__ long long s_row[kDecPiece];  // element offset of each key row of the piece (-1: bad page)
     __shared__ int s_bad;
 
     int idx = blockIdx.x;
@@ -275,12 +276,6 @@ decode_paged_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
         }
     }
     const int* trow = table + (size_t)b * max_pages;
-    // element offset of logical token t's row for this kv head, or -1 if its page is invalid
-    auto row_off = [&](int t) -> long long {
-        const int pg = trow[t / page];
-        if (pg < 0 || pg >= num_pages) return -1;
-        return (((long long)pg * Hkv + kvh) * page + (t % page)) * D + slice * 8;
-    };
     float m_run[G], l_run[G], acc[G][8];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
@@ -291,16 +286,24 @@ decode_paged_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
     }
     bool bad = false;
     for (int p0 = k0; p0 < k1; p0 += kDecPiece) {
+        {   // one block-table lookup per key of the piece (thread = key), shared by the K and V loads
+            const int key = p0 + tid;
+            long long off = -1;
+            if (key < k1) {
+                const int pg = trow[key / page];
+                if (pg >= 0 && pg < num_pages)
+                    off = (((long long)pg * Hkv + kvh) * page + (key % page)) * D;
+                else
+                    bad = true;
+            }
+            s_row[tid] = off;
+        }
+        __syncthreads();
         uint4 kr[STEPS];
 #pragma unroll
         for (int s2 = 0; s2 < STEPS; ++s2) {
-            const int key = p0 + s2 * KPC + group;
-            kr[s2] = make_uint4(0, 0, 0, 0);
-            if (key < k1) {
-                const long long off = row_off(key);
-                if (off >= 0) kr[s2] = __ldg(reinterpret_cast<const uint4*>(kp + off));
-                else bad = true;
-            }
+            const long long off = s_row[s2 * KPC + group];
+            kr[s2] = off >= 0 ? __ldg(reinterpret_cast<const uint4*>(kp + off + slice * 8)) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int s2 = 0; s2 < STEPS; ++s2) {
@@ -367,12 +370,8 @@ decode_paged_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
         uint4 vr[STEPS];
 #pragma unroll
         for (int s2 = 0; s2 < STEPS; ++s2) {
-            const int key = p0 + s2 * KPC + group;
-            vr[s2] = make_uint4(0, 0, 0, 0);
-            if (key < k1) {
-                const long long off = row_off(key);
-                if (off >= 0) vr[s2] = __ldg(reinterpret_cast<const uint4*>(vp + off));
-            }
+            const long long off = s_row[s2 * KPC + group];
+            vr[s2] = off >= 0 ? __ldg(reinterpret_cast<const uint4*>(vp + off + slice * 8)) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int s2 = 0; s2 < STEPS; ++s2) {

@@ -57,6 +57,7 @@ struct FwdParams {
     __nv_bfloat16* o;
     float* lse;
     int BH, Nq, Nk, causal;
+    int window;  // > 0: causal sliding window of this many keys
     int n_mtiles, num_work;
     float scale_log2;
     DevError* err;
@@ -72,6 +73,15 @@ __device__ __forceinline__ int fwd_num_kv(const FwdParams& p, int row0) {
     return min(kv_total, (int)(lim / 128) + 1);
 }
 
+// First key block a work tile needs: with a sliding window, the block of the
+// first visible key of its first row.
+template <bool WIN>
+__device__ __forceinline__ int fwd_kv_first(const FwdParams& p, int row0) {
+    if (!WIN || p.window <= 0) return 0;
+    const long long lo = (long long)row0 + p.Nk - p.Nq - p.window + 1;
+    return lo <= 0 ? 0 : (int)(lo / 128);
+}
+
 // Work tile w -> (bh, first row).  Causal: heaviest row tiles first.
 __device__ __forceinline__ void fwd_decode(const FwdParams& p, int w, int& bh, int& row0) {
     const int mr = w / p.BH;
@@ -82,10 +92,10 @@ __device__ __forceinline__ void fwd_decode(const FwdParams& p, int w, int& bh, i
 
 // Pass 1 over one 128-column S row in TMEM (thread = row): the maximum of the
 // raw scores.  Chunks of 32 columns are double-buffered (the next loads while
-// this one is scanned).  MASKED: columns c > lim2 are excluded; instantiated
-// only for the blocks that hold a masked column.
+// this one is scanned).  MASKED: columns c > lim2 or c < lo2 are excluded;
+// instantiated only for the blocks that hold a masked column.
 template <bool MASKED>
-__device__ __forceinline__ float row_max_pass(uint32_t taddr, int lim2) {
+__device__ __forceinline__ float row_max_pass(uint32_t taddr, int lim2, int lo2) {
     float mraw = -INFINITY;
     uint32_t va[32], vb[32];
     tmem_ld32_async(taddr, va);
@@ -99,8 +109,8 @@ __device__ __forceinline__ float row_max_pass(uint32_t taddr, int lim2) {
         for (int i = 0; i < 32; i += 2) {
             float x0 = __uint_as_float(v[i]), x1 = __uint_as_float(v[i + 1]);
             if constexpr (MASKED) {
-                if (q4 * 32 + i > lim2) x0 = -INFINITY;
-                if (q4 * 32 + i + 1 > lim2) x1 = -INFINITY;
+                if (q4 * 32 + i > lim2 || q4 * 32 + i < lo2) x0 = -INFINITY;
+                if (q4 * 32 + i + 1 > lim2 || q4 * 32 + i + 1 < lo2) x1 = -INFINITY;
             }
             mraw = fmax3(mraw, x0, x1);
         }
@@ -113,7 +123,7 @@ __device__ __forceinline__ float row_max_pass(uint32_t taddr, int lim2) {
 // over the S columns already read (keys [32 q, 32 q + 32) to columns
 // [16 q, 16 q + 16); the load in flight is always of columns >= 32 (q + 1)).
 template <bool MASKED>
-__device__ __forceinline__ float exp_pass(uint32_t taddr, int lim2, float c, float msub) {
+__device__ __forceinline__ float exp_pass(uint32_t taddr, int lim2, int lo2, float c, float msub) {
     float2 rs = make_float2(0.f, 0.f);
     const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
     uint32_t va[32], vb[32];
@@ -129,8 +139,8 @@ __device__ __forceinline__ float exp_pass(uint32_t taddr, int lim2, float c, flo
         for (int i = 0; i < 16; ++i) {
             float s0 = __uint_as_float(v[2 * i]), s1 = __uint_as_float(v[2 * i + 1]);
             if constexpr (MASKED) {
-                if (q4 * 32 + 2 * i > lim2) s0 = -INFINITY;
-                if (q4 * 32 + 2 * i + 1 > lim2) s1 = -INFINITY;
+                if (q4 * 32 + 2 * i > lim2 || q4 * 32 + 2 * i < lo2) s0 = -INFINITY;
+                if (q4 * 32 + 2 * i + 1 > lim2 || q4 * 32 + 2 * i + 1 < lo2) s1 = -INFINITY;
             }
             const float2 x = ffma2(make_float2(s0, s1), c2, nm2);  // s*c - m, two lanes
             const float2 e = make_float2(ex2(x.x), ex2(x.y));
@@ -144,7 +154,9 @@ __device__ __forceinline__ float exp_pass(uint32_t taddr, int lim2, float c, flo
     return rs.x + rs.y;
 }
 
-template <int D>
+// WIN: the sliding-window variant (a separate instantiation, so the plain
+// path carries none of its bounds).
+template <int D, bool WIN>
 __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
@@ -207,7 +219,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             for (int w = blockIdx.x; w < p.num_work && ok; w += gridDim.x) {
                 int bh, row0;
                 fwd_decode(p, w, bh, row0);
-                const int n = fwd_num_kv(p, row0);
+                const int jlo = fwd_kv_first<WIN>(p, row0);
+                const int n = max(0, fwd_num_kv(p, row0) - jlo);
                 if (n == 0) continue;
                 if (q_iter > 0 && !mbar_wait(BAR_QE, (q_iter - 1) & 1, ctl, kSiteQEmpty)) break;
                 mbar_arrive_expect_tx(BAR_QF, 2 * C::Q_BYTES);
@@ -226,7 +239,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                         const uint32_t dst = s_base + C::OFF_KV + slot * C::KV_BYTES;
                         for (int c = 0; c < C::KCH; ++c)
                             tma_load_3d(dst + c * C::CHUNK_BYTES, kv == 0 ? &map_k : &map_v,
-                                        bar_kvf(slot), c * 64, j * 128, bh, pol_kv);
+                                        bar_kvf(slot), c * 64, (jlo + j) * 128, bh, pol_kv);
                         issued |= 1u << slot;
                         issued_par = (issued_par & ~(1u << slot)) | (phase << slot);
                         if (++slot == C::NSLOT) {
@@ -274,7 +287,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             for (int w = blockIdx.x; w < p.num_work && ok; w += gridDim.x) {
                 int bh, row0;
                 fwd_decode(p, w, bh, row0);
-                const int n = fwd_num_kv(p, row0);
+                const int n = max(0, fwd_num_kv(p, row0) - fwd_kv_first<WIN>(p, row0));
                 if (n == 0) continue;
                 if (!mbar_wait(BAR_QF, q_iter & 1, ctl, kSiteQFull)) break;
                 ++q_iter;
@@ -342,7 +355,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         for (int w = blockIdx.x; w < p.num_work; w += gridDim.x) {
             int bh, row0;
             fwd_decode(p, w, bh, row0);
-            const int n = fwd_num_kv(p, row0);
+            const int jlo = fwd_kv_first<WIN>(p, row0);
+            const int n = max(0, fwd_num_kv(p, row0) - jlo);
             const int tile_row0 = row0 + t * 128;
             const int row = tile_row0 + r;
             float m_use = -INFINITY, l = 0.f;
@@ -352,13 +366,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 ++s_iter;
                 tc_fence_after();
                 // pass 1: row maximum of the raw scores (scale > 0 commutes with max)
-                const int kbase = j * 128;
-                const bool masked = kbase + 128 > p.Nk || (p.causal && kbase + 127 > tile_row0 + off);
+                const int kbase = (jlo + j) * 128;
+                const bool masked = kbase + 128 > p.Nk || (p.causal && kbase + 127 > tile_row0 + off) ||
+                                    (WIN && kbase < tile_row0 + 127 + off - p.window + 1);
                 const int lim = p.causal ? min(row + off, p.Nk - 1) : p.Nk - 1;
                 const int lim2 = lim - kbase;  // last visible column of this block
+                // first visible column (sliding window), far below 0 without one
+                const int lo2 = WIN ? row + off - p.window + 1 - kbase : -(1 << 30);
                 // uniform over the warpgroup: masked blocks take the instantiation with the mask
-                const float mraw = masked ? row_max_pass<true>(lane_addr + col_s, lim2)
-                                          : row_max_pass<false>(lane_addr + col_s, lim2);
+                const float mraw = masked ? row_max_pass<true>(lane_addr + col_s, lim2, lo2)
+                                          : row_max_pass<false>(lane_addr + col_s, lim2, lo2);
                 const float m_new = fmaxf(m_use, mraw * c);
                 if (j == 0) {
                     m_use = m_new;
@@ -378,8 +395,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 }
                 const float msub = (m_use == -INFINITY) ? 0.f : m_use;
                 // pass 2: p = 2^(s*c - m), row sum, bf16 P over the S columns already read
-                const float rsum = masked ? exp_pass<true>(lane_addr + col_s, lim2, c, msub)
-                                          : exp_pass<false>(lane_addr + col_s, lim2, c, msub);
+                const float rsum = masked ? exp_pass<true>(lane_addr + col_s, lim2, lo2, c, msub)
+                                          : exp_pass<false>(lane_addr + col_s, lim2, lo2, c, msub);
                 l += rsum;
                 tc_fence_before();
                 mbar_arrive(bar_p);
@@ -430,11 +447,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     }
 }
 
-template <int D>
-cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
+template <int D, bool WIN>
+cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
     using C = Fwd<D>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess) return e;
     FwdParams p;
@@ -444,14 +461,20 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
     p.Nq = a.Nq;
     p.Nk = a.Nk;
     p.causal = a.causal;
+    p.window = a.window;
     p.n_mtiles = (a.Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
     p.num_work = p.n_mtiles * p.BH;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
     p.timeout_ns = a.timeout_ns;
     const int grid = p.num_work < a.num_sms ? p.num_work : a.num_sms;
-    fwd_kernel<D><<<grid, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, p);
+    fwd_kernel<D, WIN><<<grid, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
+    return a.window > 0 ? launch_fwd_dw<D, true>(a, s) : launch_fwd_dw<D, false>(a, s);
 }
 
 }  // namespace

@@ -17,6 +17,7 @@ struct FwdLaunch {
     int B, H, Nq, Nk, d;
     float scale;
     int causal;
+    int window;  // > 0: causal sliding window (keys per query)
     int num_sms;
     DevError* err;
     uint64_t timeout_ns;
@@ -36,6 +37,7 @@ struct BwdLaunch {
     int B, H, Nq, Nk, d;
     float scale;
     int causal;
+    int window;  // > 0: causal sliding window (keys per query)
     int num_sms;
     DevError* err;
     uint64_t timeout_ns;

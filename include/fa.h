@@ -64,6 +64,14 @@ typedef enum {
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int Nq, int Nk, int d, float scale, int causal, void *stream);
 
+/* Causal sliding-window forward: like fa_fwd with causal = 1, except that
+ * query i sees only the `window` (>= 1) keys ending at its diagonal, keys j
+ * with i + Nk - Nq - window < j <= i + Nk - Nq (the fixed-window local
+ * attention of johe.ru "Flash Attention: ...", section "Альтернативы").  Only
+ * the key blocks inside a tile's window are loaded and multiplied. */
+int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int H, int Nq, int Nk, int d, float scale, int window, void *stream);
+
 /* Bytes of fp32 workspace fa_bwd needs: the row terms D [B,H,Nq] (dQ is
  * accumulated on chip, in a pass of its own).  Returns 0 for invalid sizes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
@@ -83,6 +91,12 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            const void *dO, void *dq, void *dk, void *dv,
            int B, int H, int Nq, int Nk, int d, float scale, int causal,
            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward of fa_fwd_window (same window, same conventions as fa_bwd). */
+int fa_bwd_window(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                  const void *dO, void *dq, void *dk, void *dv,
+                  int B, int H, int Nq, int Nk, int d, float scale, int window,
+                  void *workspace, size_t workspace_bytes, void *stream);
 
 /* The three steps of fa_bwd, for callers that schedule them (or time them)
  * separately; fa_bwd is exactly these three launches in this order.
