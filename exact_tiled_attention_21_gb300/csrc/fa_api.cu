@@ -3,6 +3,7 @@
 // fallback: every call either launches the GPU kernels or returns an error.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <mutex>
@@ -72,6 +73,27 @@ int make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
                      es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// Tiled map of any rank (bf16, 128-byte swizzle, zero fill out of range).
+// strides: bytes of dims 1..rank-1.
+int make_map_nd(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                const cuuint32_t* box) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int st = encoder(&enc);
+    if (st != FA_OK) return st;
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// Page sizes the tensor-core paged decode takes: whole 8-row swizzle atoms
+// per page, and pages that tile a 128-key stage (or stages that tile a page).
+bool paged_mma_ok(int B, int d, int page) {
+    if (B > 2048 || d != 128 || page % 8 != 0) return false;  // lengths of up to 2048 sequences staged on chip
+    return page <= 128 ? (128 % page == 0) : (page % 128 == 0);
 }
 
 // Shared shape checks.  Sizes must keep every element index below 2^31 per
@@ -393,6 +415,26 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, con
     a.d = d;
     a.splits = num_splits;
     a.scale = scale;
+    a.mma = paged_mma_ok(B, d, page_size);
+    if (a.mma) {
+        if (device_state(nullptr, &a.num_sms) != FA_OK) return FA_ERR_CUDA;
+        a.timeout_ns = g_timeout_ns.load();
+        const cuuint64_t qd[3] = {(cuuint64_t)d, (cuuint64_t)B * Hq, 1};
+        const cuuint64_t qs[2] = {(cuuint64_t)d * 2, (cuuint64_t)B * Hq * d * 2};
+        const cuuint32_t qb[3] = {64, 16, 1};
+        const cuuint64_t kd[4] = {(cuuint64_t)d, (cuuint64_t)page_size, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
+        const cuuint64_t ks[3] = {(cuuint64_t)d * 2, (cuuint64_t)page_size * d * 2,
+                                  (cuuint64_t)Hkv * page_size * d * 2};
+        const cuuint32_t kb[4] = {64, (cuuint32_t)std::min(page_size, 128), 1, 1};
+        // V: the feature dimension as (64, half) so one box holds a page's rows of both halves
+        const cuuint64_t vd[5] = {64, (cuuint64_t)page_size, 2, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
+        const cuuint64_t vs[4] = {(cuuint64_t)d * 2, 128, (cuuint64_t)page_size * d * 2,
+                                  (cuuint64_t)Hkv * page_size * d * 2};
+        const cuuint32_t vb[5] = {64, (cuuint32_t)std::min(page_size, 128), 2, 1, 1};
+        if (make_map_nd(&a.map_q, q, 3, qd, qs, qb) || make_map_nd(&a.map_k, k_pages, 4, kd, ks, kb) ||
+            make_map_nd(&a.map_v, v_pages, 5, vd, vs, vb))
+            return FA_ERR_CUDA;
+    }
     return launch_decode_paged(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -446,7 +446,17 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
 }
 
 cudaError_t launch_decode_paged(const PagedDecodeLaunch& a, cudaStream_t s) {
+    if (a.mma) return launch_decode_paged_mma(a, s);
     return a.d == 128 ? launch_paged_d<128>(a, s) : launch_paged_d<64>(a, s);
+}
+
+cudaError_t launch_decode_combine(const float* part_o, const float* part_lse, void* o, float* lse, int BH,
+                                  int splits, int d, cudaStream_t s) {
+    if (d == 128)
+        decode_combine_kernel<128><<<(BH + 3) / 4, 128, 0, s>>>(part_o, part_lse, (__nv_bfloat16*)o, lse, BH, splits);
+    else
+        decode_combine_kernel<64><<<(BH + 3) / 4, 128, 0, s>>>(part_o, part_lse, (__nv_bfloat16*)o, lse, BH, splits);
+    return cudaGetLastError();
 }
 
 }  // namespace fa

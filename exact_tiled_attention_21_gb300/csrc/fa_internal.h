@@ -68,6 +68,13 @@ struct PagedDecodeLaunch {
     int B, Hq, Hkv, page, max_pages, num_pages, d, splits;
     float scale;
     DevError* err;
+    // tensor-core path only (d = 128, page a multiple of 8 that divides 128 or is a multiple of it):
+    bool mma;
+    CUtensorMap map_q;         // 3-D (d, B*Hq, 1), box (64, 16, 1), 128B swizzle
+    CUtensorMap map_k;         // 4-D (d, page, Hkv, num_pages), box (64, min(page,128), 1, 1), 128B swizzle
+    CUtensorMap map_v;         // 5-D (64, page, 2, Hkv, num_pages), box (64, min(page,128), 2, 1, 1), 128B swizzle
+    int num_sms;
+    uint64_t timeout_ns;
 };
 
 // Each returns a cudaError_t of the launch (cudaSuccess when queued).
@@ -77,6 +84,10 @@ cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s);  // dK, dV
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s);    // dQ
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_paged(const PagedDecodeLaunch& a, cudaStream_t s);
+cudaError_t launch_decode_paged_mma(const PagedDecodeLaunch& a, cudaStream_t s);
+// LSE-weighted merge of per-split partials into o (bf16) and lse (fp32, may be null).
+cudaError_t launch_decode_combine(const float* part_o, const float* part_lse, void* o, float* lse, int BH,
+                                  int splits, int d, cudaStream_t s);
 
 // Rows of the forward's CTA work tile (two 128-row softmax tiles).
 constexpr int kFwdRowsPerCta = 256;

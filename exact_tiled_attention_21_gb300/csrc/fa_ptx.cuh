@@ -24,7 +24,8 @@ struct DevError {
 enum : int {
     kSiteQFull = 1, kSiteQEmpty, kSiteKvFull, kSiteKvEmpty, kSiteSFull, kSitePFull, kSiteOFinal,
     kSiteTeardown, kSiteBwdQFull, kSiteBwdQEmpty, kSiteBwdKvFull, kSiteBwdS, kSiteBwdP, kSiteBwdDP,
-    kSiteBwdDS, kSiteBwdDQ, kSiteBwdDone, kSiteAlign, kSiteProbe, kSitePagedTable
+    kSiteBwdDS, kSiteBwdDQ, kSiteBwdDone, kSiteAlign, kSiteProbe, kSitePagedTable,
+    kSitePagedQ, kSitePagedKv, kSitePagedS, kSitePagedP, kSitePagedPv, kSitePagedO
 };
 
 constexpr int kErrTimeout = -6;
@@ -91,6 +92,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same condition (never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits until the phase of parity `parity` of barrier `bar` has completed.
 // Gives up after ctl.timeout_ns (records kErrTimeout at `site`) or as soon as
 // another role of the CTA has given up.  Returns false when it gave up.
@@ -137,6 +151,26 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+// 4-D tiled load (paged caches: element, row within the page, head, page).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+        : "memory");
+}
+
+// 5-D tiled load (paged caches with the feature dimension split in halves).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3, int c4, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "l"(policy)
         : "memory");
 }
 
@@ -239,6 +273,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// TMEM -> registers, 32 lanes x 16 columns, waited for.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : FA_R8(0), FA_R8(8)
+        : "r"(taddr)
+        : "memory");
+}
+
 // The same load without its wait: up to two loads may be in flight; the
 // registers are valid only after tmem_wait_ld on them.
 __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
@@ -294,6 +339,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 #undef FA_W8
+
+// Named barrier `id` over `n` threads (a multiple of 32) that also returns the
+// AND of `pred` over them: the same answer in every participating thread.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
 
 // ------------------------------------------------------------------ math
 __device__ __forceinline__ float ex2(float x) {

@@ -48,6 +48,24 @@ def check_out(o, lse, o_ref, lse_ref, what="", max_abs=FWD_MAX_ABS):
     return float(err.max()), float(err.mean())
 
 
+def check_out_elementwise(o, lse, o_ref, lse_ref, vmax, what=""):
+    """Per-element bound for peaked softmaxes, where |O| ~ |v|: the output's
+    own bf16 rounding (half an ulp, <= 2^-8 |O|) plus the bf16 rounding of
+    the weights before the value product (<= 2^-9 max|V|), plus 1e-4 for
+    fp32 accumulation.  The flat max/mean tolerances assume |O| << 1."""
+    o = np.asarray(o, dtype=np.float64)
+    assert np.isfinite(o).all(), "%s: non-finite output" % what
+    bound = 2.0 ** -8 * np.abs(o_ref) + 2.0 ** -9 * vmax + 1e-4
+    excess = np.abs(o - o_ref) - bound
+    assert excess.max() <= 0, "%s: |O-O_ref| exceeds the rounding bound by %g" % (what, excess.max())
+    if lse is not None:
+        fin = ~np.isneginf(lse_ref)
+        assert np.array_equal(np.isneginf(np.asarray(lse)), ~fin), "%s: -inf LSE pattern differs" % what
+        if fin.any():
+            le = np.abs(np.asarray(lse, dtype=np.float64)[fin] - lse_ref[fin]).max()
+            assert le <= LSE_ABS, "%s: max |LSE-LSE_ref| = %g" % (what, le)
+
+
 def check_grad(g, g_ref, what="", cancel_scale=None):
     """max |g - g_ref| <= GRAD_REL * max |g_ref|.
 

@@ -10,7 +10,7 @@ import torch
 import exact_tiled_attention_21_gb300 as fa_mod
 from exact_tiled_attention_21_gb300 import synthetic as syn
 from oracle import naive
-from tests.parity import check_out, f64
+from tests.parity import check_out, check_out_elementwise, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -45,6 +45,13 @@ CASES = [
     (2, 4, 4, 8, [129, 1], 64, 3),              # one query head per kv head
     (1, 4, 2, 1, [77], 128, 16),                # single-token pages
     (2, 4, 2, 16, [5, 3], 128, 16),             # more splits than tokens: empty splits
+    (2, 32, 2, 8, [1000, 129], 128, 5),         # 8-token pages, group of 16 (one full MMA group)
+    (2, 8, 2, 128, [700, 128], 128, 3),         # one page per 128-key stage
+    (2, 8, 2, 256, [1000, 300], 128, 2),        # pages longer than a stage
+    (1, 32, 1, 16, [517], 128, 4),              # multi-query, 32 heads: two groups of 16
+    (1, 40, 2, 32, [333], 128, 2),              # group of 20: 16 + 4 heads
+    (1, 8, 2, 48, [500], 128, 3),               # 48-token pages (not a divisor of 128)
+    (1, 8, 2, 16, [20000], 128, 1),             # one split: 157 stages through the ring
 ]
 
 
@@ -91,3 +98,41 @@ def test_paged_decode_rejects_bad_page_index_on_device(cuda_lib):
     st, detail = cuda_lib.fa_get_last_device_error()
     assert st == fa_mod.FA_ERR_INVALID_ARG, detail
     assert cuda_lib.fa_get_last_device_error()[0] == 0
+
+
+@pytest.mark.parametrize("P", [16, 48, 256])
+def test_paged_decode_ignores_unused_slots(cuda_lib, P):
+    """Tokens past seq_lens[b] in the last page, and pages no table names,
+    may hold anything (NaN here): the result depends only on the tokens in
+    range."""
+    lens = [P * 3 + 5, 1, 2 * P]
+    q, kp, vp, table, L = _case(31 + P, 3, 8, 2, P, lens, 128)
+    kp_bad, vp_bad = kp.clone(), vp.clone()
+    used = np.zeros((kp.shape[0], P), dtype=bool)
+    for b, n in enumerate(lens):
+        for t in range(n):
+            used[table[b, t // P], t % P] = True
+    mask = torch.from_numpy(~used)[:, None, :, None].expand_as(kp)
+    kp_bad[mask] = float("nan")
+    vp_bad[mask] = float("nan")
+    o, lse = _run(cuda_lib, q, kp_bad, vp_bad, table, L, 4)
+    o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(128))
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    check_out(f64(o), f64(lse), o_ref, lse_ref, "unused slots P%d" % P)
+
+
+def test_paged_decode_growing_scores(cuda_lib):
+    """Key norms that grow along the sequence raise every head's running
+    maximum by far more than 2^8 between stages, so the output accumulator
+    is rescaled many times within one split."""
+    B, Hq, Hkv, P, n = 1, 8, 2, 16, 3000
+    q, kp, vp, table, L = _case(44, B, Hq, Hkv, P, [n], 128)
+    ramp = torch.zeros(kp.shape[0], 1, P, 1)
+    for t in range(n):
+        ramp[table[0, t // P], 0, t % P, 0] = 0.5 + 12.0 * t / n
+    kp = (kp.float() * ramp).to(torch.bfloat16)
+    o, lse = _run(cuda_lib, q, kp, vp, table, L, 1)
+    o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(128))
+    # late keys dominate (|O| ~ |v|): the rounding bound per element applies
+    vmax = float(np.abs(f64(vp)).max())
+    check_out_elementwise(f64(o), f64(lse), o_ref, lse_ref, vmax, "growing scores")
