@@ -151,8 +151,12 @@ size_t fa_decode_paged_workspace_bytes(int B, int Hq, int d, int num_splits);
  *  seq_lens [B] int32, 1 <= seq_lens[b] <= max_pages * page_size;
  *  o [B, Hq, d] bf16; lse [B, Hq] fp32 or NULL.
  * Each sequence is cut into num_splits (1..256) contiguous chunks of
- * ceil(seq_lens[b] / num_splits) tokens, merged as in fa_decode.  Every K/V
- * row is read once per group of up to 4 query heads.  Host checks: Hq % Hkv
+ * ceil(seq_lens[b] / num_splits) tokens (rounded up to whole 128-token stages
+ * on the tensor-core path: d = 128, B <= 2048, page_size a multiple of 8 that
+ * divides 128 or is a multiple of 128), merged as in fa_decode.  Every K/V
+ * row is read once per group of up to 16 query heads on that path (4 on the
+ * general one).  Tokens past seq_lens[b] in a page are never used, whatever
+ * they hold.  Host checks: Hq % Hkv
  * == 0, d in {64, 128}, alignment, workspace.  The table and lengths live in
  * device memory and are checked by the kernel: a page index outside
  * [0, num_pages) or a length out of range is never dereferenced; it is read
