@@ -107,6 +107,42 @@ def backward(q, k, v, do, scale, causal=False, rows=None, Nq=None, window=0):
     return dq, dk, dv
 
 
+def forward_varlen(q, k, v, lens_q, lens_k, scale, causal=False):
+    """A padded batch of sequences of different lengths ([ZIMA] "Kernel-Fusion
+    ...": masking applied to the scores; here the mask is the sequence's own
+    extent).  q [B,H,Nq,d], k/v [B,H,Nk,d]; sequence b is q[b,:, :lens_q[b]]
+    against k/v[b,:, :lens_k[b]], with the bottom-right causal alignment of its
+    own lengths.  Rows past lens_q[b] are padding: O = 0, LSE = -inf."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Nq, _ = q.shape
+    O = np.zeros(q.shape[:-1] + (v.shape[-1],))
+    L = np.full((B, H, Nq), -np.inf)
+    for b in range(B):
+        nq, nk = int(lens_q[b]), int(lens_k[b])
+        if nq == 0:
+            continue
+        if nk == 0:  # no key at all: every row sees nothing
+            continue
+        o, lse = forward(q[b, :, :nq], k[b, :, :nk], v[b, :, :nk], scale, causal)
+        O[b, :, :nq] = o
+        L[b, :, :nq] = lse
+    return O, L
+
+
+def backward_varlen(q, k, v, do, lens_q, lens_k, scale, causal=False):
+    """Gradients of ``forward_varlen``: each sequence's slice as in ``backward``;
+    padding rows of dQ, dK and dV are zero."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(q.shape[0]):
+        nq, nk = int(lens_q[b]), int(lens_k[b])
+        if nq == 0 or nk == 0:
+            continue
+        g = backward(q[b, :, :nq], k[b, :, :nk], v[b, :, :nk], do[b, :, :nq], scale, causal)
+        dq[b, :, :nq], dk[b, :, :nk], dv[b, :, :nk] = g
+    return dq, dk, dv
+
+
 def decode(q, kcache, vcache, scale):
     """One query per (b, h) against its cache.  q [B,H,d], caches [B,H,Nk,d].
 

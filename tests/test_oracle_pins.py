@@ -399,6 +399,108 @@ def test_sliding_window_backward_finite_differences():
     check_finite_differences(bwd_w, fwd_w)
 
 
+# ---------------------------------------------------------------- per-sequence lengths
+VL_LENS = [(5, 7), (0, 4), (3, 0), (6, 2), (2, 9)]  # (len_q, len_k) per sequence; Nq = 6, Nk = 9
+
+
+def _vl_case(causal_dim=6):
+    B, H, Nq, Nk, d = len(VL_LENS), 2, 6, 9, causal_dim
+    q, k = RNG.standard_normal((B, H, Nq, d)), RNG.standard_normal((B, H, Nk, d))
+    v = RNG.standard_normal((B, H, Nk, 5))
+    lq = np.array([a for a, _ in VL_LENS]); lk = np.array([b for _, b in VL_LENS])
+    return q, k, v, lq, lk
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_closed_form_zero_query(causal):
+    """Q = 0: row i < len_q sees keys [0, len_k) (causal: [0, i + len_k - len_q])
+    with equal weights, so O_i is the mean of those V rows and LSE_i = ln(count);
+    a row with no key, and every row past len_q, has O = 0 and LSE = -inf."""
+    q, k, v, lq, lk = _vl_case()
+    o, lse = naive.forward_varlen(np.zeros_like(q), k, v, lq, lk, 0.7, causal)
+    for b, (nq, nk) in enumerate(VL_LENS):
+        for i in range(q.shape[2]):
+            cnt = 0 if i >= nq else (min(nk, i + nk - nq + 1) if causal else nk)
+            cnt = max(cnt, 0)
+            if cnt == 0:
+                assert np.all(o[b, :, i] == 0) and np.all(np.isneginf(lse[b, :, i]))
+            else:
+                np.testing.assert_allclose(o[b, :, i], v[b, :, :cnt].mean(axis=1), atol=1e-12)
+                np.testing.assert_allclose(lse[b, :, i], math.log(cnt), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_ignores_padding_and_matches_sdpa(causal):
+    """Values in padding positions change nothing; each valid row equals torch
+    SDPA with an explicit key-padding (and causal band) mask on the padded
+    tensors."""
+    q, k, v, lq, lk = _vl_case()
+    o, lse = naive.forward_varlen(q, k, v, lq, lk, 0.7, causal)
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    for b, (nq, nk) in enumerate(VL_LENS):
+        q2[b, :, nq:] = 1e3
+        k2[b, :, nk:] = -7.0
+        v2[b, :, nk:] = 5e2
+    o2, lse2 = naive.forward_varlen(q2, k2, v2, lq, lk, 0.7, causal)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    Nq, Nk = q.shape[2], k.shape[2]
+    for b, (nq, nk) in enumerate(VL_LENS):
+        i = torch.arange(Nq)[:, None]
+        j = torch.arange(Nk)[None, :]
+        mask = (j < nk) & (i < nq)
+        if causal:
+            mask &= j <= i + nk - nq
+        has = mask.any(-1).numpy()
+        if not has.any():
+            continue
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q2[b][:, has]), torch.from_numpy(k2[b]), torch.from_numpy(v2[b]),
+            attn_mask=mask[has], scale=0.7)
+        np.testing.assert_allclose(o[b][:, has], ref.numpy(), atol=1e-12)
+
+
+def test_varlen_full_lengths_equal_dense():
+    q, k, v, _, _ = _vl_case()
+    B, Nq, Nk = q.shape[0], q.shape[2], k.shape[2]
+    for causal in (False, True):
+        o, lse = naive.forward_varlen(q, k, v, [Nq] * B, [Nk] * B, 0.7, causal)
+        o2, lse2 = naive.forward(q, k, v, 0.7, causal)
+        np.testing.assert_allclose(o, o2, atol=1e-12)
+        np.testing.assert_allclose(lse, lse2, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_backward_finite_differences(causal):
+    """Central differences of L = sum(dO * O) through forward_varlen, over every
+    input element including padding (whose gradient must be exactly zero)."""
+    lens = [(3, 4), (2, 5), (0, 3)]
+    B, H, Nq, Nk, d = len(lens), 1, 3, 5, 2
+    q, k, v = RNG.standard_normal((B, H, Nq, d)), RNG.standard_normal((B, H, Nk, d)), RNG.standard_normal((B, H, Nk, d))
+    do = RNG.standard_normal((B, H, Nq, d))
+    lq = [a for a, _ in lens]; lk = [b for _, b in lens]
+    grads = naive.backward_varlen(q, k, v, do, lq, lk, 0.8, causal)
+    h = 1e-6
+
+    def L(qq, kk, vv):
+        o, _ = naive.forward_varlen(qq, kk, vv, lq, lk, 0.8, causal)
+        return float((o * do).sum())
+
+    for which, g in enumerate(grads):
+        args = [q, k, v]
+        num = np.zeros_like(args[which])
+        for idx in np.ndindex(*num.shape):
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            num[idx] = (L(*plus) - L(*minus)) / (2 * h)
+        assert np.abs(num - g).max() / max(np.abs(num).max(), 1e-3) <= 1e-6, (which, causal)
+        for b, (nq, nk) in enumerate(lens):
+            pad = g[b, :, (nq if which == 0 else nk):]
+            assert np.all(pad == 0)
+
+
 # ---------------------------------------------------------------- mutation check
 def _mutant_forward(kind):
     def fwd(q, k, v, scale, causal=False, return_p=False):
