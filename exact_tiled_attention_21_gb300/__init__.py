@@ -195,6 +195,28 @@ def fa_bwd_window(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, windo
            "fa_bwd_window")
 
 
+def fa_fwd_varlen(q, k, v, o, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream=None):
+    fn = load().fa_fwd_varlen
+    if fn.argtypes is None:
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        fn.argtypes = [vp] * 7 + [i] * 5 + [ctypes.c_float, i, vp]
+        fn.restype = i
+    _raise(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(seqlens_q), _ptr(seqlens_k), B, H, Nq, Nk, d,
+              float(scale), int(causal), _stream(stream)), "fa_fwd_varlen")
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal,
+                  workspace, workspace_bytes, stream=None):
+    fn = load().fa_bwd_varlen
+    if fn.argtypes is None:
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        fn.argtypes = [vp] * 11 + [i] * 5 + [ctypes.c_float, i, vp, ctypes.c_size_t, vp]
+        fn.restype = i
+    _raise(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+              _ptr(seqlens_q), _ptr(seqlens_k), B, H, Nq, Nk, d, float(scale), int(causal), _ptr(workspace),
+              workspace_bytes, _stream(stream)), "fa_bwd_varlen")
+
+
 def fa_selftest_wait_timeout(timeout_ns, stream=None):
     """Launch the watchdog self-test kernel (a wait that must run out)."""
     fn = load().fa_selftest_wait_timeout
@@ -268,8 +290,16 @@ def _check(t, name, shape):
         raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
 
 
-def forward(q, k, v, scale=None, causal=False, stream=None):
-    """O, LSE for q [B,H,Nq,d], k/v [B,H,Nk,d] (bf16 CUDA).  LSE is fp32 [B,H,Nq]."""
+def _lens(t, B, name):
+    if not (t.is_cuda and t.dtype == torch.int32 and t.is_contiguous() and t.shape == (B,)):
+        raise ValueError("%s must be a contiguous int32 CUDA tensor of shape (%d,)" % (name, B))
+
+
+def forward(q, k, v, scale=None, causal=False, stream=None, seqlens_q=None, seqlens_k=None):
+    """O, LSE for q [B,H,Nq,d], k/v [B,H,Nk,d] (bf16 CUDA).  LSE is fp32 [B,H,Nq].
+
+    With seqlens_q / seqlens_k (int32 [B] on the device, both or neither):
+    per-sequence lengths within the padded tensors (fa_fwd_varlen)."""
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     _check(q, "q", (B, H, Nq, d))
@@ -278,11 +308,17 @@ def forward(q, k, v, scale=None, causal=False, stream=None):
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream)
+    if seqlens_q is not None or seqlens_k is not None:
+        _lens(seqlens_q, B, "seqlens_q")
+        _lens(seqlens_k, B, "seqlens_k")
+        fa_fwd_varlen(q, k, v, o, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream)
+    else:
+        fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream)
     return o, lse
 
 
-def backward(q, k, v, o, lse, dO, scale=None, causal=False, stream=None, workspace=None):
+def backward(q, k, v, o, lse, dO, scale=None, causal=False, stream=None, workspace=None, seqlens_q=None,
+             seqlens_k=None):
     """dQ, dK, dV (bf16) for the forward output o / lse and upstream gradient dO."""
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
@@ -294,8 +330,14 @@ def backward(q, k, v, o, lse, dO, scale=None, causal=False, stream=None, workspa
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace,
-           workspace.numel() * workspace.element_size(), stream)
+    if seqlens_q is not None or seqlens_k is not None:
+        _lens(seqlens_q, B, "seqlens_q")
+        _lens(seqlens_k, B, "seqlens_k")
+        fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal,
+                      workspace, workspace.numel() * workspace.element_size(), stream)
+    else:
+        fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace,
+               workspace.numel() * workspace.element_size(), stream)
     return dq, dk, dv
 
 

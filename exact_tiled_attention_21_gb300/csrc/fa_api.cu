@@ -173,8 +173,10 @@ const char* fa_status_string(int st) {
 }  // extern "C"
 
 namespace {
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-             int d, float scale, int causal, int window, void* stream) {
+             int d, float scale, int causal, int window, const int* lens_q, const int* lens_k, void* stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
@@ -182,6 +184,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (st != FA_OK) return st;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_ALIGNMENT;
+    if ((lens_q && !aligned4(lens_q)) || (lens_k && !aligned4(lens_k))) return FA_ERR_ALIGNMENT;
     FwdLaunch a;
     st = device_state(&a.err, &a.num_sms);
     if (st != FA_OK) return st;
@@ -199,6 +202,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     a.scale = scale;
     a.causal = causal;
     a.window = window;
+    a.lens_q = lens_q;
+    a.lens_k = lens_k;
     a.timeout_ns = g_timeout_ns.load();
     return launch_fwd(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -208,13 +213,19 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
            int Nk, int d, float scale, int causal, void* stream) {
-    return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 0, stream);
+    return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 0, nullptr, nullptr, stream);
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* seqlens_q,
+                  const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal, void* stream) {
+    if (!seqlens_q || !seqlens_k) return FA_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 0, seqlens_q, seqlens_k, stream);
 }
 
 int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                   int Nk, int d, float scale, int window, void* stream) {
     if (window < 1) return FA_ERR_INVALID_ARG;
-    return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, 1, window, stream);
+    return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, 1, window, nullptr, nullptr, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
@@ -261,6 +272,8 @@ int bwd_prepare(BwdLaunch* a, const void* q, const void* k, const void* v, const
     a->scale = scale;
     a->causal = causal;
     a->window = 0;
+    a->lens_q = nullptr;
+    a->lens_k = nullptr;
     a->timeout_ns = g_timeout_ns.load();
     return FA_OK;
 }
@@ -269,8 +282,10 @@ int launched(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
              void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
-             int window, void* workspace, size_t workspace_bytes, void* stream) {
+             int window, const int* lens_q, const int* lens_k, void* workspace, size_t workspace_bytes,
+             void* stream) {
     if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    if ((lens_q && !aligned4(lens_q)) || (lens_k && !aligned4(lens_k))) return FA_ERR_ALIGNMENT;
     int st = check_shape(B, H, Nq, Nk, d);
     if (st != FA_OK) return st;
     if (!workspace || workspace_bytes < bwd_ws_bytes(B, H, Nq, d)) return FA_ERR_WORKSPACE;
@@ -280,6 +295,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
                      scale, causal, true);
     if (st != FA_OK) return st;
     a.window = window;
+    a.lens_q = lens_q;
+    a.lens_k = lens_k;
     cudaStream_t s = (cudaStream_t)stream;
     if ((st = launched(launch_bwd_pre(a, s))) != FA_OK) return st;
     if ((st = launched(launch_bwd_dkdv(a, s))) != FA_OK) return st;
@@ -293,16 +310,24 @@ extern "C" {
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
            void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
            void* workspace, size_t workspace_bytes, void* stream) {
-    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, 0, workspace,
-                    workspace_bytes, stream);
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, 0, nullptr, nullptr,
+                    workspace, workspace_bytes, stream);
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq,
+                  int Nk, int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!seqlens_q || !seqlens_k) return FA_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, 0, seqlens_q, seqlens_k,
+                    workspace, workspace_bytes, stream);
 }
 
 int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                   void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int window,
                   void* workspace, size_t workspace_bytes, void* stream) {
     if (window < 1) return FA_ERR_INVALID_ARG;
-    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, 1, window, workspace,
-                    workspace_bytes, stream);
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, 1, window, nullptr, nullptr,
+                    workspace, workspace_bytes, stream);
 }
 
 int fa_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H, int Nq, int d, void* stream) {

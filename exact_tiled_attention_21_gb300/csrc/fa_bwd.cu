@@ -63,12 +63,26 @@ struct BwdParams {
     const float* delta;
     int BH, Nq, Nk, causal, n_qt, n_kt;
     int window;  // > 0: causal sliding window of this many keys
+    const int* lens_q;  // per-sequence query / key counts, or null (Nq / Nk)
+    const int* lens_k;
+    int H;
     float scale, scale_log2;
     DevError* err;
     uint64_t timeout_ns;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Query and key counts of head bh's sequence (per-sequence lengths clamped to
+// [0, Nq] and [0, Nk]; the forward records lengths out of range).  Rows and
+// keys past them are padding: their LSE reads as -inf (P = 0), key columns are
+// masked, and their gradients are stored as zeros.
+__device__ __forceinline__ void bwd_seqlen(const BwdParams& p, int bh, int& nq, int& nk) {
+    nq = p.Nq;
+    nk = p.Nk;
+    if (p.lens_q) nq = min(max(__ldg(p.lens_q + bh / p.H), 0), p.Nq);
+    if (p.lens_k) nk = min(max(__ldg(p.lens_k + bh / p.H), 0), p.Nk);
+}
 
 // ------------------------------------------------------------------ D = rowsum(dO o O)
 template <int D>
@@ -217,16 +231,18 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // head, key tile 0 (the most query tiles when causal) first
     const int bh = blockIdx.x / p.n_kt;
     const int kt = blockIdx.x - bh * p.n_kt;
-    const int off = p.Nk - p.Nq;
+    int nq, nk;
+    bwd_seqlen(p, bh, nq, nk);
+    const int off = nk - nq;
     int i0 = 0;
     if (p.causal) {
         const int first_q = kt * 128 - off;  // smallest query that sees key kt*128
         i0 = first_q <= 0 ? 0 : first_q / 128;
     }
-    int i_end = p.n_qt;
+    int i_end = kt * 128 < nk ? (nq + 127) / 128 : 0;  // no query tile past the sequence
     if (p.window > 0) {  // the last query that sees the tile's last key
         const long long qlast = (long long)kt * 128 + 127 - off + p.window - 1;
-        i_end = qlast < 0 ? 0 : (int)min((long long)p.n_qt, qlast / 128 + 1);
+        i_end = qlast < 0 ? 0 : (int)min((long long)i_end, qlast / 128 + 1);
     }
     const int n = i0 < i_end ? i_end - i0 : 0;
     const uint32_t sK = s_base + C::OFF_FIXED, sV = sK + C::TILE;
@@ -259,7 +275,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     const int q = i * 128 + lane + 32 * t;
                     nl2[t] = INFINITY;
                     ndl[t] = 0.f;
-                    if (q < p.Nq) {
+                    if (q < nq) {
                         const float L = p.lse[(size_t)bh * p.Nq + q];
                         nl2[t] = (L == -INFINITY) ? INFINITY : L * kLog2e;
                         ndl[t] = p.delta[(size_t)bh * p.Nq + q];
@@ -345,7 +361,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const int h = warp >> 2;
         const int r = ((warp & 3) << 5) + lane;  // key row within the tile = TMEM lane
         const int kg = kt * 128 + r;
-        const bool row_ok = kg < p.Nk;
+        const bool row_ok = kg < p.Nk;   // stored (zeros past the sequence)
+        const bool key_ok = kg < nk;     // a key of the sequence
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t colA = C::COL_A + 64 * h, colB = C::COL_B + 64 * h;
         const float sc = p.scale_log2;
@@ -369,7 +386,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mbar_arrive(B_SF);
             // masked entries: rows past Nk (whole row) and, causal, columns c < cmin.
             // Tiles with none in the warp take the instantiation without the test.
-            const int cmin_eff = row_ok ? cmin : (1 << 30);
+            const int cmin_eff = key_ok ? cmin : (1 << 30);
             // sliding window: queries c > cmax_w no longer see key kg
             const int cmax_w = p.window > 0 ? kg - off + p.window - 1 - i * 128 - 64 * h : (1 << 30);
             auto p_phase = [&](auto MASK) {
@@ -483,12 +500,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const int bh = blockIdx.x / p.n_qt;  // head-major (K / V of one head shared in L2)
     const int mr = blockIdx.x - bh * p.n_qt;
     const int it = p.causal ? p.n_qt - 1 - mr : mr;  // causal: late query tiles (most keys) first
-    const int off = p.Nk - p.Nq;
-    int n = p.n_kt;
-    if (p.causal) {
-        const int qmax = min(it * 128 + 127, p.Nq - 1);
+    int nq, nk;
+    bwd_seqlen(p, bh, nq, nk);
+    const int off = nk - nq;
+    int n = it * 128 < nq ? (nk + 127) / 128 : 0;  // a tile wholly past the sequence only stores zeros
+    if (p.causal && n > 0) {
+        const int qmax = min(it * 128 + 127, nq - 1);
         const long long lim = (long long)qmax + off;
-        n = lim < 0 ? 0 : min(p.n_kt, (int)(lim / 128) + 1);
+        n = lim < 0 ? 0 : min(n, (int)(lim / 128) + 1);
     }
     int jlo = 0;  // sliding window: first key tile the tile's first query sees
     if (p.window > 0) {
@@ -568,13 +587,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t colA = C::COL_A + 64 * h, colB = C::COL_B + 64 * h;
         float l2 = INFINITY, dl = 0.f;
-        if (row_ok) {
+        if (qg < nq) {  // a row past the sequence keeps P = 0
             const float L = p.lse[(size_t)bh * p.Nq + qg];
             l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
             dl = p.delta[(size_t)bh * p.Nq + qg];
         }
         const float sc = p.scale_log2;
-        const int lim_row = p.causal ? min(qg + off, p.Nk - 1) : p.Nk - 1;  // last key this row sees
+        const int lim_row = p.causal ? min(qg + off, nk - 1) : nk - 1;  // last key this row sees
         // Q_i and dO_i into TMEM as the A operands of the score products: row = lane,
         // bf16 pairs in column order; warpgroup h writes d-columns [h D/2, (h+1) D/2)
         if (n > 0) {
@@ -687,6 +706,9 @@ BwdParams make_params(const BwdLaunch& a) {
     p.Nk = a.Nk;
     p.causal = a.causal;
     p.window = a.window;
+    p.lens_q = a.lens_q;
+    p.lens_k = a.lens_k;
+    p.H = a.H;
     p.n_qt = (a.Nq + 127) / 128;
     p.n_kt = (a.Nk + 127) / 128;
     p.scale = a.scale;

@@ -58,17 +58,38 @@ struct FwdParams {
     float* lse;
     int BH, Nq, Nk, causal;
     int window;  // > 0: causal sliding window of this many keys
+    const int* lens_q;  // per-sequence query / key counts (varlen instantiation only; may be null)
+    const int* lens_k;
+    int H;
     int n_mtiles, num_work;
     float scale_log2;
     DevError* err;
     uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ int fwd_num_kv(const FwdParams& p, int row0) {
-    const int kv_total = (p.Nk + 127) / 128;
+// Query and key counts of a work tile's sequence: Nq and Nk, or with
+// per-sequence lengths (VL) those of its batch entry, clamped to [0, Nq] and
+// [0, Nk] (bad: a length was out of range).
+struct SeqLen {
+    int nq, nk;
+    bool bad;
+};
+template <bool VL>
+__device__ __forceinline__ SeqLen fwd_seqlen(const FwdParams& p, int w) {
+    if (!VL || w >= p.num_work) return {p.Nq, p.Nk, false};
+    const int b = (w % p.BH) / p.H;
+    const int lq = p.lens_q ? __ldg(p.lens_q + b) : p.Nq;
+    const int lk = p.lens_k ? __ldg(p.lens_k + b) : p.Nk;
+    const int nq = min(max(lq, 0), p.Nq), nk = min(max(lk, 0), p.Nk);
+    return {nq, nk, nq != lq || nk != lk};
+}
+
+__device__ __forceinline__ int fwd_num_kv(const FwdParams& p, int row0, int nq, int nk) {
+    if (row0 >= nq) return 0;
+    const int kv_total = (nk + 127) / 128;
     if (!p.causal) return kv_total;
-    const int max_row = min(row0 + kFwdRowsPerCta - 1, p.Nq - 1);
-    const long long lim = (long long)max_row + p.Nk - p.Nq;  // last key the last row sees
+    const int max_row = min(row0 + kFwdRowsPerCta - 1, nq - 1);
+    const long long lim = (long long)max_row + nk - nq;  // last key the last row sees
     if (lim < 0) return 0;
     return min(kv_total, (int)(lim / 128) + 1);
 }
@@ -76,9 +97,9 @@ __device__ __forceinline__ int fwd_num_kv(const FwdParams& p, int row0) {
 // First key block a work tile needs: with a sliding window, the block of the
 // first visible key of its first row.
 template <bool WIN>
-__device__ __forceinline__ int fwd_kv_first(const FwdParams& p, int row0) {
+__device__ __forceinline__ int fwd_kv_first(const FwdParams& p, int row0, int nq, int nk) {
     if (!WIN || p.window <= 0) return 0;
-    const long long lo = (long long)row0 + p.Nk - p.Nq - p.window + 1;
+    const long long lo = (long long)row0 + nk - nq - p.window + 1;
     return lo <= 0 ? 0 : (int)(lo / 128);
 }
 
@@ -154,9 +175,10 @@ __device__ __forceinline__ float exp_pass(uint32_t taddr, int lim2, int lo2, flo
     return rs.x + rs.y;
 }
 
-// WIN: the sliding-window variant (a separate instantiation, so the plain
-// path carries none of its bounds).
-template <int D, bool WIN>
+// WIN: the sliding-window variant; VL: per-sequence lengths (rows past a
+// sequence's length give O = 0, LSE = -inf; keys past it are masked).  Each is
+// a separate instantiation, so the plain path carries none of their bounds.
+template <int D, bool WIN, bool VL>
 __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
@@ -216,11 +238,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             uint32_t phase = 0, q_iter = 0;
             uint32_t issued = 0, issued_par = 0;  // per slot: filled at least once / its last parity
             bool ok = true;
+            SeqLen sl_next = fwd_seqlen<VL>(p, blockIdx.x);
             for (int w = blockIdx.x; w < p.num_work && ok; w += gridDim.x) {
+                const SeqLen sl = sl_next;  // loaded one tile ahead
+                sl_next = fwd_seqlen<VL>(p, w + gridDim.x);
                 int bh, row0;
                 fwd_decode(p, w, bh, row0);
-                const int jlo = fwd_kv_first<WIN>(p, row0);
-                const int n = max(0, fwd_num_kv(p, row0) - jlo);
+                const int jlo = fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk);
+                const int n = max(0, fwd_num_kv(p, row0, sl.nq, sl.nk) - jlo);
                 if (n == 0) continue;
                 if (q_iter > 0 && !mbar_wait(BAR_QE, (q_iter - 1) & 1, ctl, kSiteQEmpty)) break;
                 mbar_arrive_expect_tx(BAR_QF, 2 * C::Q_BYTES);
@@ -284,10 +309,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 }
             };
             bool ok = true;
+            SeqLen sl_next = fwd_seqlen<VL>(p, blockIdx.x);
             for (int w = blockIdx.x; w < p.num_work && ok; w += gridDim.x) {
+                const SeqLen sl = sl_next;
+                sl_next = fwd_seqlen<VL>(p, w + gridDim.x);
                 int bh, row0;
                 fwd_decode(p, w, bh, row0);
-                const int n = max(0, fwd_num_kv(p, row0) - fwd_kv_first<WIN>(p, row0));
+                const int n = max(0, fwd_num_kv(p, row0, sl.nq, sl.nk) - fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk));
                 if (n == 0) continue;
                 if (!mbar_wait(BAR_QF, q_iter & 1, ctl, kSiteQFull)) break;
                 ++q_iter;
@@ -350,13 +378,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const uint32_t col_o = t ? C::COL_O1 : C::COL_O0;
         const uint32_t bar_s = BAR_S + 8 * t, bar_p = BAR_P + 8 * t, bar_o = BAR_O + 8 * t;
         const float c = p.scale_log2;
-        const int off = p.Nk - p.Nq;
         uint32_t s_iter = 0, o_iter = 0;
+        SeqLen sl_next = fwd_seqlen<VL>(p, blockIdx.x);
         for (int w = blockIdx.x; w < p.num_work; w += gridDim.x) {
+            const SeqLen sl = sl_next;
+            sl_next = fwd_seqlen<VL>(p, w + gridDim.x);
+            if (VL && sl.bad && tid == 0 && atomicCAS(&p.err->code, 0, kErrInvalid) == 0) {
+                p.err->site = kSiteSeqLen;
+                p.err->block = blockIdx.x;
+                p.err->aux = w;
+            }
+            const int off = sl.nk - sl.nq;
             int bh, row0;
             fwd_decode(p, w, bh, row0);
-            const int jlo = fwd_kv_first<WIN>(p, row0);
-            const int n = max(0, fwd_num_kv(p, row0) - jlo);
+            const int jlo = fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk);
+            const int n = max(0, fwd_num_kv(p, row0, sl.nq, sl.nk) - jlo);
             const int tile_row0 = row0 + t * 128;
             const int row = tile_row0 + r;
             float m_use = -INFINITY, l = 0.f;
@@ -367,9 +403,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 tc_fence_after();
                 // pass 1: row maximum of the raw scores (scale > 0 commutes with max)
                 const int kbase = (jlo + j) * 128;
-                const bool masked = kbase + 128 > p.Nk || (p.causal && kbase + 127 > tile_row0 + off) ||
-                                    (WIN && kbase < tile_row0 + 127 + off - p.window + 1);
-                const int lim = p.causal ? min(row + off, p.Nk - 1) : p.Nk - 1;
+                const bool masked = kbase + 128 > sl.nk || (p.causal && kbase + 127 > tile_row0 + off) ||
+                                    (WIN && kbase < tile_row0 + 127 + off - p.window + 1) ||
+                                    (VL && tile_row0 + 127 >= sl.nq);
+                // last visible key of this row; none for a row past its sequence
+                const int lim = (VL && row >= sl.nq) ? -1 : (p.causal ? min(row + off, sl.nk - 1) : sl.nk - 1);
                 const int lim2 = lim - kbase;  // last visible column of this block
                 // first visible column (sliding window), far below 0 without one
                 const int lo2 = WIN ? row + off - p.window + 1 - kbase : -(1 << 30);
@@ -447,11 +485,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     }
 }
 
-template <int D, bool WIN>
+template <int D, bool WIN, bool VL>
 cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
     using C = Fwd<D>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, WIN, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess) return e;
     FwdParams p;
@@ -462,19 +500,23 @@ cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
     p.Nk = a.Nk;
     p.causal = a.causal;
     p.window = a.window;
+    p.lens_q = a.lens_q;
+    p.lens_k = a.lens_k;
+    p.H = a.H;
     p.n_mtiles = (a.Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
     p.num_work = p.n_mtiles * p.BH;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
     p.timeout_ns = a.timeout_ns;
     const int grid = p.num_work < a.num_sms ? p.num_work : a.num_sms;
-    fwd_kernel<D, WIN><<<grid, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, p);
+    fwd_kernel<D, WIN, VL><<<grid, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
-    return a.window > 0 ? launch_fwd_dw<D, true>(a, s) : launch_fwd_dw<D, false>(a, s);
+    if (a.lens_q || a.lens_k) return launch_fwd_dw<D, false, true>(a, s);
+    return a.window > 0 ? launch_fwd_dw<D, true, false>(a, s) : launch_fwd_dw<D, false, false>(a, s);
 }
 
 }  // namespace

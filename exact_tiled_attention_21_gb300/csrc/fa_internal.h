@@ -18,6 +18,8 @@ struct FwdLaunch {
     float scale;
     int causal;
     int window;  // > 0: causal sliding window (keys per query)
+    const int* lens_q;  // device int32 [B] per-sequence query / key counts, or null (Nq / Nk)
+    const int* lens_k;
     int num_sms;
     DevError* err;
     uint64_t timeout_ns;
@@ -38,6 +40,8 @@ struct BwdLaunch {
     float scale;
     int causal;
     int window;  // > 0: causal sliding window (keys per query)
+    const int* lens_q;  // device int32 [B] per-sequence query / key counts, or null (Nq / Nk)
+    const int* lens_k;
     int num_sms;
     DevError* err;
     uint64_t timeout_ns;

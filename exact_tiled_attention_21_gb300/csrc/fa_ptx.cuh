@@ -25,7 +25,7 @@ enum : int {
     kSiteQFull = 1, kSiteQEmpty, kSiteKvFull, kSiteKvEmpty, kSiteSFull, kSitePFull, kSiteOFinal,
     kSiteTeardown, kSiteBwdQFull, kSiteBwdQEmpty, kSiteBwdKvFull, kSiteBwdS, kSiteBwdP, kSiteBwdDP,
     kSiteBwdDS, kSiteBwdDQ, kSiteBwdDone, kSiteAlign, kSiteProbe, kSitePagedTable,
-    kSitePagedQ, kSitePagedKv, kSitePagedS, kSitePagedP, kSitePagedPv, kSitePagedO
+    kSitePagedQ, kSitePagedKv, kSitePagedS, kSitePagedP, kSitePagedPv, kSitePagedO, kSiteSeqLen
 };
 
 constexpr int kErrTimeout = -6;

@@ -72,6 +72,23 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
 int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse,
                   int B, int H, int Nq, int Nk, int d, float scale, int window, void *stream);
 
+/* Forward over a padded batch of sequences of different lengths (a mask
+ * variant of fa_fwd: zimaspace.com "Wie reduziert Flash Attention ...",
+ * masking is applied to the tile scores before the softmax).  seqlens_q and
+ * seqlens_k are device int32 [B]: sequence b has seqlens_q[b] <= Nq query
+ * rows and seqlens_k[b] <= Nk keys, stored in the first rows of its
+ * [H, Nq, d] / [H, Nk, d] slices.  Row i < seqlens_q[b] attends to keys
+ * j < seqlens_k[b] (causal: also j <= i + seqlens_k[b] - seqlens_q[b]).  Rows
+ * past seqlens_q[b] get O = 0 and LSE = -inf.  Query and key tiles wholly past a
+ * sequence are skipped.  Padding positions of q, k and v must hold finite
+ * values (their contents do not change the result).  A length outside
+ * [0, Nq] / [0, Nk] is clamped and recorded as FA_ERR_INVALID_ARG in the
+ * device error word.  Other conventions as fa_fwd; both length pointers are
+ * required (FA_ERR_INVALID_ARG if null) and 4-byte aligned. */
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                  const int *seqlens_q, const int *seqlens_k,
+                  int B, int H, int Nq, int Nk, int d, float scale, int causal, void *stream);
+
 /* Bytes of fp32 workspace fa_bwd needs: the row terms D [B,H,Nq] (dQ is
  * accumulated on chip, in a pass of its own).  Returns 0 for invalid sizes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
@@ -96,6 +113,16 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
 int fa_bwd_window(const void *q, const void *k, const void *v, const void *o, const float *lse,
                   const void *dO, void *dq, void *dk, void *dv,
                   int B, int H, int Nq, int Nk, int d, float scale, int window,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward of fa_fwd_varlen (same lengths, same conventions as fa_bwd).
+ * Gradient rows past a sequence's length (dq past seqlens_q[b], dk and dv
+ * past seqlens_k[b]) are written as zeros.  dO must be finite in padding rows
+ * too; lse is fa_fwd_varlen's (-inf in padding rows). */
+int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                  const void *dO, void *dq, void *dk, void *dv,
+                  const int *seqlens_q, const int *seqlens_k,
+                  int B, int H, int Nq, int Nk, int d, float scale, int causal,
                   void *workspace, size_t workspace_bytes, void *stream);
 
 /* The three steps of fa_bwd, for callers that schedule them (or time them)
