@@ -77,6 +77,39 @@ CONFIGS = {
 }
 
 
+def head_f32(seed, tag, b, h, n, d, std=1.0):
+    """One head's [n, d] float32 block (CPU), unrounded: the source of FP8 inputs."""
+    g = torch.Generator("cpu").manual_seed(head_seed(seed, tag, b, h))
+    x = torch.randn((n, d), generator=g, dtype=torch.float32)
+    return x * std if std != 1.0 else x
+
+
+def to_e4m3(x, rows=None):
+    """Quantise float32 [B, H, N, d] to e4m3 bytes with fp32 scales.
+
+    rows=None: one scale per head, shape [B*H]; otherwise one scale per
+    ``rows``-row block of each head, shape [B*H, ceil(N/rows)].  A scale is the
+    block's largest magnitude / 448 (1 for an all-zero block), and the stored
+    byte is torch's round-to-nearest e4m3 of x / scale.  Returns
+    (uint8 [B, H, N, d], float32 scales).  Input preparation only: the value an
+    element stands for is e4m3(byte) * scale."""
+    B, H, N, d = x.shape
+    xs = x.reshape(B * H, N, d)
+    if rows is None:
+        amax = xs.abs().amax(dim=(1, 2))
+        sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        q = xs / sc[:, None, None]
+    else:
+        nb = -(-N // rows)
+        pad = torch.zeros(B * H, nb * rows, d)
+        pad[:, :N] = xs
+        amax = pad.reshape(B * H, nb, rows, d).abs().amax(dim=(2, 3))
+        sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        q = (pad.reshape(B * H, nb, rows, d) / sc[:, :, None, None]).reshape(B * H, nb * rows, d)[:, :N]
+    q = q.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return q.reshape(B, H, N, d).contiguous(), sc.float().contiguous()
+
+
 def default_scale(d):
     """The scale the workloads use: 1/sqrt(d)."""
     return 1.0 / math.sqrt(d)

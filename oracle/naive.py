@@ -143,6 +143,56 @@ def backward_varlen(q, k, v, do, lens_q, lens_k, scale, causal=False):
     return dq, dk, dv
 
 
+def e4m3_value(byte):
+    """The number an OCP e4m3 byte stands for (1 sign bit, 4 exponent bits with
+    bias 7, 3 mantissa bits; exponent 0 is subnormal, 2^-6 * m/8; the pattern
+    S.1111.111 is NaN; there are no infinities)."""
+    b = int(byte)
+    sign = -1.0 if b & 0x80 else 1.0
+    e, m = (b >> 3) & 0xF, b & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+_E4M3 = np.array([e4m3_value(b) for b in range(256)])
+
+
+def dequant_e4m3(x8, scales, rows=None):
+    """fp64 values of e4m3 bytes [B,H,N,d] with one scale per head ([B*H]) or
+    per ``rows``-row block of each head ([B*H, ceil(N/rows)])."""
+    x8 = np.asarray(x8, dtype=np.uint8)
+    B, H, N, d = x8.shape
+    val = _E4M3[x8].reshape(B * H, N, d)
+    sc = np.asarray(scales, dtype=np.float64)
+    if rows is None:
+        val = val * sc.reshape(B * H, 1, 1)
+    else:
+        val = val * np.repeat(sc.reshape(B * H, -1), rows, axis=1)[:, :N, None]
+    return val.reshape(B, H, N, d)
+
+
+def forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, scale, causal=False, rows=None, Nq=None):
+    """The FP8 block-scaled forward ([JOHE] "Flash Attention 3": block-scaled
+    attention; "Flash Attention 4": FP8) as the exact attention of the values
+    the inputs stand for: q and k with one scale per 128-row block, v with one
+    per head.  ``rows`` / ``Nq`` as in ``forward`` (q8 then holds those rows,
+    and q_scale stays the full per-block array of the Nq rows)."""
+    if rows is None:
+        q = dequant_e4m3(q8, q_scale, rows=128)
+    else:
+        rows_a = np.asarray(rows)
+        q8 = np.asarray(q8, dtype=np.uint8)
+        B, H = q8.shape[:2]
+        qsc = np.asarray(q_scale, dtype=np.float64).reshape(B * H, -1)[:, rows_a // 128]
+        q = (_E4M3[q8].reshape(B * H, len(rows_a), -1) * qsc[:, :, None]).reshape(q8.shape)
+    k = dequant_e4m3(k8, k_scale, rows=128)
+    v = dequant_e4m3(v8, v_scale)
+    return forward(q, k, v, scale, causal, rows=rows, Nq=Nq)
+
+
 def decode(q, kcache, vcache, scale):
     """One query per (b, h) against its cache.  q [B,H,d], caches [B,H,Nk,d].
 

@@ -501,6 +501,69 @@ def test_varlen_backward_finite_differences(causal):
             assert np.all(pad == 0)
 
 
+# ---------------------------------------------------------------- FP8 block-scaled forward
+def test_e4m3_decoder_matches_library():
+    """The oracle's decoder, written from the format (bias 7, 3 mantissa bits,
+    subnormals, one NaN pattern per sign), equals torch's float8_e4m3fn for
+    all 256 bytes."""
+    lib = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = np.array([naive.e4m3_value(b) for b in range(256)])
+    assert np.array_equal(np.isnan(lib), np.isnan(mine))
+    assert np.array_equal(lib[~np.isnan(lib)], mine[~np.isnan(mine)])
+    assert naive.e4m3_value(0x7E) == 448.0 and naive.e4m3_value(0x01) == 2.0 ** -9
+
+
+def test_fp8_block_scales_and_folding():
+    """Each 128-row block of q and k takes its own scale and v one per head:
+    built element by element here; a factor moved from the q scales into the
+    softmax scale changes nothing; sampled rows equal the full result."""
+    from exact_tiled_attention_21_gb300 import synthetic as syn
+    B, H, Nq, Nk, d = 1, 2, 200, 300, 8
+    g = torch.Generator("cpu").manual_seed(5)
+    q8, sq = syn.to_e4m3(torch.randn(B, H, Nq, d, generator=g) * 3, rows=128)
+    k8, sk = syn.to_e4m3(torch.randn(B, H, Nk, d, generator=g), rows=128)
+    v8, sv = syn.to_e4m3(torch.randn(B, H, Nk, d, generator=g))
+    assert sq.shape == (B * H, 2) and sk.shape == (B * H, 3) and sv.shape == (B * H,)
+    q = np.zeros((B, H, Nq, d)); k = np.zeros((B, H, Nk, d)); v = np.zeros((B, H, Nk, d))
+    q8n, k8n, v8n = q8.numpy(), k8.numpy(), v8.numpy()
+    for h in range(H):
+        for i in range(Nq):
+            q[0, h, i] = [naive.e4m3_value(x) * float(sq[h, i // 128]) for x in q8n[0, h, i]]
+        for j in range(Nk):
+            k[0, h, j] = [naive.e4m3_value(x) * float(sk[h, j // 128]) for x in k8n[0, h, j]]
+            v[0, h, j] = [naive.e4m3_value(x) * float(sv[h]) for x in v8n[0, h, j]]
+    for causal in (False, True):
+        o8, l8 = naive.forward_fp8(q8n, k8n, v8n, sq.numpy(), sk.numpy(), sv.numpy(), 0.3, causal)
+        o, l = naive.forward(q, k, v, 0.3, causal)
+        np.testing.assert_allclose(o8, o, atol=1e-12)
+        np.testing.assert_allclose(l8, l, atol=1e-12)
+        o2, l2 = naive.forward_fp8(q8n, k8n, v8n, 2 * sq.numpy(), sk.numpy(), sv.numpy(), 0.15, causal)
+        np.testing.assert_allclose(o2, o, atol=1e-12)
+        np.testing.assert_allclose(l2, l, atol=1e-12)
+        rows = [0, 127, 128, 199]
+        o3, l3 = naive.forward_fp8(q8n[:, :, rows], k8n, v8n, sq.numpy(), sk.numpy(), sv.numpy(), 0.3, causal,
+                                   rows=rows, Nq=Nq)
+        np.testing.assert_allclose(o3, o[:, :, rows], atol=1e-12)
+        np.testing.assert_allclose(l3, l[:, :, rows], atol=1e-12)
+
+
+def test_e4m3_quantiser_error():
+    """The input generator's quantiser: each value is within half an e4m3 step
+    of x / scale (relative 2^-4, or 2^-10 absolute in the subnormal range)."""
+    from exact_tiled_attention_21_gb300 import synthetic as syn
+    x = torch.randn(1, 3, 300, 16, generator=torch.Generator("cpu").manual_seed(9)) * 5
+    for rows in (None, 128):
+        x8, sc = syn.to_e4m3(x, rows=rows)
+        deq = naive.dequant_e4m3(x8.numpy(), sc.numpy(), rows=rows)
+        xs = x.double().numpy()
+        if rows is None:
+            s_el = np.repeat(sc.double().numpy(), 300 * 16).reshape(1, 3, 300, 16)
+        else:
+            s_el = np.repeat(sc.double().numpy(), 128, axis=1)[:, :300].reshape(1, 3, 300, 1) * np.ones((1, 1, 1, 16))
+        err = np.abs(deq - xs) / s_el
+        assert np.all(err <= np.maximum(2.0 ** -4 * np.abs(xs) / s_el, 2.0 ** -10) + 1e-9)
+
+
 # ---------------------------------------------------------------- mutation check
 def _mutant_forward(kind):
     def fwd(q, k, v, scale, causal=False, return_p=False):
