@@ -217,6 +217,49 @@ def fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, seqlens_q, seqlens_k, B, H, N
               workspace_bytes, _stream(stream)), "fa_bwd_varlen")
 
 
+def fa_fwd_fp8_workspace_bytes(B, H, Nk, d):
+    fn = load().fa_fwd_fp8_workspace_bytes
+    if fn.argtypes is None:
+        fn.argtypes = [ctypes.c_int] * 4
+        fn.restype = ctypes.c_size_t
+    return fn(B, H, Nk, d)
+
+
+def fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, Nq, Nk, d, scale, causal, workspace,
+               workspace_bytes, stream=None):
+    fn = load().fa_fwd_fp8
+    if fn.argtypes is None:
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        fn.argtypes = [vp] * 8 + [i] * 5 + [ctypes.c_float, i, vp, ctypes.c_size_t, vp]
+        fn.restype = i
+    _raise(fn(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _ptr(o), _ptr(lse),
+              B, H, Nq, Nk, d, float(scale), int(causal), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "fa_fwd_fp8")
+
+
+def forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, scale=None, causal=False, stream=None, workspace=None):
+    """O (bf16) and LSE for e4m3 q8 [B,H,Nq,128], k8/v8 [B,H,Nk,128] (uint8 CUDA tensors) with fp32
+    scales: q_scale [B*H, ceil(Nq/128)], k_scale [B*H, ceil(Nk/128)], v_scale [B*H]."""
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    for t, n, shp in ((q8, "q8", (B, H, Nq, d)), (k8, "k8", (B, H, Nk, d)), (v8, "v8", (B, H, Nk, d))):
+        if not (t.is_cuda and t.dtype == torch.uint8 and t.is_contiguous() and tuple(t.shape) == shp):
+            raise ValueError("%s must be a contiguous uint8 CUDA tensor of shape %s" % (n, shp))
+    for t, n, shp in ((q_scale, "q_scale", (B * H, -(-Nq // 128))), (k_scale, "k_scale", (B * H, -(-Nk // 128))),
+                      (v_scale, "v_scale", (B * H,))):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and tuple(t.shape) == shp):
+            raise ValueError("%s must be a contiguous float32 CUDA tensor of shape %s" % (n, shp))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    nbytes = fa_fwd_fp8_workspace_bytes(B, H, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q8.device)
+    o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
+    fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, Nq, Nk, d, scale, causal, workspace,
+               workspace.numel() * workspace.element_size(), stream)
+    return o, lse
+
+
 def fa_selftest_wait_timeout(timeout_ns, stream=None):
     """Launch the watchdog self-test kernel (a wait that must run out)."""
     fn = load().fa_selftest_wait_timeout

@@ -78,12 +78,12 @@ int make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
 // Tiled map of any rank (bf16, 128-byte swizzle, zero fill out of range).
 // strides: bytes of dims 1..rank-1.
 int make_map_nd(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                const cuuint32_t* box) {
+                const cuuint32_t* box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     int st = encoder(&enc);
     if (st != FA_OK) return st;
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+    CUresult r = enc(m, dtype, rank, const_cast<void*>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
@@ -461,6 +461,57 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, con
             return FA_ERR_CUDA;
     }
     return launch_decode_paged(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int Nk, int d) {
+    if (B < 1 || H < 1 || Nk < 1 || d != 128 || (long long)B * H > (1ll << 24)) return 0;
+    const size_t nk_pad = ((size_t)Nk + 15) & ~(size_t)15;
+    return (((size_t)B * H * 128 * nk_pad) + 255) & ~(size_t)255;
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int B, int H, int Nq, int Nk, int d, float scale,
+               int causal, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !q_scale || !k_scale || !v_scale || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, Nq, Nk, d);
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !aligned4(q_scale) || !aligned4(k_scale) || !aligned4(v_scale))
+        return FA_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < fa_fwd_fp8_workspace_bytes(B, H, Nk, d)) return FA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
+    Fp8FwdLaunch a;
+    st = device_state(&a.err, &a.num_sms);
+    if (st != FA_OK) return st;
+    const cuuint64_t BH = (cuuint64_t)B * H;
+    const int nk_pad = (Nk + 15) & ~15;
+    const cuuint32_t box[3] = {128, 128, 1};
+    const cuuint64_t qd[3] = {128, (cuuint64_t)Nq, BH}, qs[2] = {128, (cuuint64_t)Nq * 128};
+    const cuuint64_t kd[3] = {128, (cuuint64_t)Nk, BH}, ks[2] = {128, (cuuint64_t)Nk * 128};
+    const cuuint64_t vd[3] = {(cuuint64_t)nk_pad, 128, BH}, vs[2] = {(cuuint64_t)nk_pad, (cuuint64_t)nk_pad * 128};
+    if (make_map_nd(&a.map_q, q, 3, qd, qs, box, CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+        make_map_nd(&a.map_k, k, 3, kd, ks, box, CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+        make_map_nd(&a.map_vt, workspace, 3, vd, vs, box, CU_TENSOR_MAP_DATA_TYPE_UINT8))
+        return FA_ERR_CUDA;
+    a.v = v;
+    a.vt = workspace;
+    a.o = o;
+    a.lse = lse;
+    a.q_scale = q_scale;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.B = B;
+    a.H = H;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.Nk_pad = nk_pad;
+    a.scale = scale;
+    a.causal = causal;
+    a.timeout_ns = g_timeout_ns.load();
+    return launch_fwd_fp8(a, (cudaStream_t)stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {

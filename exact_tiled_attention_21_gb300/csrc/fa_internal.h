@@ -81,6 +81,24 @@ struct PagedDecodeLaunch {
     uint64_t timeout_ns;
 };
 
+struct Fp8FwdLaunch {
+    CUtensorMap map_q, map_k;  // 3-D uint8 (128, N, B*H), box (128, 128, 1), 128B swizzle
+    CUtensorMap map_vt;        // 3-D uint8 (Nk_pad, 128, B*H) over vt, box (128, 128, 1), 128B swizzle
+    const void* v;             // e4m3 [B*H, Nk, 128]
+    void* vt;                  // workspace: e4m3 [B*H, 128, Nk_pad]
+    void* o;                   // bf16 [B*H, Nq, 128]
+    float* lse;
+    const float* q_scale;
+    const float* k_scale;
+    const float* v_scale;
+    int B, H, Nq, Nk, Nk_pad;
+    float scale;
+    int causal;
+    int num_sms;
+    DevError* err;
+    uint64_t timeout_ns;
+};
+
 // Each returns a cudaError_t of the launch (cudaSuccess when queued).
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s);   // D = rowsum(dO o O)
@@ -89,6 +107,7 @@ cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s);    // dQ
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_paged(const PagedDecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_paged_mma(const PagedDecodeLaunch& a, cudaStream_t s);
+cudaError_t launch_fwd_fp8(const Fp8FwdLaunch& a, cudaStream_t s);  // V^T copy, then the forward
 // LSE-weighted merge of per-split partials into o (bf16) and lse (fp32, may be null).
 cudaError_t launch_decode_combine(const float* part_o, const float* part_lse, void* o, float* lse, int BH,
                                   int splits, int d, cudaStream_t s);

@@ -89,6 +89,28 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
                   const int *seqlens_q, const int *seqlens_k,
                   int B, int H, int Nq, int Nk, int d, float scale, int causal, void *stream);
 
+/* Bytes of workspace fa_fwd_fp8 needs: a transposed copy of V,
+ * [B*H, 128, Nk rounded up to 16] bytes.  Returns 0 for invalid sizes. */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int Nk, int d);
+
+/* FP8 forward with block scales (johe.ru "Flash Attention: ...", sections
+ * "Flash Attention 3": block-scaled attention, and "Flash Attention 4": FP8).
+ * q [B,H,Nq,128], k and v [B,H,Nk,128] as e4m3 bytes (OCP FP8, no infinities).
+ * The value an element stands for is its e4m3 value times its scale:
+ *  q_scale fp32 [B*H, ceil(Nq/128)]: one per 128-row block of q;
+ *  k_scale fp32 [B*H, ceil(Nk/128)]: one per 128-row block of k;
+ *  v_scale fp32 [B*H]: one per head of v.
+ * Computes the forward of fa_fwd on those values: o [B,H,Nq,128] bf16 and lse
+ * [B,H,Nq] fp32.  Scores accumulate in fp32.  P = exp(S - m) is rounded to
+ * e4m3 (relative error <= 2^-4, or 2^-10 absolute below 2^-6) for the value
+ * product, and the result is multiplied by v_scale / l.  d must be 128
+ * (FA_ERR_UNSUPPORTED otherwise).  workspace: at least
+ * fa_fwd_fp8_workspace_bytes(B,H,Nk,d) bytes, 16-byte aligned; it receives V^T
+ * (one extra pass over V) so that both products take K-major operands. */
+int fa_fwd_fp8(const void *q, const void *k, const void *v, const float *q_scale, const float *k_scale,
+               const float *v_scale, void *o, float *lse, int B, int H, int Nq, int Nk, int d, float scale,
+               int causal, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Bytes of fp32 workspace fa_bwd needs: the row terms D [B,H,Nq] (dQ is
  * accumulated on chip, in a pass of its own).  Returns 0 for invalid sizes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);

@@ -66,6 +66,30 @@ def check_out_elementwise(o, lse, o_ref, lse_ref, vmax, what=""):
             assert le <= LSE_ABS, "%s: max |LSE-LSE_ref| = %g" % (what, le)
 
 
+def check_out_fp8(o, lse, o_ref, lse_ref, p_ref, v, what=""):
+    """FP8 forward against the exact attention of the dequantised inputs, per
+    element, with the bound from the arithmetic: P's e4m3 rounding (relative
+    2^-4 of each weight, or 2^-10 absolute below 2^-6 in units where the row's
+    reference maximum weighs at most 1, i.e. at most max_j P_ij of the
+    normalised weight), the bf16 rounding of O (2^-8 |O|), 1e-4 for fp32
+    accumulation.  Scores are exact products of e4m3 values accumulated in
+    fp32, so the LSE keeps the usual tolerance."""
+    o = np.asarray(o, dtype=np.float64)
+    assert np.isfinite(o).all(), "%s: non-finite output" % what
+    av = np.abs(v)
+    bound = (2.0 ** -4 * (p_ref @ av) + 2.0 ** -10 * p_ref.max(axis=-1, keepdims=True) * av.sum(axis=-2, keepdims=True)
+             + 2.0 ** -8 * np.abs(o_ref) + 1e-4)
+    err = np.abs(o - o_ref)
+    excess = (err - bound).max()
+    assert excess <= 0, "%s: |O-O_ref| exceeds the FP8 rounding bound by %g" % (what, excess)
+    fin = ~np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(np.asarray(lse)), ~fin), "%s: -inf LSE pattern differs" % what
+    if fin.any():
+        le = np.abs(np.asarray(lse, dtype=np.float64)[fin] - lse_ref[fin]).max()
+        assert le <= LSE_ABS, "%s: max |LSE-LSE_ref| = %g" % (what, le)
+    return float(err.max()), float(err.mean()), float(bound.mean())
+
+
 def check_grad(g, g_ref, what="", cancel_scale=None):
     """max |g - g_ref| <= GRAD_REL * max |g_ref|.
 
