@@ -376,6 +376,34 @@ def run_ours(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError("device error in the paged decode run: %s" % detail)
 
+    # ---- FP8 block-scaled forward (next-row feature; timed separately, not part of the step)
+    def e4m3_bytes(*shape):  # finite e4m3 bytes of either sign (no NaN pattern)
+        mag = torch.randint(0, 126, shape, generator=torch.Generator().manual_seed(7), dtype=torch.int32)
+        sign = torch.randint(0, 2, shape, generator=torch.Generator().manual_seed(8), dtype=torch.int32) << 7
+        return (mag | sign).to(torch.uint8).to(dev)
+    f8q, f8k, f8v = (e4m3_bytes(1, H, N, D) for _ in range(3))
+    f8sq = torch.full((H, N // 128), 1.0 / 64, device=dev)
+    f8sk = f8sq.clone()
+    f8sv = torch.full((H,), 1.0 / 64, device=dev)
+    f8o = torch.empty(1, H, N, D, dtype=torch.bfloat16, device=dev)
+    f8l = torch.empty(1, H, N, device=dev)
+    f8ws = torch.empty(fa.fa_fwd_fp8_workspace_bytes(1, H, N, D), dtype=torch.uint8, device=dev)
+    f8_call = lambda: fa.fa_fwd_fp8(f8q, f8k, f8v, f8sq, f8sk, f8sv, f8o, f8l, 1, H, N, N, D, SCALE, 1, f8ws,
+                                    f8ws.numel(), stream)
+    for _ in range(3):
+        f8_call()
+    barrier()
+    fe0, fe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fe0.record(stream)
+    for _ in range(20):
+        f8_call()
+    fe1.record(stream)
+    barrier()
+    f8_ms = fe0.elapsed_time(fe1) / 20
+    st, detail = fa.fa_get_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError("device error in the FP8 forward run: %s" % detail)
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -411,6 +439,11 @@ def run_ours(args, rank, world, local_rank):
         "decode_paged": {"value": pg_bytes / (pg_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": pg_ms,
                          "config": "B=32 Hq=32 Hkv=8 page=16 Nk=4096 d=128 16 splits (grouped-query, paged)",
                          "frac_of_hbm": pg_bytes / (pg_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "fwd_fp8": {"value": FWD_FLOPS / (f8_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms": f8_ms,
+                    "config": "B=1 H=32 N=8192 d=128 causal, e4m3 q/k (one scale per 128 rows) and v (one per "
+                              "head), including the V transpose into the workspace",
+                    "frac_of_peak": FWD_FLOPS / (f8_ms * 1e-3) / 1e12 / (2 * pk["bf16_sustained"]),
+                    "peak_source": "bf16 sustained x 2 (nominal dense fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s)"},
         "roofline": {
             "kernel": "bwd_dkdv_kernel<128>",
             "bound": "tensor",
