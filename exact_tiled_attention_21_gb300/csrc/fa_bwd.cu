@@ -11,16 +11,20 @@
 //   bwd_pre   D_i = rowsum(dO o O) in fp32 (one warp per row).
 //   bwd_dkdv  one CTA per 128-key tile (KV-tile parallel): K_j, V_j stay in
 //             shared memory, Q_i / dO_i stream through a 2-stage ring;
-//             tcgen05: S^T = K Q^T and dP^T = V dO^T into TMEM, dV += P^T dO
-//             and dK += dS^T Q with P^T / dS^T read from TMEM; dK, dV
-//             accumulate in TMEM over all query tiles.
-//   bwd_dq    one CTA per 128-query tile (Q-tile parallel): Q_i, dO_i stay,
-//             K_j / V_j stream; S = Q K^T, dP = dO V^T, dQ += dS K with dS
-//             from TMEM.  dQ is accumulated in fp32 TMEM and written once, so
-//             the backward needs no atomics and is deterministic.
+//             tcgen05: S^T = K Q^T and dP^T = V dO^T into TMEM; P^T goes to
+//             shared memory (so S^T of the next query tile can be issued as
+//             soon as S^T is read) for dV += P^T dO; dS^T is written over
+//             dP^T in TMEM for dK += dS^T Q; dK, dV accumulate in TMEM over
+//             all query tiles.
+//   bwd_dq    one CTA per 128-query tile (Q-tile parallel): Q_i, dO_i are
+//             written into TMEM by the compute threads and stay; K_j / V_j
+//             stream; S = Q K^T and dP = dO V^T take Q, dO from TMEM; dQ +=
+//             dS K with dS from TMEM.  dQ is accumulated in fp32 TMEM and
+//             written once, so the backward needs no atomics and is
+//             deterministic.
 // In both, one thread per TMEM lane (the 128 rows of the tile) computes P
-// and dS; P stays in registers (packed bf16) so the next score MMA can be
-// issued while dS is being formed.
+// and dS for the 64 columns of its warpgroup; P stays in registers (packed
+// bf16) so the next score MMA can be issued while dS is being formed.
 #include <type_traits>
 
 #include "fa_internal.h"

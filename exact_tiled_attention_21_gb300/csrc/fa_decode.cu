@@ -212,12 +212,15 @@ cudaError_t launch_decode_d(const DecodeLaunch& a, cudaStream_t s) {
 
 
 // ------------------------------------------------------------------ paged, grouped-query decode
-// One CTA per (b, kv head, split, group of G <= 4 query heads).  The split's keys
-// are the logical tokens [split * chunk, min(len, (split + 1) * chunk)) of the
-// sequence, chunk = ceil(len / splits), found through the block table one
-// key at a time; each K and V row is read once and used for all G query heads
-// of the group (they share the kv head).  Same online pieces, partials and
-// combine as the contiguous decode.  A page index outside [0, num_pages) or
+// The general path (d = 64, page sizes the tensor-core kernel of
+// fa_decode_mma.cu does not take, more than 2048 sequences).  One CTA per (b,
+// kv head, split, group of G <= 4 query heads).  The split's keys are the
+// logical tokens [split * chunk, min(len, (split + 1) * chunk)) of the
+// sequence, chunk = ceil(len / splits); each 128-key piece's page rows are
+// looked up once through the block table (thread = key) into shared memory;
+// each K and V row is read once and used for all G query heads of the group
+// (they share the kv head).  Same online pieces, partials and combine as the
+// contiguous decode.  A page index outside [0, num_pages) or
 // a length outside [1, max_pages * page] is recorded as FA_ERR_INVALID_ARG in
 // the error word and read as zeros, never dereferenced.
 template <int D, int G>
