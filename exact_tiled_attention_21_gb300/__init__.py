@@ -154,8 +154,9 @@ def fa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, B, Hq, H
               _ptr(workspace), int(workspace_bytes), _stream(stream)), "fa_decode_paged")
 
 
-def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale=None, num_splits=16, stream=None):
-    """O [B,Hq,d] bf16 and LSE [B,Hq] fp32 against a paged cache (int32 table and lengths on the device)."""
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale=None, num_splits=0, stream=None):
+    """O [B,Hq,d] bf16 and LSE [B,Hq] fp32 against a paged cache (int32 table and lengths on the device).
+    num_splits <= 0: the library's choice."""
     B, Hq, d = q.shape
     num_pages, Hkv, page_size = k_pages.shape[:3]
     max_pages = block_table.shape[1]

@@ -123,6 +123,31 @@ int decode_auto_splits(int Nk) {
     return s < 1 ? 1 : (s > 16 ? 16 : s);
 }
 
+// Paged decode, automatic splits.  The lengths live on the device, so the host
+// plans for the longest possible sequence (max_pages * page).  The tensor-core
+// kernel is persistent: items = B * Hkv * (head groups) * splits are dealt to
+// the SMs round-robin.  Its cost model is waves * (1/splits + 0.02): a split
+// is a share of the sequence plus a fixed per-item overhead.  It picks the
+// best of 1..16 splits with at least 128 keys each.  The general kernel uses
+// the contiguous decode's rule.
+int paged_auto_splits(int B, int Hq, int Hkv, int max_len, int num_sms, bool mma) {
+    if (!mma) return decode_auto_splits(max_len);
+    const int g = Hq / Hkv;
+    const int nh = g <= 4 ? 4 : (g <= 8 ? 8 : 16);
+    const long long base = (long long)B * Hkv * ((g + nh - 1) / nh);
+    int best = 1;
+    double best_cost = 1e30;
+    for (int sp = 1; sp <= 16 && (sp == 1 || (long long)sp * 128 <= max_len); ++sp) {
+        const long long waves = (base * sp + num_sms - 1) / num_sms;
+        const double cost = (double)waves * (1.0 / sp + 0.02);
+        if (cost < best_cost - 1e-12) {
+            best_cost = cost;
+            best = sp;
+        }
+    }
+    return best;
+}
+
 size_t decode_ws_bytes(int B, int H, int d, int splits) {
     const size_t parts = (size_t)B * H * splits;
     return parts * d * 4 + ((parts * 4 + 255) & ~(size_t)255);
@@ -400,8 +425,8 @@ int fa_decode(const void* q, const void* kcache, const void* vcache, void* o, fl
 }
 
 size_t fa_decode_paged_workspace_bytes(int B, int Hq, int d, int num_splits) {
-    if (B < 1 || Hq < 1 || (d != 64 && d != 128) || num_splits < 1 || num_splits > 256) return 0;
-    return decode_ws_bytes(B, Hq, d, num_splits);
+    if (B < 1 || Hq < 1 || (d != 64 && d != 128) || num_splits > 256) return 0;
+    return decode_ws_bytes(B, Hq, d, num_splits <= 0 ? 16 : num_splits);  // automatic: at most 16
 }
 
 int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
@@ -409,7 +434,7 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, con
                     int max_pages, int num_pages, int d, float scale, int num_splits, void* workspace,
                     size_t workspace_bytes, void* stream) {
     if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
-    if (!scale_ok(scale) || num_splits < 1 || num_splits > 256) return FA_ERR_INVALID_ARG;
+    if (!scale_ok(scale) || num_splits > 256) return FA_ERR_INVALID_ARG;
     if (B < 1 || Hq < 1 || Hkv < 1 || page_size < 1 || max_pages < 1 || num_pages < 1) return FA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
@@ -417,11 +442,14 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, con
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || (lse && !aligned16(lse)) ||
         (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return FA_ERR_ALIGNMENT;
+    PagedDecodeLaunch a;
+    int st = device_state(&a.err, &a.num_sms);
+    if (st != FA_OK) return st;
+    a.mma = paged_mma_ok(B, d, page_size);
+    if (num_splits <= 0)
+        num_splits = paged_auto_splits(B, Hq, Hkv, max_pages * page_size, a.num_sms, a.mma);
     if (!workspace || workspace_bytes < decode_ws_bytes(B, Hq, d, num_splits)) return FA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
-    PagedDecodeLaunch a;
-    int st = device_state(&a.err, nullptr);
-    if (st != FA_OK) return st;
     a.q = q;
     a.kp = k_pages;
     a.vp = v_pages;
@@ -440,9 +468,7 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, con
     a.d = d;
     a.splits = num_splits;
     a.scale = scale;
-    a.mma = paged_mma_ok(B, d, page_size);
     if (a.mma) {
-        if (device_state(nullptr, &a.num_sms) != FA_OK) return FA_ERR_CUDA;
         a.timeout_ns = g_timeout_ns.load();
         const cuuint64_t qd[3] = {(cuuint64_t)d, (cuuint64_t)B * Hq, 1};
         const cuuint64_t qs[2] = {(cuuint64_t)d * 2, (cuuint64_t)B * Hq * d * 2};

@@ -185,7 +185,9 @@ int fa_decode(const void *q, const void *kcache, const void *vcache, void *o, fl
               int B, int H, int Nk, int d, float scale, int num_splits,
               void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of fp32 workspace fa_decode_paged needs (partials of B*Hq heads). */
+/* Bytes of fp32 workspace fa_decode_paged needs (partials of B*Hq heads);
+ * num_splits <= 0 (automatic) returns the size for 16 splits, the most the
+ * automatic choice takes. */
 size_t fa_decode_paged_workspace_bytes(int B, int Hq, int d, int num_splits);
 
 /* Decode against a paged KV cache with grouped-query heads (the serving
@@ -199,6 +201,8 @@ size_t fa_decode_paged_workspace_bytes(int B, int Hq, int d, int num_splits);
  *  block_table [B, max_pages] int32: physical page of each logical page;
  *  seq_lens [B] int32, 1 <= seq_lens[b] <= max_pages * page_size;
  *  o [B, Hq, d] bf16; lse [B, Hq] fp32 or NULL.
+ * num_splits <= 0 lets the library choose (from B, the heads, the longest
+ * possible sequence max_pages * page_size and the SM count; at most 16).
  * Each sequence is cut into num_splits (1..256) contiguous chunks of
  * ceil(seq_lens[b] / num_splits) tokens (rounded up to whole 128-token stages
  * on the tensor-core path: d = 128, B <= 2048, page_size a multiple of 8 that

@@ -52,6 +52,8 @@ CASES = [
     (1, 40, 2, 32, [333], 128, 2),              # group of 20: 16 + 4 heads
     (1, 8, 2, 48, [500], 128, 3),               # 48-token pages (not a divisor of 128)
     (1, 8, 2, 16, [20000], 128, 1),             # one split: 157 stages through the ring
+    (32, 32, 8, 16, [4096] * 30 + [1, 777], 128, 0),  # automatic split count (tensor-core path)
+    (3, 8, 2, 48, [1000, 3, 480], 128, 0),      # automatic split count (general path)
 ]
 
 
