@@ -25,6 +25,7 @@
 // In both, one thread per TMEM lane (the 128 rows of the tile) computes P
 // and dS for the 64 columns of its warpgroup; P stays in registers (packed
 // bf16) so the next score MMA can be issued while dS is being formed.
+#include <algorithm>
 #include <type_traits>
 
 #include "fa_internal.h"
@@ -70,12 +71,27 @@ struct BwdParams {
     const int* lens_q;  // per-sequence query / key counts, or null (Nq / Nk)
     const int* lens_k;
     int H;
+    int hc_kv, hc_q;  // heads per scheduling chunk of the dK/dV and dQ grids
     float scale, scale_log2;
     DevError* err;
     uint64_t timeout_ns;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// CTA order of a grid of BH heads x n_t tiles, tile 0 the longest: heads come
+// in chunks of hc whose streamed operands fit in L2 together; within a chunk
+// every head's tile 0 first, then every head's tile 1, and so on, so the
+// hardware starts the longest CTAs first and the last wave is short ones.
+__device__ __forceinline__ void chunked_order(int idx, int n_t, int BH, int hc, int& bh, int& t) {
+    const int chunk_sz = hc * n_t;
+    const int c = idx / chunk_sz;
+    const int r = idx - c * chunk_sz;
+    const int h0 = c * hc;
+    const int hn = min(hc, BH - h0);
+    t = r / hn;
+    bh = h0 + (r - t * hn);
+}
 
 // Query and key counts of head bh's sequence (per-sequence lengths clamped to
 // [0, Nq] and [0, Nk]; the forward records lengths out of range).  Rows and
@@ -231,10 +247,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 13);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // head-major, so the CTAs in flight share one head's Q / dO in L2; within a
-    // head, key tile 0 (the most query tiles when causal) first
-    const int bh = blockIdx.x / p.n_kt;
-    const int kt = blockIdx.x - bh * p.n_kt;
+    int bh, kt;  // key tile 0 (the most query tiles when causal) first, heads in L2-sized chunks
+    chunked_order(blockIdx.x, p.n_kt, p.BH, p.hc_kv, bh, kt);
     int nq, nk;
     bwd_seqlen(p, bh, nq, nk);
     const int off = nk - nq;
@@ -501,8 +515,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 13);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x / p.n_qt;  // head-major (K / V of one head shared in L2)
-    const int mr = blockIdx.x - bh * p.n_qt;
+    int bh, mr;  // causal: late query tiles (most keys) first, heads in L2-sized chunks
+    chunked_order(blockIdx.x, p.n_qt, p.BH, p.hc_q, bh, mr);
     const int it = p.causal ? p.n_qt - 1 - mr : mr;  // causal: late query tiles (most keys) first
     int nq, nk;
     bwd_seqlen(p, bh, nq, nk);
@@ -713,6 +727,12 @@ BwdParams make_params(const BwdLaunch& a) {
     p.lens_q = a.lens_q;
     p.lens_k = a.lens_k;
     p.H = a.H;
+    // heads whose streamed tiles (Q and dO for the dK/dV pass, K and V for the dQ
+    // pass) fit in 64 MiB of L2 together
+    const long long budget = 64ll << 20;
+    const long long per_kv = 2ll * a.Nq * a.d * 2, per_q = 2ll * a.Nk * a.d * 2;
+    p.hc_kv = (int)std::max(1ll, std::min((long long)p.BH, budget / per_kv));
+    p.hc_q = (int)std::max(1ll, std::min((long long)p.BH, budget / per_q));
     p.n_qt = (a.Nq + 127) / 128;
     p.n_kt = (a.Nk + 127) / 128;
     p.scale = a.scale;
