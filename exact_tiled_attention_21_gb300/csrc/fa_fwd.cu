@@ -238,10 +238,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             uint32_t phase = 0, q_iter = 0;
             uint32_t issued = 0, issued_par = 0;  // per slot: filled at least once / its last parity
             bool ok = true;
-            SeqLen sl_next = fwd_seqlen<VL>(p, blockIdx.x);
-            for (int w = blockIdx.x; w < p.num_work && ok; w += gridDim.x) {
+            SeqLen sl_next = fwd_seqlen<VL>(p, persistent_work(0, blockIdx.x, gridDim.x));
+            for (int rd = 0; rd * (int)gridDim.x < p.num_work && ok; ++rd) {
+                const int w = persistent_work(rd, blockIdx.x, gridDim.x);
                 const SeqLen sl = sl_next;  // loaded one tile ahead
-                sl_next = fwd_seqlen<VL>(p, w + gridDim.x);
+                sl_next = fwd_seqlen<VL>(p, persistent_work(rd + 1, blockIdx.x, gridDim.x));
+                if (w >= p.num_work) continue;
                 int bh, row0;
                 fwd_decode(p, w, bh, row0);
                 const int jlo = fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk);
@@ -309,10 +311,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 }
             };
             bool ok = true;
-            SeqLen sl_next = fwd_seqlen<VL>(p, blockIdx.x);
-            for (int w = blockIdx.x; w < p.num_work && ok; w += gridDim.x) {
-                const SeqLen sl = sl_next;
-                sl_next = fwd_seqlen<VL>(p, w + gridDim.x);
+            SeqLen sl_next = fwd_seqlen<VL>(p, persistent_work(0, blockIdx.x, gridDim.x));
+            for (int rd = 0; rd * (int)gridDim.x < p.num_work && ok; ++rd) {
+                const int w = persistent_work(rd, blockIdx.x, gridDim.x);
+                const SeqLen sl = sl_next;  // loaded one tile ahead
+                sl_next = fwd_seqlen<VL>(p, persistent_work(rd + 1, blockIdx.x, gridDim.x));
+                if (w >= p.num_work) continue;
                 int bh, row0;
                 fwd_decode(p, w, bh, row0);
                 const int n = max(0, fwd_num_kv(p, row0, sl.nq, sl.nk) - fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk));
@@ -379,10 +383,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const uint32_t bar_s = BAR_S + 8 * t, bar_p = BAR_P + 8 * t, bar_o = BAR_O + 8 * t;
         const float c = p.scale_log2;
         uint32_t s_iter = 0, o_iter = 0;
-        SeqLen sl_next = fwd_seqlen<VL>(p, blockIdx.x);
-        for (int w = blockIdx.x; w < p.num_work; w += gridDim.x) {
+        SeqLen sl_next = fwd_seqlen<VL>(p, persistent_work(0, blockIdx.x, gridDim.x));
+        for (int rd = 0; rd * (int)gridDim.x < p.num_work; ++rd) {
+            const int w = persistent_work(rd, blockIdx.x, gridDim.x);
             const SeqLen sl = sl_next;
-            sl_next = fwd_seqlen<VL>(p, w + gridDim.x);
+            sl_next = fwd_seqlen<VL>(p, persistent_work(rd + 1, blockIdx.x, gridDim.x));
+            if (w >= p.num_work) continue;
             if (VL && sl.bad && tid == 0 && atomicCAS(&p.err->code, 0, kErrInvalid) == 0) {
                 p.err->site = kSiteSeqLen;
                 p.err->block = blockIdx.x;

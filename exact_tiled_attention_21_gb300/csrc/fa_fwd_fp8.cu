@@ -224,7 +224,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             int slot = 0;
             uint32_t phase = 0, q_iter = 0, issued = 0, issued_par = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < p.num_work && ok; w += gridDim.x) {
+            for (int rd = 0; rd * (int)gridDim.x < p.num_work && ok; ++rd) {
+                const int w = persistent_work(rd, blockIdx.x, gridDim.x);
+                if (w >= p.num_work) continue;
                 int bh, row0;
                 f8_decode(p, w, bh, row0);
                 const int n = f8_num_kv(p, row0);
@@ -287,7 +289,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                 }
             };
             bool ok = true;
-            for (int w = blockIdx.x; w < p.num_work && ok; w += gridDim.x) {
+            for (int rd = 0; rd * (int)gridDim.x < p.num_work && ok; ++rd) {
+                const int w = persistent_work(rd, blockIdx.x, gridDim.x);
+                if (w >= p.num_work) continue;
                 int bh, row0;
                 f8_decode(p, w, bh, row0);
                 const int n = f8_num_kv(p, row0);
@@ -357,7 +361,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         uint8_t* prow = smem + C::OFF_P + t * C::TILE + r * 128;
         const int off = p.Nk - p.Nq;
         uint32_t s_iter = 0, o_iter = 0;
-        for (int w = blockIdx.x; w < p.num_work; w += gridDim.x) {
+        for (int rd = 0; rd * (int)gridDim.x < p.num_work; ++rd) {
+            const int w = persistent_work(rd, blockIdx.x, gridDim.x);
+            if (w >= p.num_work) continue;
             int bh, row0;
             f8_decode(p, w, bh, row0);
             const int n = f8_num_kv(p, row0);

@@ -10,6 +10,14 @@
 
 namespace fa {
 
+// Work tile of persistent CTA `cta` (of G) in round `rd`: the rounds alternate
+// direction, so when the work list is ordered heaviest first every CTA's total
+// comes out nearly equal (CTA 0 takes the heaviest tile of one round and the
+// lightest of the next).
+__device__ __forceinline__ int persistent_work(int rd, int cta, int G) {
+    return rd * G + ((rd & 1) ? G - 1 - cta : cta);
+}
+
 struct FwdLaunch {
     CUtensorMap map_q, map_k, map_v;  // 3-D maps (d, N, B*H), box (64, 128, 1), 128B swizzle
     void* o;
