@@ -105,26 +105,45 @@ __device__ __forceinline__ void bwd_seqlen(const BwdParams& p, int bh, int& nq, 
 }
 
 // ------------------------------------------------------------------ D = rowsum(dO o O)
+// HBM-bound: D/8 lanes per row, 16-byte loads, each warp with 4 row groups'
+// loads in flight before it reduces.
+template <int D>
+constexpr int kPreRowsPerBlock = 8 * (32 / (D / 8)) * 4;
+
 template <int D>
 __global__ void __launch_bounds__(256)
 bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
                float* __restrict__ delta, long long rows) {
-    constexpr int PER = D / 32;
-    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const __nv_bfloat16* a = o + row * D + lane * PER;
-    const __nv_bfloat16* b = dO + row * D + lane * PER;
-    float s = 0.f;
+    constexpr int LPR = D / 8, RPW = 32 / LPR, STEPS = 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row0 = (long long)blockIdx.x * kPreRowsPerBlock<D> + (long long)warp * RPW * STEPS + lane / LPR;
+    const int part = lane % LPR;
+    uint4 x[STEPS], y[STEPS];
 #pragma unroll
-    for (int i = 0; i < PER; i += 2) {
-        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(a + i));
-        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(b + i));
-        s = fmaf(x.x, y.x, s);
-        s = fmaf(x.y, y.y, s);
+    for (int st = 0; st < STEPS; ++st) {
+        const long long row = row0 + st * RPW;
+        x[st] = y[st] = make_uint4(0u, 0u, 0u, 0u);
+        if (row < rows) {
+            x[st] = __ldg(reinterpret_cast<const uint4*>(o + row * D) + part);
+            y[st] = __ldg(reinterpret_cast<const uint4*>(dO + row * D) + part);
+        }
     }
-    for (int w = 16; w >= 1; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
-    if (lane == 0) delta[row] = s;
+#pragma unroll
+    for (int st = 0; st < STEPS; ++st) {
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&x[st]);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&y[st]);
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 u = __bfloat1622float2(a2[i]), v = __bfloat1622float2(b2[i]);
+            sum = fmaf(u.x, v.x, sum);
+            sum = fmaf(u.y, v.y, sum);
+        }
+#pragma unroll
+        for (int w = LPR / 2; w >= 1; w >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
+        const long long row = row0 + st * RPW;
+        if (part == 0 && row < rows) delta[row] = sum;
+    }
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -745,7 +764,7 @@ BwdParams make_params(const BwdLaunch& a) {
 template <int D>
 cudaError_t launch_pre_d(const BwdLaunch& a, cudaStream_t s) {
     const long long rows = (long long)a.B * a.H * a.Nq;
-    bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+    bwd_pre_kernel<D><<<(unsigned)((rows + kPreRowsPerBlock<D> - 1) / kPreRowsPerBlock<D>), 256, 0, s>>>(
         (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, a.delta, rows);
     return cudaGetLastError();
 }
