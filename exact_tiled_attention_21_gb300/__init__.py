@@ -87,6 +87,8 @@ def load():
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
     lib.fa_version.restype = i
+    lib.fa_fwd_tile_rows.argtypes = [i] * 6
+    lib.fa_fwd_tile_rows.restype = i
     _lib = lib
     return lib
 
@@ -281,6 +283,15 @@ def fa_decode_workspace_bytes(B, H, Nk, d, num_splits=0):
 def fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream=None):
     _raise(load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
                          float(scale), int(bool(causal)), _stream(stream)), "fa_fwd")
+
+
+def fa_fwd_tile_rows(B, H, Nq, Nk, d, causal):
+    """Query rows per work tile fa_fwd takes for these sizes (256, or 128 for
+    split-KV tiles)."""
+    rows = load().fa_fwd_tile_rows(B, H, Nq, Nk, d, int(bool(causal)))
+    if rows < 0:
+        raise FAError(rows, "fa_fwd_tile_rows")
+    return rows
 
 
 def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace,

@@ -241,6 +241,22 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 0, nullptr, nullptr, stream);
 }
 
+int fa_fwd_tile_rows(int B, int H, int Nq, int Nk, int d, int causal) {
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, Nq, Nk, d);
+    if (st != FA_OK) return st;
+    FwdLaunch a;
+    st = device_state(&a.err, &a.num_sms);
+    if (st != FA_OK) return st;
+    a.B = B;
+    a.H = H;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.causal = causal;
+    return fwd_use_split(a) ? 128 : kFwdRowsPerCta;
+}
+
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* seqlens_q,
                   const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal, void* stream) {
     if (!seqlens_q || !seqlens_k) return FA_ERR_INVALID_ARG;

@@ -42,8 +42,9 @@ struct Fwd {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_KV = 2 * Q_BYTES;
     static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_BYTES;
-    // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2], o_final[2], teardown
-    static constexpr int NBAR = 2 + 2 * NSLOT + 7;
+    // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2], o_final[2], teardown,
+    // merge_ready, merge_done (split-KV)
+    static constexpr int NBAR = 2 + 2 * NSLOT + 9;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr int THREADS = 320;
@@ -61,6 +62,7 @@ struct FwdParams {
     const int* lens_q;  // per-sequence query / key counts (varlen instantiation only; may be null)
     const int* lens_k;
     int H;
+    int rows;  // query rows per work tile: 256 (two 128-row tiles) or 128 (split-KV)
     int n_mtiles, num_work;
     float scale_log2;
     DevError* err;
@@ -88,7 +90,7 @@ __device__ __forceinline__ int fwd_num_kv(const FwdParams& p, int row0, int nq, 
     if (row0 >= nq) return 0;
     const int kv_total = (nk + 127) / 128;
     if (!p.causal) return kv_total;
-    const int max_row = min(row0 + kFwdRowsPerCta - 1, nq - 1);
+    const int max_row = min(row0 + p.rows - 1, nq - 1);
     const long long lim = (long long)max_row + nk - nq;  // last key the last row sees
     if (lim < 0) return 0;
     return min(kv_total, (int)(lim / 128) + 1);
@@ -108,7 +110,7 @@ __device__ __forceinline__ void fwd_decode(const FwdParams& p, int w, int& bh, i
     const int mr = w / p.BH;
     bh = w - mr * p.BH;
     const int m = p.causal ? (p.n_mtiles - 1 - mr) : mr;
-    row0 = m * kFwdRowsPerCta;
+    row0 = m * p.rows;
 }
 
 // Pass 1 over one 128-column S row in TMEM (thread = row): the maximum of the
@@ -176,9 +178,14 @@ __device__ __forceinline__ float exp_pass(uint32_t taddr, int lim2, int lo2, flo
 }
 
 // WIN: the sliding-window variant; VL: per-sequence lengths (rows past a
-// sequence's length give O = 0, LSE = -inf; keys past it are masked).  Each is
-// a separate instantiation, so the plain path carries none of their bounds.
-template <int D, bool WIN, bool VL>
+// sequence's length give O = 0, LSE = -inf; keys past it are masked).  SPLIT:
+// for grids with few work tiles, a work tile is one 128-row query tile whose
+// key blocks alternate between the two softmax warpgroups (even blocks to 0,
+// odd to 1), each with its own running max, sum and O in TMEM; warpgroup 0
+// merges the two at the end (the LSE-weighted combine of the online
+// recurrence).  Each is a separate instantiation, so the plain path carries
+// none of their bounds.
+template <int D, bool WIN, bool VL, bool SPLIT>
 __global__ void __launch_bounds__(Fwd<D>::THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
@@ -194,6 +201,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const uint32_t BAR_P = BAR_S + 16;                 // p_full[t]
     const uint32_t BAR_O = BAR_P + 16;                 // o_final[t]
     const uint32_t BAR_TD = BAR_O + 16;                // teardown
+    const uint32_t BAR_MR = BAR_TD + 8;                // split-KV: warpgroup 1's (m, l) staged
+    const uint32_t BAR_MD = BAR_MR + 8;                // split-KV: warpgroup 0 done with O_1 and (m, l)
     uint32_t* tmem_slot = (uint32_t*)(smem + C::OFF_MISC);
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
@@ -214,6 +223,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             mbar_init(BAR_O + 8 * t, 1);
         }
         mbar_init(BAR_TD, 1);
+        mbar_init(BAR_MR, 128);
+        mbar_init(BAR_MD, 128);
         fence_mbar_init();
         if ((s_base & 1023u) != 0) record_error(ctl, kErrTimeout, kSiteAlign, (int)(s_base & 1023u));
     }
@@ -250,8 +261,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 const int n = max(0, fwd_num_kv(p, row0, sl.nq, sl.nk) - jlo);
                 if (n == 0) continue;
                 if (q_iter > 0 && !mbar_wait(BAR_QE, (q_iter - 1) & 1, ctl, kSiteQEmpty)) break;
-                mbar_arrive_expect_tx(BAR_QF, 2 * C::Q_BYTES);
-                for (int t = 0; t < 2; ++t)
+                mbar_arrive_expect_tx(BAR_QF, (SPLIT ? 1 : 2) * C::Q_BYTES);
+                for (int t = 0; t < (SPLIT ? 1 : 2); ++t)
                     for (int c = 0; c < C::KCH; ++c)
                         tma_load_3d(s_base + C::OFF_Q + t * C::Q_BYTES + c * C::CHUNK_BYTES, &map_q,
                                     BAR_QF, c * 64, row0 + t * 128, bh, pol_q);
@@ -311,6 +322,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 }
             };
             bool ok = true;
+            uint32_t fill = 0, pit0 = 0, pit1 = 0;  // split-KV: ring fills consumed, P handoffs per warpgroup
             SeqLen sl_next = fwd_seqlen<VL>(p, persistent_work(0, blockIdx.x, gridDim.x));
             for (int rd = 0; rd * (int)gridDim.x < p.num_work && ok; ++rd) {
                 const int w = persistent_work(rd, blockIdx.x, gridDim.x);
@@ -323,6 +335,50 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 if (n == 0) continue;
                 if (!mbar_wait(BAR_QF, q_iter & 1, ctl, kSiteQFull)) break;
                 ++q_iter;
+                if constexpr (SPLIT) {
+                    // Ring fill f holds K_{f/2} (f even) or V_{f/2} (f odd) of this tile; block j goes
+                    // to warpgroup j & 1, so K_{j+2} is taken before V_{j+1} (at most 3 fills ahead
+                    // of the oldest one not yet released, below NSLOT).
+                    const uint32_t F = fill;
+                    auto fslot = [&](uint32_t f) { return (int)(f % C::NSLOT); };
+                    auto fwait = [&](uint32_t f) {
+                        return mbar_wait(bar_kvf(fslot(f)), (f / C::NSLOT) & 1, ctl, kSiteKvFull);
+                    };
+                    auto faddr = [&](uint32_t f) { return s_base + C::OFF_KV + fslot(f) * C::KV_BYTES; };
+                    for (int t = 0; t < 2 && t < n; ++t) {
+                        const uint32_t f = F + 2 * t;
+                        if (!fwait(f)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_s(t ? C::COL_S1 : C::COL_S0, sQ0, faddr(f));
+                        mma_commit(BAR_S + 8 * t);
+                        mma_commit(bar_kve(fslot(f)));
+                    }
+                    for (int j = 0; j < n && ok; ++j) {
+                        const int t = j & 1;
+                        uint32_t& pit = t ? pit1 : pit0;
+                        if (!mbar_wait(BAR_P + 8 * t, pit & 1, ctl, kSitePFull)) { ok = false; break; }
+                        ++pit;
+                        const uint32_t fv = F + 2 * j + 1;
+                        if (!fwait(fv)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_o(t ? C::COL_O1 : C::COL_O0, t ? C::COL_S1 : C::COL_S0, faddr(fv), j >= 2);
+                        mma_commit(bar_kve(fslot(fv)));
+                        if (j + 2 < n) {
+                            const uint32_t fk = F + 2 * j + 4;
+                            if (!fwait(fk)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_s(t ? C::COL_S1 : C::COL_S0, sQ0, faddr(fk));
+                            mma_commit(BAR_S + 8 * t);
+                            mma_commit(bar_kve(fslot(fk)));
+                        } else {
+                            mma_commit(BAR_O + 8 * t);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(BAR_QE);
+                    fill = F + 2 * n;
+                    continue;
+                }
                 int kslot = slot;
                 if (!mbar_wait(bar_kvf(kslot), phase, ctl, kSiteKvFull)) break;
                 tc_fence_after();
@@ -383,6 +439,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const uint32_t bar_s = BAR_S + 8 * t, bar_p = BAR_P + 8 * t, bar_o = BAR_O + 8 * t;
         const float c = p.scale_log2;
         uint32_t s_iter = 0, o_iter = 0;
+        uint32_t o1_iter = 0, merge_iter = 0;  // split-KV: warpgroup 1's O handoffs, merges
+        bool md_pending = false;               // split-KV (warpgroup 1): merge of the last tile not yet confirmed
+        float2* stage = (float2*)(smem + C::OFF_Q + C::Q_BYTES);  // split-KV: warpgroup 1's (m, l) per row
         SeqLen sl_next = fwd_seqlen<VL>(p, persistent_work(0, blockIdx.x, gridDim.x));
         for (int rd = 0; rd * (int)gridDim.x < p.num_work; ++rd) {
             const int w = persistent_work(rd, blockIdx.x, gridDim.x);
@@ -399,11 +458,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             fwd_decode(p, w, bh, row0);
             const int jlo = fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk);
             const int n = max(0, fwd_num_kv(p, row0, sl.nq, sl.nk) - jlo);
-            const int tile_row0 = row0 + t * 128;
+            const int tile_row0 = row0 + (SPLIT ? 0 : t * 128);
             const int row = tile_row0 + r;
+            const int j0 = SPLIT ? t : 0, jstep = SPLIT ? 2 : 1;
             float m_use = -INFINITY, l = 0.f;
             bool ok = true;
-            for (int j = 0; j < n; ++j) {
+            for (int j = j0; j < n; j += jstep) {
                 if (!mbar_wait(bar_s, s_iter & 1, ctl, kSiteSFull)) { ok = false; break; }
                 ++s_iter;
                 tc_fence_after();
@@ -421,7 +481,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 const float mraw = masked ? row_max_pass<true>(lane_addr + col_s, lim2, lo2)
                                           : row_max_pass<false>(lane_addr + col_s, lim2, lo2);
                 const float m_new = fmaxf(m_use, mraw * c);
-                if (j == 0) {
+                if (j == j0) {
                     m_use = m_new;
                 } else if (__any_sync(0xffffffffu, m_new > m_use + 8.f)) {
                     // rescale the accumulator so that O and l keep a common reference max
@@ -443,17 +503,51 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                                           : exp_pass<false>(lane_addr + col_s, lim2, lo2, c, msub);
                 l += rsum;
                 tc_fence_before();
+                if (SPLIT && md_pending) {  // O_1 is free only once the last tile's merge has read it
+                    if (!mbar_wait(BAR_MD, (merge_iter - 1) & 1, ctl, kSiteOFinal)) { ok = false; break; }
+                    md_pending = false;
+                }
                 mbar_arrive(bar_p);
             }
             if (!ok) break;
             // ---------------- epilogue: O / l -> bf16, LSE
-            if (n > 0) {
+            const int n_t = SPLIT ? (n - t + 1) / 2 : n;  // key blocks this warpgroup took
+            if (n_t > 0) {
                 if (!mbar_wait(bar_o, o_iter & 1, ctl, kSiteOFinal)) break;
                 ++o_iter;
                 tc_fence_after();
             }
+            // split-KV: the other warpgroup's (m, l), and the weights of both halves
+            float a0 = 1.f, a1 = 0.f;
+            if constexpr (SPLIT) {
+                if (t == 1) {  // hand (m, l) to warpgroup 0, which merges and stores
+                    if (md_pending && !mbar_wait(BAR_MD, (merge_iter - 1) & 1, ctl, kSiteOFinal)) break;
+                    stage[r] = make_float2(m_use, l);
+                    tc_fence_before();
+                    mbar_arrive(BAR_MR);
+                    ++merge_iter;
+                    md_pending = true;
+                    continue;
+                }
+                if (!mbar_wait(BAR_MR, merge_iter & 1, ctl, kSiteOFinal)) break;
+                ++merge_iter;
+                const float2 ml1 = stage[r];
+                if (n > 1) {  // warpgroup 1 took at least one block
+                    if (!mbar_wait(BAR_O + 8, o1_iter & 1, ctl, kSiteOFinal)) break;
+                    ++o1_iter;
+                }
+                tc_fence_after();
+                if (ml1.y > 0.f) {
+                    const float m = fmaxf(m_use, ml1.x);
+                    a0 = (l > 0.f) ? ex2(m_use - m) : 0.f;
+                    a1 = ex2(ml1.x - m);
+                    l = a0 * l + a1 * ml1.y;
+                    m_use = m;
+                }
+            }
             const bool valid = row < p.Nq;
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
+            const float w0 = a0 * inv, w1 = a1 * inv;
             __nv_bfloat16* orow = p.o + ((size_t)bh * p.Nq + (valid ? row : 0)) * D;
 #pragma unroll 1
             for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -465,9 +559,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     for (int i = 0; i < 32; ++i) v[i] = 0u;
                 }
                 uint32_t pk[16];
+                // tcgen05.ld is warp-collective: the O_1 read depends on the tile (n), never on the
+                // row; rows whose half 1 saw no key have a1 = 0 and O_1 = 0 there.
+                if (SPLIT && n > 1) {
+                    uint32_t u[32];
+                    tmem_ld32(lane_addr + C::COL_O1 + q4 * 32, u);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * w0 + __uint_as_float(u[2 * i]) * w1,
+                                          __uint_as_float(v[2 * i + 1]) * w0 + __uint_as_float(u[2 * i + 1]) * w1);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * w0, __uint_as_float(v[2 * i + 1]) * w0);
+                }
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
 #pragma unroll
@@ -479,6 +584,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 p.lse[(size_t)bh * p.Nq + row] =
                     (l > 0.f) ? (m_use + lg2(l)) * 0.69314718055994531f : -INFINITY;
             tc_fence_before();
+            if (SPLIT) mbar_arrive(BAR_MD);  // O_1 and the staged (m, l) may be overwritten
         }
     }
 
@@ -491,12 +597,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     }
 }
 
-template <int D, bool WIN, bool VL>
+template <int D, bool WIN, bool VL, bool SPLIT>
 cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
     using C = Fwd<D>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, WIN, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
+    static_assert(!SPLIT || (!WIN && !VL), "split-KV tiles are built for the plain forward only");
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, WIN, VL, SPLIT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     FwdParams p;
     p.o = (__nv_bfloat16*)a.o;
@@ -509,23 +616,62 @@ cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
     p.lens_q = a.lens_q;
     p.lens_k = a.lens_k;
     p.H = a.H;
-    p.n_mtiles = (a.Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
+    p.rows = SPLIT ? 128 : kFwdRowsPerCta;
+    p.n_mtiles = (a.Nq + p.rows - 1) / p.rows;
     p.num_work = p.n_mtiles * p.BH;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
     p.timeout_ns = a.timeout_ns;
     const int grid = p.num_work < a.num_sms ? p.num_work : a.num_sms;
-    fwd_kernel<D, WIN, VL><<<grid, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, p);
+    fwd_kernel<D, WIN, VL, SPLIT><<<grid, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, p);
     return cudaGetLastError();
+}
+
+// Tile mode for the plain forward.  The grid is persistent with a static
+// schedule (round rd of CTA c takes work tile persistent_work(rd, c, G)), so
+// the host can add up every CTA's share for both tile sizes and take the one
+// whose busiest CTA finishes first.  Costs, in units of one 128-key block of
+// a 256-row tile, fitted to GB300 timings: a key block of a split-KV tile
+// costs 0.55 (half the rows, but the two softmax warpgroups alternate on one
+// tile's blocks, at ~85% of the two-tile rate), and a tile costs 1.5 (256
+// rows) or 2 (split-KV: the merge) for its prologue and epilogue.  Only small
+// grids are evaluated; past four tiles per SM the 256-row tiles always win.
+int fwd_makespan(int BH, int Nq, int Nk, int causal, int rows, int block_cost, int tile_cost, int num_sms) {
+    const int n_m = (Nq + rows - 1) / rows;
+    const int work = n_m * BH, G = work < num_sms ? work : num_sms;
+    const int kv_total = (Nk + 127) / 128;
+    long long tot[1024] = {};
+    for (int w = 0; w < work; ++w) {
+        const int rd = w / G, pos = w - rd * G, cta = (rd & 1) ? G - 1 - pos : pos;
+        const int mr = w / BH, m = causal ? n_m - 1 - mr : mr;
+        int n = kv_total;
+        if (causal) {
+            const long long lim = (long long)(m * rows + rows - 1 < Nq - 1 ? m * rows + rows - 1 : Nq - 1) + Nk - Nq;
+            n = lim < 0 ? 0 : (int)(lim / 128 + 1 < kv_total ? lim / 128 + 1 : kv_total);
+        }
+        tot[cta] += (long long)n * block_cost + tile_cost;
+    }
+    long long mx = 0;
+    for (int c = 0; c < G; ++c) mx = tot[c] > mx ? tot[c] : mx;
+    return (int)(mx < (1LL << 30) ? mx : (1LL << 30));
 }
 
 template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
-    if (a.lens_q || a.lens_k) return launch_fwd_dw<D, false, true>(a, s);
-    return a.window > 0 ? launch_fwd_dw<D, true, false>(a, s) : launch_fwd_dw<D, false, false>(a, s);
+    if (a.lens_q || a.lens_k) return launch_fwd_dw<D, false, true, false>(a, s);
+    if (a.window > 0) return launch_fwd_dw<D, true, false, false>(a, s);
+    return fwd_use_split(a) ? launch_fwd_dw<D, false, false, true>(a, s) : launch_fwd_dw<D, false, false, false>(a, s);
 }
 
 }  // namespace
+
+bool fwd_use_split(const FwdLaunch& a) {
+    const long long work256 = (long long)((a.Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta) * a.B * a.H;
+    if (work256 > 4LL * a.num_sms || a.num_sms > 1024 || a.num_sms <= 0) return false;
+    const int BH = a.B * a.H;
+    return fwd_makespan(BH, a.Nq, a.Nk, a.causal, 128, 55, 200, a.num_sms) <
+           fwd_makespan(BH, a.Nq, a.Nk, a.causal, kFwdRowsPerCta, 100, 150, a.num_sms);
+}
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s) {
     return a.d == 128 ? launch_fwd_d<128>(a, s) : launch_fwd_d<64>(a, s);

@@ -109,6 +109,9 @@ struct Fp8FwdLaunch {
 
 // Each returns a cudaError_t of the launch (cudaSuccess when queued).
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
+// Whether the plain forward (no window, no per-sequence lengths) takes
+// 128-row split-KV tiles for a.B, a.H, a.Nq, a.Nk, a.causal on a.num_sms SMs.
+bool fwd_use_split(const FwdLaunch& a);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s);   // D = rowsum(dO o O)
 cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s);  // dK, dV
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s);    // dQ

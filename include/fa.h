@@ -64,6 +64,17 @@ typedef enum {
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int Nq, int Nk, int d, float scale, int causal, void *stream);
 
+/* Query rows per work tile fa_fwd takes for these sizes on the current device:
+ * 256 (two 128-row query tiles share every key/value block) or 128 (split-KV
+ * tiles: the key blocks of one 128-row tile alternate between two softmax
+ * groups, merged at the end with the log-sum-exp weights, the combine of
+ * wiki.ai-engineering.at "Flash Attention", section "Lösung: Online
+ * Softmax").  The choice minimises the busiest SM's share of a static
+ * persistent schedule; it only changes the rounding order.  Returns a negative
+ * fa_status for invalid sizes or no usable device.  Host-only; launches
+ * nothing. */
+int fa_fwd_tile_rows(int B, int H, int Nq, int Nk, int d, int causal);
+
 /* Causal sliding-window forward: like fa_fwd with causal = 1, except that
  * query i sees only the `window` (>= 1) keys ending at its diagonal, keys j
  * with i + Nk - Nq - window < j <= i + Nk - Nq (the fixed-window local

@@ -52,6 +52,14 @@ CASES = [
 ]
 
 
+def test_forward_cases_cover_split_tiles(cuda_lib):
+    """Most small cases above run through split-KV tiles (odd and even key
+    block counts, ragged tails, rows that see no key); single-tile ones through
+    256-row tiles."""
+    rows = [cuda_lib.fa_fwd_tile_rows(B, H, Nq, Nk, d, c) for B, H, Nq, Nk, d, c in CASES]
+    assert rows.count(128) >= 10 and rows.count(256) >= 2, rows
+
+
 @pytest.mark.parametrize("B,H,Nq,Nk,d,causal", CASES)
 def test_forward_parity(cuda_lib, B, H, Nq, Nk, d, causal):
     seed = 100 + Nq * 7 + Nk + d + causal
@@ -60,6 +68,43 @@ def test_forward_parity(cuda_lib, B, H, Nq, Nk, d, causal):
     o, lse = _run(cuda_lib, q, k, v, scale, causal)
     o_ref, lse_ref = naive.forward(f64(q), f64(k), f64(v), scale, causal)
     check_out(f64(o), f64(lse), o_ref, lse_ref, "B%d H%d Nq%d Nk%d d%d c%d" % (B, H, Nq, Nk, d, causal))
+
+
+# Enough heads for the 256-row tiles (two query tiles per CTA); most cases
+# above take split-KV tiles.
+WIDE_CASES = [
+    (2, 80, 513, 600, 64, True),
+    (4, 40, 700, 200, 64, True),     # rows that see no key
+    (4, 80, 300, 777, 128, False),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", WIDE_CASES)
+def test_forward_parity_256_row_tiles(cuda_lib, B, H, Nq, Nk, d, causal):
+    assert cuda_lib.fa_fwd_tile_rows(B, H, Nq, Nk, d, causal) == 256
+    seed = 300 + Nq * 7 + Nk + d + causal
+    q, k, v = _inputs(seed, B, H, Nq, Nk, d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(cuda_lib, q, k, v, scale, causal)
+    o_ref, lse_ref = naive.forward(f64(q), f64(k), f64(v), scale, causal)
+    check_out(f64(o), f64(lse), o_ref, lse_ref, "B%d H%d Nq%d Nk%d d%d c%d" % (B, H, Nq, Nk, d, causal))
+
+
+def test_forward_tile_modes_agree(cuda_lib):
+    """The same heads through split-KV tiles (a batch of 2 heads) and through
+    256-row tiles (those heads inside a batch of 320): the two orders of the
+    online recurrence agree within the bf16 output's rounding."""
+    B, H, N, d = 1, 320, 768, 64
+    for causal in (False, True):
+        assert cuda_lib.fa_fwd_tile_rows(B, H, N, N, d, causal) == 256
+        assert cuda_lib.fa_fwd_tile_rows(1, 2, N, N, d, causal) == 128
+    q, k, v = _inputs(41, B, H, N, N, d)
+    for causal in (False, True):
+        o_wide, l_wide = _run(cuda_lib, q, k, v, 0.125, causal)
+        o_split, l_split = _run(cuda_lib, q[:, :2].contiguous(), k[:, :2].contiguous(), v[:, :2].contiguous(),
+                                0.125, causal)
+        assert (o_wide[:, :2].float() - o_split.float()).abs().max() <= 2 ** -7
+        assert (l_wide[:, :2] - l_split).abs().max() <= 1e-4
 
 
 def test_forward_scale_argument(cuda_lib):

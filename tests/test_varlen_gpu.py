@@ -76,9 +76,11 @@ def test_varlen_forward_backward_parity(cuda_lib, H, Nq, Nk, d, causal, lq, lk):
 
 def test_varlen_full_lengths_match_dense(cuda_lib):
     """Lengths equal to the padded sizes give bit-identical results to fa_fwd /
-    fa_bwd (the same tiles, in the same order)."""
+    fa_bwd (the same tiles, in the same order).  Enough heads that fa_fwd takes
+    256-row tiles, as the per-sequence-length forward always does."""
     fa = cuda_lib
-    B, H, N, d = 2, 2, 640, 128
+    B, H, N, d = 2, 80, 640, 128
+    assert fa.fa_fwd_tile_rows(B, H, N, N, d, 0) == 256 and fa.fa_fwd_tile_rows(B, H, N, N, d, 1) == 256
     q, k, v, dO = (syn.bhnd(77, t, B, H, N, d).cuda() for t in (syn.TAG_Q, syn.TAG_K, syn.TAG_V, syn.TAG_DO))
     lens = torch.full((B,), N, dtype=torch.int32, device=q.device)
     for causal in (False, True):
