@@ -11,11 +11,12 @@
 //   bwd_pre   D_i = rowsum(dO o O) in fp32 (one warp per row).
 //   bwd_dkdv  one CTA per 128-key tile (KV-tile parallel): K_j, V_j stay in
 //             shared memory, Q_i / dO_i stream through a 2-stage ring;
-//             tcgen05: S^T = K Q^T and dP^T = V dO^T into TMEM; P^T goes to
-//             shared memory (so S^T of the next query tile can be issued as
-//             soon as S^T is read) for dV += P^T dO; dS^T is written over
-//             dP^T in TMEM for dK += dS^T Q; dK, dV accumulate in TMEM over
-//             all query tiles.
+//             tcgen05: S^T = K Q^T and dP^T = V dO^T into TMEM; S^T is read
+//             out at once (so S^T of the next query tile can be issued while
+//             P waits in registers); once dP^T is read, P^T and dS^T are
+//             written over it as bf16 for dV += P^T dO and dK += dS^T Q, both
+//             with A from TMEM; dK, dV accumulate in TMEM over all query
+//             tiles.
 //   bwd_dq    one CTA per 128-query tile (Q-tile parallel): Q_i, dO_i are
 //             written into TMEM by the compute threads and stay; K_j / V_j
 //             stream; S = Q K^T and dP = dO V^T take Q, dO from TMEM; dQ +=
@@ -41,21 +42,19 @@ struct Bwd {
     static constexpr int OFF_FIXED = 0;       // two resident tiles
     static constexpr int OFF_STAGE = 2 * TILE;  // 2 stages x 2 streamed tiles
     static constexpr int OFF_VEC = OFF_STAGE + 4 * TILE;  // dkdv: lse2/delta per stage (2 x 1 KB)
-    static constexpr int OFF_PT = OFF_VEC + 2048;         // dkdv: P^T bf16, 128 keys x 128 queries, K-major
-    static constexpr int OFF_BAR = OFF_PT + 128 * 128 * 2;
+    static constexpr int OFF_BAR = OFF_VEC + 2048;
     static constexpr int NBAR = 16;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16;  // the dynamic shared array is declared 1024-aligned
     static constexpr int THREADS = 320;  // warps 0-7 compute (two warpgroups), 8 producer, 9 MMA
     static constexpr int PRODUCER = 8, MMA = 9;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_A = 0;      // S / S^T fp32 (the dK/dV pass keeps P^T in shared memory)
-    static constexpr uint32_t COL_B = 128;    // dP / dP^T fp32; dS / dS^T bf16 over its first 64
+    static constexpr uint32_t COL_A = 0;      // S / S^T fp32
+    static constexpr uint32_t COL_B = 128;    // dP / dP^T fp32; dS (dQ pass) or P^T and dS^T (dK/dV pass) bf16 over it
     static constexpr uint32_t COL_ACC0 = 256; // dV (dkdv) or dQ (dq)
     static constexpr uint32_t COL_ACC1 = 256 + D;  // dK (dkdv)
     static constexpr uint32_t IDESC_SS = idesc_bf16(128, 128, 0, 0);
     static constexpr uint32_t IDESC_TS = idesc_bf16(128, D, 0, 1);
-    static constexpr uint32_t IDESC_SM = idesc_bf16(128, D, 0, 1);  // A K-major smem, B MN-major
 };
 
 struct BwdParams {
@@ -163,7 +162,8 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t sA, uint32_t 
 // Issue C[tmem] (+)= A[tmem, 128 x 128 bf16] B[smem, 128 x D, MN-major].  The
 // two compute warpgroups write the bf16 A operand in two halves, K = 0..63 at
 // columns a_tmem + [0, 32) and K = 64..127 at a_tmem + [64, 96), each over the
-// fp32 columns that warpgroup has itself already read.
+// fp32 columns that warpgroup has itself already read (the dK/dV pass puts P^T
+// at a_tmem = COL_B and dS^T at a_tmem = COL_B + 32, filling both halves).
 template <int D>
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, bool acc) {
 #pragma unroll
@@ -255,15 +255,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t s_base = smem_u32(smem);
     const uint32_t bar0 = s_base + C::OFF_BAR;
     // barriers
-    // S: S^T ready; SF: S^T read out of TMEM (the next S^T may overwrite it); P: P^T written
-    // to shared memory; PV: dV product done (P^T buffer free again); DP, DS: dP^T ready, dS^T written
+    // S: S^T ready; SF: S^T read out of TMEM (the next S^T may overwrite it); DP: dP^T ready;
+    // DS: P^T and dS^T written over dP^T (bf16, TMEM)
     const uint32_t B_KV = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_DP = bar0 + 48,
-                   B_P = bar0 + 56, B_DS = bar0 + 64, B_ACC = bar0 + 72, B_TD = bar0 + 80, B_SF = bar0 + 88,
-                   B_PV = bar0 + 96;
-    const uint32_t counts[13] = {1, 32, 32, 1, 1, 1, 1, 256, 256, 1, 1, 256, 1};
+                   B_DS = bar0 + 56, B_ACC = bar0 + 64, B_TD = bar0 + 72, B_SF = bar0 + 80;
+    const uint32_t counts[11] = {1, 32, 32, 1, 1, 1, 1, 256, 1, 1, 256};
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
-    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 13);
+    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 11);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int bh, kt;  // key tile 0 (the most query tiles when causal) first, heads in L2-sized chunks
@@ -286,7 +285,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     auto sQ = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
     auto sDO = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
     float* vec = (float*)(smem + C::OFF_VEC);  // stage s: lse2 at [s*256], delta at [s*256 + 128]
-    const uint32_t sPT = s_base + C::OFF_PT;    // P^T: query chunk c at c * CHUNK, key row r at r * 128
 
     if (warp == C::PRODUCER) {
         // ------------------------------------------------------------ producer (whole warp)
@@ -358,8 +356,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 issue_ss<D>(tmem + C::COL_B, sV, sDO(0));
                 mma_commit(B_DP);
             }
-            // order per query tile: S^T(i+1) as soon as S^T(i) has been read out of TMEM,
-            // dV(i) once P^T(i) is in shared memory, dK(i) once dS^T(i) is in TMEM, dP^T(i+1)
+            // order per query tile: S^T(i+1) as soon as S^T(i) has been read out of TMEM;
+            // dV(i) and dK(i) once P^T(i) and dS^T(i) are in TMEM; dP^T(i+1) over them (the
+            // tensor pipe runs in order, so it overwrites them only after both products)
             for (int ii = 0; ii < n && ok; ++ii) {
                 const int st = ii & 1;
                 const bool more = ii + 1 < n;
@@ -370,16 +369,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     issue_ss<D>(tmem + C::COL_A, sK, sQ(st ^ 1));  // S^T of the next query tile
                     mma_commit(B_S);
                 }
-                if (!(ok = mbar_wait(B_P, ii & 1, ctl, kSiteBwdP))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 8; ++k)  // dV += P^T dO: A = P^T (smem, K-major), B = dO (MN-major)
-                    mma_ss(tmem + C::COL_ACC0, sdesc_sw128(sPT + (k >> 2) * C::CHUNK + (k & 3) * 32, 16, 1024),
-                           sdesc_sw128(sDO(st) + k * 2048, C::CHUNK, 1024), C::IDESC_SM, (ii > 0 || k > 0) ? 1u : 0u);
-                mma_commit(B_PV);
                 if (!(ok = mbar_wait(B_DS, ii & 1, ctl, kSiteBwdDS))) break;
                 tc_fence_after();
-                issue_ts<D>(tmem + C::COL_ACC1, tmem + C::COL_B, sQ(st), ii > 0);  // dK += dS^T Q
+                issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sDO(st), ii > 0);      // dV += P^T dO
+                issue_ts<D>(tmem + C::COL_ACC1, tmem + C::COL_B + 32, sQ(st), ii > 0);  // dK += dS^T Q
                 mma_commit(B_STE + 8 * st);
                 if (more) {
                     issue_ss<D>(tmem + C::COL_B, sV, sDO(st ^ 1));  // dP^T of the next query tile
@@ -454,27 +447,18 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 p_phase(std::true_type{});
             else
                 p_phase(std::false_type{});
-            // P^T row r, queries [64h, 64h + 64): query chunk h, 16-byte granule g stored at
-            // g ^ (r & 7) (128-byte swizzle, matching the K-major operand descriptor)
-            if (ii > 0 && !(ok = mbar_wait(B_PV, (ii - 1) & 1, ctl, kSiteBwdP))) break;  // dV(i-1) has read it
-            {
-                uint8_t* prow = smem + C::OFF_PT + h * C::CHUNK + r * 128;
-#pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    *reinterpret_cast<uint4*>(prow + ((g ^ (r & 7)) << 4)) =
-                        make_uint4(pp[4 * g], pp[4 * g + 1], pp[4 * g + 2], pp[4 * g + 3]);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
-            mbar_arrive(B_P);
             if (!(ok = mbar_wait(B_DP, ii & 1, ctl, kSiteBwdDP))) break;
             tc_fence_after();
+            // this warpgroup's 64 dP^T columns; once both chunks are in registers, its bf16 P^T
+            // goes over the first 32 of them and dS^T over the last 32
             tmem_ld32_async(lane_addr + colB, va);
-            tmem_wait_ld(va);
             tmem_ld32_async(lane_addr + colB + 32, vb);
+            tmem_wait_ld(va);
+            tmem_wait_ld(vb);
+            tmem_st32_async(lane_addr + colB, pp);
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
                 uint32_t(&v)[32] = q4 ? vb : va;
-                if (q4) tmem_wait_ld(vb);
                 float dv[32];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -489,7 +473,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     const float b = bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dv[2 * e + 1]);
                     pk[e] = pack_bf16(a, b);
                 }
-                tmem_st16_async(lane_addr + colB + q4 * 16, pk);
+                tmem_st16_async(lane_addr + colB + 32 + q4 * 16, pk);
             }
             tmem_wait_st();
             tc_fence_before();

@@ -318,6 +318,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         FA_W8(0), FA_W8(8), FA_W8(16), FA_W8(24)
         : "memory");
 }
+// registers -> TMEM, 32 lanes x 32 columns, not waited for: pair with
+// tmem_wait_st before the columns are read by anyone else.
+__device__ __forceinline__ void tmem_st32_async(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        FA_W8(0), FA_W8(8), FA_W8(16), FA_W8(24)
+        : "memory");
+}
 // registers -> TMEM, 32 lanes x 16 columns, not waited for: pair with
 // tmem_wait_st before the columns are read by anyone else.
 __device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t (&r)[16]) {
