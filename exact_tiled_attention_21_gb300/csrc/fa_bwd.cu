@@ -149,13 +149,16 @@ __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u <<
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
 // Issue C[tmem] = A B^T over K = D with both operands K-major 128-row tiles.
+// The single issuing thread spends a few instructions per MMA: one descriptor
+// of each operand per call, constant offsets per k-step, fixed accumulate flags.
 template <int D>
 __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t sA, uint32_t sB) {
+    const uint64_t a0 = sdesc_sw128(sA, 16, 1024), b0 = sdesc_sw128(sB, 16, 1024);
+    mma_ss_first(d_tmem, a0, b0, Bwd<D>::IDESC_SS);
 #pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
+    for (int k = 1; k < D / 16; ++k) {
         const uint32_t off = (k >> 2) * Bwd<D>::CHUNK + (k & 3) * 32;
-        mma_ss(d_tmem, sdesc_sw128(sA + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024),
-               Bwd<D>::IDESC_SS, k > 0);
+        mma_ss_acc(d_tmem, sdesc_add(a0, off), sdesc_add(b0, off), Bwd<D>::IDESC_SS);
     }
 }
 
@@ -166,20 +169,23 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t sA, uint32_t 
 // at a_tmem = COL_B and dS^T at a_tmem = COL_B + 32, filling both halves).
 template <int D>
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, bool acc) {
+    const uint64_t b0 = sdesc_sw128(sB, Bwd<D>::CHUNK, 1024);
+    mma_ts(d_tmem, a_tmem, b0, Bwd<D>::IDESC_TS, acc ? 1u : 0u);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-        mma_ts(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), sdesc_sw128(sB + k * 2048, Bwd<D>::CHUNK, 1024),
-               Bwd<D>::IDESC_TS, (acc || k > 0) ? 1u : 0u);
+    for (int k = 1; k < 8; ++k)
+        mma_ts_acc(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), sdesc_add(b0, k * 2048), Bwd<D>::IDESC_TS);
 }
 
 // Issue C[tmem] = A[tmem, 128 x D bf16] B^T with B a K-major 128-row tile in
 // shared memory (the score products of the dQ pass: Q or dO from TMEM).
 template <int D>
 __device__ __forceinline__ void issue_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB) {
+    const uint64_t b0 = sdesc_sw128(sB, 16, 1024);
+    mma_ts(d_tmem, a_tmem, b0, Bwd<D>::IDESC_SS, 0u);
 #pragma unroll
-    for (int k = 0; k < D / 16; ++k)
-        mma_ts(d_tmem, a_tmem + k * 8, sdesc_sw128(sB + (k >> 2) * Bwd<D>::CHUNK + (k & 3) * 32, 16, 1024),
-               Bwd<D>::IDESC_SS, k > 0);
+    for (int k = 1; k < D / 16; ++k)
+        mma_ts_acc(d_tmem, a_tmem + k * 8, sdesc_add(b0, (k >> 2) * Bwd<D>::CHUNK + (k & 3) * 32),
+                   Bwd<D>::IDESC_SS);
 }
 
 // Writes columns [c0, c0 + D/2) of a 128-row accumulator row (thread = row)

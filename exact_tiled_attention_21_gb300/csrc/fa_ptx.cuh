@@ -251,6 +251,31 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// The same two products with the accumulate flag fixed: off (the first k-step
+// of a product) or on (every later one), so the issuing thread spends no
+// instruction on it.
+__device__ __forceinline__ void mma_ss_first(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem), "l"(adesc),
+                 "l"(bdesc), "r"(idesc)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_ss_acc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem), "l"(adesc),
+                 "l"(bdesc), "r"(idesc)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_ts_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem), "r"(a_tmem),
+                 "l"(bdesc), "r"(idesc)
+                 : "memory");
+}
+
+// Descriptor of (saddr + off) from the descriptor of saddr: the start-address
+// field is (addr >> 4) in the low 14 bits, and shared-memory addresses stay
+// below 2^18, so a 16-byte-multiple offset adds without a carry into the next
+// field.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t off) { return desc + (uint64_t)(off >> 4); }
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
