@@ -300,20 +300,22 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             int slot = 0;
             uint32_t phase = 0, q_iter = 0, p_iter = 0;
             const uint32_t sQ0 = s_base + C::OFF_Q, sQ1 = sQ0 + C::Q_BYTES;
+            // one descriptor per operand per product; k-steps add constant offsets
             auto issue_s = [&](uint32_t d_col, uint32_t sQ, uint32_t sK) {
+                const uint64_t a0 = sdesc_sw128(sQ, 16, 1024), b0 = sdesc_sw128(sK, 16, 1024);
+                mma_ss_first(tmem + d_col, a0, b0, C::IDESC_S);
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
+                for (int k = 1; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
-                    mma_ss(tmem + d_col, sdesc_sw128(sQ + off, 16, 1024),
-                           sdesc_sw128(sK + off, 16, 1024), C::IDESC_S, k > 0);
+                    mma_ss_acc(tmem + d_col, sdesc_add(a0, off), sdesc_add(b0, off), C::IDESC_S);
                 }
             };
             auto issue_o = [&](uint32_t d_col, uint32_t p_col, uint32_t sV, bool acc) {
+                const uint64_t b0 = sdesc_sw128(sV, C::CHUNK_BYTES, 1024);
+                mma_ts(tmem + d_col, tmem + p_col, b0, C::IDESC_O, acc ? 1u : 0u);
 #pragma unroll
-                for (int k = 0; k < C::BN / 16; ++k)
-                    mma_ts(tmem + d_col, tmem + p_col + k * 8,
-                           sdesc_sw128(sV + k * 2048, C::CHUNK_BYTES, 1024), C::IDESC_O,
-                           (acc || k > 0) ? 1u : 0u);
+                for (int k = 1; k < C::BN / 16; ++k)
+                    mma_ts_acc(tmem + d_col, tmem + p_col + k * 8, sdesc_add(b0, k * 2048), C::IDESC_O);
             };
             auto next = [&]() {
                 if (++slot == C::NSLOT) {

@@ -57,6 +57,12 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
         "l"(adesc), "l"(bdesc), "r"(kIdescF8), "r"(accumulate)
         : "memory");
 }
+// The same with the accumulate flag fixed on (every k-step after the first).
+__device__ __forceinline__ void mma_f8_acc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, 1;" ::"r"(d_tmem), "l"(adesc),
+                 "l"(bdesc), "r"(kIdescF8)
+                 : "memory");
+}
 
 // Four fp32 values -> four e4m3 bytes (x0 in the lowest byte), round to nearest
 // even, saturating at the largest finite value.
@@ -271,16 +277,19 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             const uint32_t sQ0 = s_base + C::OFF_Q, sQ1 = sQ0 + C::TILE;
             const uint32_t sP0 = s_base + C::OFF_P, sP1 = sP0 + C::TILE;
             // A and B both K-major, 128-byte rows: K step k starts 32 k bytes into the rows
+            // one descriptor per operand per product; k-steps add constant offsets
             auto issue_s = [&](uint32_t d_col, uint32_t sQ, uint32_t sK) {
+                const uint64_t a0 = sdesc_sw128(sQ, 16, 1024), b0 = sdesc_sw128(sK, 16, 1024);
+                mma_f8(tmem + d_col, a0, b0, 0u);
 #pragma unroll
-                for (int k = 0; k < D / 32; ++k)
-                    mma_f8(tmem + d_col, sdesc_sw128(sQ + 32 * k, 16, 1024), sdesc_sw128(sK + 32 * k, 16, 1024), k > 0);
+                for (int k = 1; k < D / 32; ++k) mma_f8_acc(tmem + d_col, sdesc_add(a0, 32 * k), sdesc_add(b0, 32 * k));
             };
             auto issue_o = [&](uint32_t d_col, uint32_t sP, uint32_t sVt, bool acc) {
+                const uint64_t a0 = sdesc_sw128(sP, 16, 1024), b0 = sdesc_sw128(sVt, 16, 1024);
+                mma_f8(tmem + d_col, a0, b0, acc ? 1u : 0u);
 #pragma unroll
-                for (int k = 0; k < 128 / 32; ++k)
-                    mma_f8(tmem + d_col, sdesc_sw128(sP + 32 * k, 16, 1024), sdesc_sw128(sVt + 32 * k, 16, 1024),
-                           (acc || k > 0) ? 1u : 0u);
+                for (int k = 1; k < 128 / 32; ++k)
+                    mma_f8_acc(tmem + d_col, sdesc_add(a0, 32 * k), sdesc_add(b0, 32 * k));
             };
             auto next = [&]() {
                 if (++slot == C::NSLOT) {
