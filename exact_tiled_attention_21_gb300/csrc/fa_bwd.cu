@@ -46,8 +46,11 @@ struct Bwd {
     static constexpr int NBAR = 16;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16;  // the dynamic shared array is declared 1024-aligned
-    static constexpr int THREADS = 320;  // warps 0-7 compute (two warpgroups), 8 producer, 9 MMA
-    static constexpr int PRODUCER = 8, MMA = 9;
+    // warps 0-7 compute (two warpgroups), 8 producer, 9 MMA issuer; the dK/dV pass adds warp 10,
+    // a second issuer: there one thread cannot issue MMAs as fast as the tensor pipe runs them
+    // while eight warps load the SM
+    static constexpr int THREADS_DQ = 320, THREADS_DKDV = 352;
+    static constexpr int PRODUCER = 8, MMA = 9, MMA2 = 10;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_A = 0;      // S / S^T fp32
     static constexpr uint32_t COL_B = 128;    // dP / dP^T fp32; dS (dQ pass) or P^T and dS^T (dK/dV pass) bf16 over it
@@ -251,7 +254,7 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
 
 // ------------------------------------------------------------------ dK, dV (KV-tile parallel)
 template <int D>
-__global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
+__global__ void __launch_bounds__(Bwd<D>::THREADS_DKDV, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                 const BwdParams p) {
@@ -263,12 +266,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // barriers
     // S: S^T ready; SF: S^T read out of TMEM (the next S^T may overwrite it); DP: dP^T ready;
     // DS: P^T and dS^T written over dP^T (bf16, TMEM)
+    // STE[s]: stage s free, once both issuers' products that read it are done (two arrivals);
+    // TD, TD2: teardown of issuer 1 and 2
     const uint32_t B_KV = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_DP = bar0 + 48,
-                   B_DS = bar0 + 56, B_ACC = bar0 + 64, B_TD = bar0 + 72, B_SF = bar0 + 80;
-    const uint32_t counts[11] = {1, 32, 32, 1, 1, 1, 1, 256, 1, 1, 256};
+                   B_DS = bar0 + 56, B_ACC = bar0 + 64, B_TD = bar0 + 72, B_SF = bar0 + 80, B_TD2 = bar0 + 88;
+    const uint32_t counts[12] = {1, 32, 32, 2, 2, 1, 1, 256, 1, 1, 256, 1};
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
-    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 11);
+    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 12);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int bh, kt;  // key tile 0 (the most query tiles when causal) first, heads in L2-sized chunks
@@ -351,44 +356,54 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
         }
     } else if (warp == C::MMA) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issuer 1: S^T
+        // S^T(i) once S^T(i-1) has been read out of TMEM and stage i is loaded
+        if (lane == 0 && !*abort_flag && n > 0) {
+            bool ok = mbar_wait(B_KV, 0, ctl, kSiteBwdKvFull);
+            for (int ii = 0; ii < n && ok; ++ii) {
+                const int st = ii & 1;
+                if (ii > 0 && !(ok = mbar_wait(B_SF, (ii - 1) & 1, ctl, kSiteBwdS))) break;
+                if (!(ok = mbar_wait(B_STF + 8 * st, (ii >> 1) & 1, ctl, kSiteBwdQFull))) break;
+                tc_fence_after();
+                issue_ss<D>(tmem + C::COL_A, sK, sQ(st));
+                mma_commit(B_S);
+                mma_commit(B_STE + 8 * st);
+            }
+            if (*abort_flag) {
+                mma_commit(B_TD);
+                mbar_drain(B_TD, 0, ctl, kSiteTeardown);
+            }
+        }
+    } else if (warp == C::MMA2) {
+        // ------------------------------------------------------------ MMA issuer 2: dP^T, dV, dK
+        // dV(i) and dK(i) once P^T(i) and dS^T(i) are in TMEM; dP^T(i+1) over them (this
+        // thread's products run in issue order, so it overwrites them only after both)
         if (lane == 0 && !*abort_flag && n > 0) {
             bool ok = mbar_wait(B_KV, 0, ctl, kSiteBwdKvFull);
             if (ok) ok = mbar_wait(B_STF, 0, ctl, kSiteBwdQFull);
             if (ok) {
                 tc_fence_after();
-                issue_ss<D>(tmem + C::COL_A, sK, sQ(0));
-                mma_commit(B_S);
                 issue_ss<D>(tmem + C::COL_B, sV, sDO(0));
                 mma_commit(B_DP);
             }
-            // order per query tile: S^T(i+1) as soon as S^T(i) has been read out of TMEM;
-            // dV(i) and dK(i) once P^T(i) and dS^T(i) are in TMEM; dP^T(i+1) over them (the
-            // tensor pipe runs in order, so it overwrites them only after both products)
             for (int ii = 0; ii < n && ok; ++ii) {
                 const int st = ii & 1;
-                const bool more = ii + 1 < n;
-                if (more) {
-                    if (!(ok = mbar_wait(B_SF, ii & 1, ctl, kSiteBwdS))) break;
-                    if (!(ok = mbar_wait(B_STF + 8 * (st ^ 1), ((ii + 1) >> 1) & 1, ctl, kSiteBwdQFull))) break;
-                    tc_fence_after();
-                    issue_ss<D>(tmem + C::COL_A, sK, sQ(st ^ 1));  // S^T of the next query tile
-                    mma_commit(B_S);
-                }
                 if (!(ok = mbar_wait(B_DS, ii & 1, ctl, kSiteBwdDS))) break;
                 tc_fence_after();
                 issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sDO(st), ii > 0);      // dV += P^T dO
                 issue_ts<D>(tmem + C::COL_ACC1, tmem + C::COL_B + 32, sQ(st), ii > 0);  // dK += dS^T Q
                 mma_commit(B_STE + 8 * st);
-                if (more) {
+                if (ii + 1 < n) {
+                    if (!(ok = mbar_wait(B_STF + 8 * (st ^ 1), ((ii + 1) >> 1) & 1, ctl, kSiteBwdQFull))) break;
+                    tc_fence_after();
                     issue_ss<D>(tmem + C::COL_B, sV, sDO(st ^ 1));  // dP^T of the next query tile
                     mma_commit(B_DP);
                 }
             }
             if (ok) mma_commit(B_ACC);
             if (*abort_flag) {
-                mma_commit(B_TD);
-                mbar_drain(B_TD, 0, ctl, kSiteTeardown);
+                mma_commit(B_TD2);
+                mbar_drain(B_TD2, 0, ctl, kSiteTeardown);
             }
         }
     } else {
@@ -503,7 +518,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 
 // ------------------------------------------------------------------ dQ (Q-tile parallel)
 template <int D>
-__global__ void __launch_bounds__(Bwd<D>::THREADS, 1)
+__global__ void __launch_bounds__(Bwd<D>::THREADS_DQ, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
               const BwdParams p) {
@@ -766,7 +781,7 @@ cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const BwdParams p = make_params(a);
-    bwd_dkdv_kernel<D><<<p.n_kt * p.BH, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, a.map_do, p);
+    bwd_dkdv_kernel<D><<<p.n_kt * p.BH, C::THREADS_DKDV, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, a.map_do, p);
     return cudaGetLastError();
 }
 
@@ -776,7 +791,7 @@ cudaError_t launch_dq_d(const BwdLaunch& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const BwdParams p = make_params(a);
-    bwd_dq_kernel<D><<<p.n_qt * p.BH, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, a.map_do, p);
+    bwd_dq_kernel<D><<<p.n_qt * p.BH, C::THREADS_DQ, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, a.map_do, p);
     return cudaGetLastError();
 }
 
