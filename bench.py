@@ -352,23 +352,26 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("device error in the end-to-end run: %s" % detail)
 
     # The same fwd + bwd step from host buffers, pipelined the way a training loop
-    # feeds a GPU: step i's inputs copy in (stream s_in) and step i-1's results copy
-    # out (s_out) while step i-1 / i compute; two sets of device tensors alternate.
-    # Every step still moves its own inputs in and its own results out inside the
-    # timed region; the time is first copy-in to last copy-out over all steps.
+    # feeds a GPU: step i+1's inputs copy in (stream s_in) and step i-1's results copy
+    # out (s_out) while step i computes; three sets of device tensors rotate, so a
+    # copy-in never waits for the copy-out of the set before it and the two
+    # directions of the host link run at the same time.  Every step still moves its
+    # own inputs in and its own results out inside the timed region; the time is
+    # first copy-in to last copy-out over all steps.
+    NSETS = 3
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    sets = [(q, k, v, dO, o, lse, dq, dk, dv),
-            tuple(torch.empty_like(t) for t in (q, k, v, dO, o, lse, dq, dk, dv))]
-    bws2 = torch.empty_like(bws)
+    sets = [(q, k, v, dO, o, lse, dq, dk, dv)] + [
+        tuple(torch.empty_like(t) for t in (q, k, v, dO, o, lse, dq, dk, dv)) for _ in range(NSETS - 1)]
+    bws_sets = [bws] + [torch.empty_like(bws) for _ in range(NSETS - 1)]
 
     def pipelined(nsteps, t0, t1):
-        free = [None, None]
-        ready = [torch.cuda.Event() for _ in range(2)]
-        done = [torch.cuda.Event() for _ in range(2)]
+        free = [None] * NSETS
+        ready = [torch.cuda.Event() for _ in range(NSETS)]
+        done = [torch.cuda.Event() for _ in range(NSETS)]
         t0.record(stream)
         s_in.wait_event(t0)
         for i in range(nsteps):
-            b = i % 2
+            b = i % NSETS
             q_, k_, v_, dO_, o_, lse_, dq2, dk2, dv2 = sets[b]
             if free[b] is not None:
                 s_in.wait_event(free[b])
@@ -377,7 +380,7 @@ def run_ours(args, rank, world, local_rank):
                     d_.copy_(h_, non_blocking=True)
             ready[b].record(s_in)
             stream.wait_event(ready[b])
-            ws_ = bws if b == 0 else bws2
+            ws_ = bws_sets[b]
             fa.fa_fwd(q_, k_, v_, o_, lse_, B, H, N, N, D, SCALE, True, stream)
             fa.fa_bwd(q_, k_, v_, o_, lse_, dO_, dq2, dk2, dv2, B, H, N, N, D, SCALE, True, ws_, ws_.numel(),
                       stream)
@@ -513,7 +516,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": world * (FWD_FLOPS + BWD_FLOPS) / (e2e_fb * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "pipelined": "copies of neighbouring steps overlap this step's compute (separate copy-in and "
-                             "copy-out streams, two alternating sets of device tensors)",
+                             "copy-out streams, three rotating sets of device tensors)",
                 "serial_value": world * (FWD_FLOPS + BWD_FLOPS) / (e2e_fb_serial * 1e-3) / 1e12,
                 "decode_gbs": world * DEC_BYTES / (e2e_dec * 1e-3) / 1e9,
                 "decode_h2d_bytes": h2d_dec, "decode_d2h_bytes": d2h_dec,

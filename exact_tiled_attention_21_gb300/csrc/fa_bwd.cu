@@ -667,17 +667,20 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             if (!(ok = mbar_wait(B_S, jj & 1, ctl, kSiteBwdS))) break;
             tc_fence_after();
             uint32_t pp[32];
-            uint32_t va[32], vb[32];  // chunk 1 loads while chunk 0 is processed
+            uint32_t va[32], vb[32];
+            // read this warpgroup's 64 S columns, then release them: the next S may overwrite
+            tmem_ld32_async(lane_addr + colA, va);
+            tmem_ld32_async(lane_addr + colA + 32, vb);
+            tmem_wait_ld(va);
+            tmem_wait_ld(vb);
+            tc_fence_before();
+            mbar_arrive(B_SF);
             // masked entries: columns c > cmax (keys past Nk or, causal, past the
             // row's limit); tiles with none in the warp skip the test.
             auto p_phase = [&](auto MASK) {
-            tmem_ld32_async(lane_addr + colA, va);
-            tmem_wait_ld(va);
-            tmem_ld32_async(lane_addr + colA + 32, vb);
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
                 uint32_t(&v)[32] = q4 ? vb : va;
-                if (q4) tmem_wait_ld(vb);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int c0 = q4 * 32 + 2 * e;
@@ -696,8 +699,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                 p_phase(std::true_type{});
             else
                 p_phase(std::false_type{});
-            tc_fence_before();
-            mbar_arrive(B_SF);
             if (!(ok = mbar_wait(B_DP, jj & 1, ctl, kSiteBwdDP))) break;
             tc_fence_after();
             tmem_ld32_async(lane_addr + colB, va);
