@@ -62,6 +62,31 @@ def test_backward_parity(cuda_lib, B, H, Nq, Nk, d, causal):
     check_grad(f64(dv), rv, "dV " + tag)
 
 
+# Many heads at small N, every head checked: grids of several waves of CTAs
+# (B*H = the SM count, times the key or query tiles per head).
+MANY_HEAD_CASES = [
+    (384, 384, 64, True),
+    (200, 256, 128, False),   # ragged query tail
+]
+
+
+@pytest.mark.parametrize("Nq,Nk,d,causal", MANY_HEAD_CASES)
+def test_backward_parity_many_heads(cuda_lib, Nq, Nk, d, causal):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, H = (2, sms // 2) if sms % 2 == 0 else (1, sms)
+    seed = 900 + Nq * 3 + Nk + d + causal
+    q, k, v, dO = _inputs(seed, B, H, Nq, Nk, d)
+    scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = _run(cuda_lib, q, k, v, dO, scale, causal)
+    rq, rk, rv = naive.backward(f64(q), f64(k), f64(v), f64(dO), scale, causal)
+    tag = "B%d H%d Nq%d Nk%d d%d c%d" % (B, H, Nq, Nk, d, causal)
+    dp_max = np.abs(f64(dO) @ np.swapaxes(f64(v), -1, -2)).max()
+    cancel = scale * dp_max * max(np.abs(f64(k)).max(), np.abs(f64(q)).max())
+    check_grad(f64(dq), rq, "dQ " + tag, cancel_scale=cancel)
+    check_grad(f64(dk), rk, "dK " + tag, cancel_scale=cancel)
+    check_grad(f64(dv), rv, "dV " + tag)
+
+
 def test_backward_deterministic(cuda_lib):
     """No atomics anywhere: two runs give identical bits."""
     q, k, v, dO = _inputs(9, 1, 4, 640, 640, 128)

@@ -20,6 +20,9 @@ CASES = [
     (2, 300, 900, 64, True, [300, 17, 256, 1], [900, 1, 500, 256]),   # Nk > Nq: queries at the end
     (2, 900, 300, 128, True, [900, 300, 40, 600], [300, 300, 200, 1]),  # rows that see no key
     (3, 256, 256, 64, False, [256, 255], [128, 129]),
+    # many heads; key tiles of empty sequences (no query tile, dK = dV = 0) among
+    # the others
+    (40, 384, 384, 64, True, [384, 100, 0, 257], [384, 128, 0, 300]),
 ]
 
 
