@@ -273,6 +273,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t counts[12] = {1, 32, 32, 2, 2, 1, 1, 256, 1, 1, 256, 1};
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
+    // the dQ pass launched after this grid may start on SMs this grid leaves free
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 12);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -733,6 +735,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
     }
     bwd_teardown<D>(tmem);
+    // When launched to overlap the end of the dK/dV grid, this grid must not finish before
+    // it: work that follows both on the stream may read dK and dV once this grid is done.
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 BwdParams make_params(const BwdLaunch& a) {
@@ -786,14 +791,28 @@ cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// after_dkdv: launched right after the dK/dV grid on the same stream.  The two
+// passes are independent (both only read the preprocess's D), so this grid is
+// launched as a programmatic dependent: its CTAs may take the SMs that the
+// dK/dV grid's last wave leaves free.
 template <int D>
-cudaError_t launch_dq_d(const BwdLaunch& a, cudaStream_t s) {
+cudaError_t launch_dq_d(const BwdLaunch& a, cudaStream_t s, bool after_dkdv) {
     using C = Bwd<D>;
     cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const BwdParams p = make_params(a);
-    bwd_dq_kernel<D><<<p.n_qt * p.BH, C::THREADS_DQ, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, a.map_do, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.n_qt * p.BH));
+    cfg.blockDim = dim3(C::THREADS_DQ);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_dkdv ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D>, a.map_q, a.map_k, a.map_v, a.map_do, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -804,8 +823,8 @@ cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s) {
 cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s) {
     return a.d == 128 ? launch_dkdv_d<128>(a, s) : launch_dkdv_d<64>(a, s);
 }
-cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s) {
-    return a.d == 128 ? launch_dq_d<128>(a, s) : launch_dq_d<64>(a, s);
+cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s, bool after_dkdv) {
+    return a.d == 128 ? launch_dq_d<128>(a, s, after_dkdv) : launch_dq_d<64>(a, s, after_dkdv);
 }
 
 }  // namespace fa

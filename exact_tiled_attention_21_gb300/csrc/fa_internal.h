@@ -114,7 +114,8 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
 bool fwd_use_split(const FwdLaunch& a);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s);   // D = rowsum(dO o O)
 cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s);  // dK, dV
-cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s);    // dQ
+cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s, bool after_dkdv = false);  // dQ; after_dkdv:
+                                                                                     // overlaps the dK/dV grid's end
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_paged(const PagedDecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_paged_mma(const PagedDecodeLaunch& a, cudaStream_t s);

@@ -87,6 +87,32 @@ def test_backward_parity_many_heads(cuda_lib, Nq, Nk, d, causal):
     check_grad(f64(dv), rv, "dV " + tag)
 
 
+@pytest.mark.parametrize("B,H,N", [(1, 1, 128), (1, 2, 700), (1, 32, 2048)])
+def test_backward_matches_step_entry_points(cuda_lib, B, H, N):
+    """fa_bwd launches the dQ pass to overlap the end of the dK/dV pass: the
+    same kernels as the three step entry points, so the same bits; and work
+    queued on the stream right after fa_bwd sees finished dK and dV (the dQ
+    grid completes only after the dK/dV grid)."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    d = 128
+    q, k, v, dO = (t.to(dev) for t in _inputs(31 + N, B, H, N, N, d))
+    o, lse = fa.forward(q, k, v, causal=True)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, N, d), dtype=torch.uint8, device=dev)
+    dq1, dk1, dv1 = torch.empty_like(q), torch.full_like(k, float("nan")), torch.full_like(v, float("nan"))
+    fa.fa_bwd(q, k, v, o, lse, dO, dq1, dk1, dv1, B, H, N, N, d, d ** -0.5, True, ws, ws.numel())
+    dk_seen, dv_seen = dk1.clone(), dv1.clone()  # queued right behind fa_bwd, no synchronisation between
+    delta = torch.empty(B, H, N, device=dev)
+    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa.fa_bwd_preprocess(o, dO, delta, B, H, N, d)
+    fa.fa_bwd_dkdv(q, k, v, lse, delta, dO, dk2, dv2, B, H, N, N, d, d ** -0.5, True)
+    fa.fa_bwd_dq(q, k, v, lse, delta, dO, dq2, B, H, N, N, d, d ** -0.5, True)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error()[0] == 0
+    assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    assert torch.equal(dk_seen, dk2) and torch.equal(dv_seen, dv2)
+
+
 def test_backward_deterministic(cuda_lib):
     """No atomics anywhere: two runs give identical bits."""
     q, k, v, dO = _inputs(9, 1, 4, 640, 640, 128)
