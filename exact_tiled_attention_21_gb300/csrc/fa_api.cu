@@ -340,7 +340,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     a.lens_k = lens_k;
     cudaStream_t s = (cudaStream_t)stream;
     if ((st = launched(launch_bwd_pre(a, s))) != FA_OK) return st;
-    if ((st = launched(launch_bwd_dkdv(a, s))) != FA_OK) return st;
+    if ((st = launched(launch_bwd_dkdv(a, s, true))) != FA_OK) return st;
     return launched(launch_bwd_dq(a, s, true));
 }
 

@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(256)
 bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
                float* __restrict__ delta, long long rows) {
     constexpr int LPR = D / 8, RPW = 32 / LPR, STEPS = 4;
+    // the dK/dV pass launched after this grid may set up (and load K, V) meanwhile
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row0 = (long long)blockIdx.x * kPreRowsPerBlock<D> + (long long)warp * RPW * STEPS + lane / LPR;
     const int part = lane % LPR;
@@ -273,8 +275,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t counts[12] = {1, 32, 32, 2, 2, 1, 1, 256, 1, 1, 256, 1};
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
-    // the dQ pass launched after this grid may start on SMs this grid leaves free
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 12);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -298,6 +298,19 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     auto sQ = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
     auto sDO = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
     float* vec = (float*)(smem + C::OFF_VEC);  // stage s: lse2 at [s*256], delta at [s*256 + 128]
+    const bool kv_issued = warp == C::PRODUCER && lane == 0 && n > 0 && !*abort_flag;
+    if (kv_issued) {  // K and V do not come from the preprocess: they load before the wait for it
+        mbar_arrive_expect_tx(B_KV, 2 * C::TILE);
+        for (int c = 0; c < C::KCH; ++c) {
+            tma_load_3d(sK + c * C::CHUNK, &map_k, B_KV, c * 64, kt * 128, bh, l2_policy_evict_last());
+            tma_load_3d(sV + c * C::CHUNK, &map_v, B_KV, c * 64, kt * 128, bh, l2_policy_evict_last());
+        }
+    }
+    // Launched as a programmatic dependent of the preprocess, this grid may start before D is
+    // complete: every read of D comes after this wait.  Then the dQ pass launched after this grid
+    // (which reads D too) may start on SMs this grid leaves free.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == C::PRODUCER) {
         // ------------------------------------------------------------ producer (whole warp)
@@ -306,11 +319,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             if (lane == 0) {
                 tma_prefetch_desc(&map_q);
                 tma_prefetch_desc(&map_do);
-                mbar_arrive_expect_tx(B_KV, 2 * C::TILE);
-                for (int c = 0; c < C::KCH; ++c) {
-                    tma_load_3d(sK + c * C::CHUNK, &map_k, B_KV, c * 64, kt * 128, bh, pol);
-                    tma_load_3d(sV + c * C::CHUNK, &map_v, B_KV, c * 64, kt * 128, bh, pol);
-                }
             }
             uint32_t issued = 0, issued_par = 0;
             // per-column LSE*log2(e) and D of query tile i (4 values of each per lane),
@@ -352,7 +360,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 if (ii + 1 < n) fetch_vec(i + 1);
             }
             if (*abort_flag && lane == 0) {  // let the loads in flight land before exit
-                mbar_drain(B_KV, 0, ctl, kSiteTeardown);
+                if (kv_issued) mbar_drain(B_KV, 0, ctl, kSiteTeardown);
                 for (int st = 0; st < 2; ++st)
                     if (issued & (1u << st)) mbar_drain(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
             }
@@ -780,15 +788,27 @@ cudaError_t launch_pre_d(const BwdLaunch& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// after_pre: launched right after the preprocess on the same stream, as its
+// programmatic dependent (setup and the K/V loads overlap the preprocess's end).
 template <int D>
-cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t s) {
+cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t s, bool after_pre) {
     using C = Bwd<D>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const BwdParams p = make_params(a);
-    bwd_dkdv_kernel<D><<<p.n_kt * p.BH, C::THREADS_DKDV, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, a.map_do, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.n_kt * p.BH));
+    cfg.blockDim = dim3(C::THREADS_DKDV);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_pre ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<D>, a.map_q, a.map_k, a.map_v, a.map_do, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // after_dkdv: launched right after the dK/dV grid on the same stream.  The two
@@ -820,8 +840,8 @@ cudaError_t launch_dq_d(const BwdLaunch& a, cudaStream_t s, bool after_dkdv) {
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s) {
     return a.d == 128 ? launch_pre_d<128>(a, s) : launch_pre_d<64>(a, s);
 }
-cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s) {
-    return a.d == 128 ? launch_dkdv_d<128>(a, s) : launch_dkdv_d<64>(a, s);
+cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s, bool after_pre) {
+    return a.d == 128 ? launch_dkdv_d<128>(a, s, after_pre) : launch_dkdv_d<64>(a, s, after_pre);
 }
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s, bool after_dkdv) {
     return a.d == 128 ? launch_dq_d<128>(a, s, after_dkdv) : launch_dq_d<64>(a, s, after_dkdv);

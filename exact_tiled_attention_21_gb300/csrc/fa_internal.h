@@ -113,7 +113,8 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
 // 128-row split-KV tiles for a.B, a.H, a.Nq, a.Nk, a.causal on a.num_sms SMs.
 bool fwd_use_split(const FwdLaunch& a);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s);   // D = rowsum(dO o O)
-cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s);  // dK, dV
+cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s, bool after_pre = false);  // dK, dV; after_pre:
+                                                                                        // overlaps the preprocess's end
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s, bool after_dkdv = false);  // dQ; after_dkdv:
                                                                                      // overlaps the dK/dV grid's end
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);

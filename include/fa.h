@@ -160,9 +160,10 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
 
 /* The three steps of fa_bwd, for callers that schedule them (or time them)
  * separately; fa_bwd is exactly these three launches in this order, except
- * that it launches the dQ pass as a programmatic dependent of the dK/dV pass
- * (its CTAs may start on SMs that the last dK/dV CTAs leave free; the dQ grid
- * still completes only after the dK/dV grid has).
+ * that it launches each as a programmatic dependent of the one before: the
+ * dK/dV pass sets up and loads K/V while the preprocess ends, and the dQ pass
+ * may start on SMs that the last dK/dV CTAs leave free.  Every read of D still
+ * follows the preprocess, and the dQ grid completes only after the dK/dV grid.
  *  fa_bwd_preprocess: delta [B,H,Nq] fp32 = rowsum(dO o O).
  *  fa_bwd_dkdv: dk, dv [B,H,Nk,d] from q, k, v, lse, delta, dO; one CTA per
  *    128-key tile, P and dS rebuilt on chip for every query tile it sees.
