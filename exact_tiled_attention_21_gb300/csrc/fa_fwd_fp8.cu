@@ -18,6 +18,8 @@
 //   O_t += P_t V_j     P_t from shared memory (the softmax threads write their
 //                      row as e4m3, 128-byte swizzle), V_j^T from a transposed
 //                      copy of V (both operands K-major).
+// Since P_t does not alias S_t, S_t(j+1) is issued ahead of P_t V_j; a
+// pv_done[t] barrier tells the softmax when P_t and O_t may be written again.
 // The transposed copy [B*H, 128, Nk rounded up to 16] is made by vt_kernel into
 // the caller's workspace before the forward runs.
 #include "fa_internal.h"
@@ -33,8 +35,9 @@ struct F8 {
     static constexpr int OFF_P = 2 * TILE;      // P tiles t = 0, 1
     static constexpr int OFF_KV = 4 * TILE;
     static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
-    // q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2], o_final[2], teardown
-    static constexpr int NBAR = 2 + 2 * NSLOT + 7;
+    // q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2], o_final[2], teardown,
+    // pv_done[2]
+    static constexpr int NBAR = 2 + 2 * NSLOT + 9;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;
     static constexpr int THREADS = 320;
@@ -188,6 +191,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const uint32_t BAR_P = BAR_S + 16;                 // p_full[t]
     const uint32_t BAR_O = BAR_P + 16;                 // o_final[t]
     const uint32_t BAR_TD = BAR_O + 16;                // teardown
+    const uint32_t BAR_PV = BAR_TD + 8;               // pv_done[t]: P_t V_j done (P_t and O_t free again)
     uint32_t* tmem_slot = (uint32_t*)(smem + C::OFF_MISC);
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
@@ -207,6 +211,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             mbar_init(BAR_O + 8 * t, 1);
         }
         mbar_init(BAR_TD, 1);
+        mbar_init(BAR_PV, 1);
+        mbar_init(BAR_PV + 8, 1);
         fence_mbar_init();
         if ((s_base & 1023u) != 0) record_error(ctl, kErrTimeout, kSiteAlign, (int)(s_base & 1023u));
     }
@@ -317,6 +323,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                 issue_s(C::COL_S1, sQ1, sK);
                 mma_commit(BAR_S + 8);
                 mma_commit(bar_kve(kslot));
+                // Per block j and tile t: S_t(j+1) first, then P_t V_j.  P_t lives in shared
+                // memory, not over S_t, so the next scores need not wait for the value product;
+                // the softmax learns from pv_done[t] when P_t and O_t may be written again.
                 for (int j = 0; j < n; ++j) {
                     const int vslot = slot;
                     if (!mbar_wait(bar_kvf(vslot), phase, ctl, kSiteKvFull)) { ok = false; break; }
@@ -325,9 +334,6 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                     const bool more = j + 1 < n;
                     if (!mbar_wait(BAR_P, p_iter & 1, ctl, kSitePFull)) { ok = false; break; }
                     tc_fence_after();
-                    issue_o(C::COL_O0, sP0, sVt, j > 0);
-                    // S_0 of the next block is issued after P_0 V_j: when the softmax sees
-                    // it complete, the P_0 tile and O_0 are free to be written again
                     if (more) {
                         kslot = slot;
                         if (!mbar_wait(bar_kvf(kslot), phase, ctl, kSiteKvFull)) { ok = false; break; }
@@ -336,18 +342,21 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                         sK = s_base + C::OFF_KV + kslot * C::TILE;
                         issue_s(C::COL_S0, sQ0, sK);
                         mma_commit(BAR_S);
-                    } else {
-                        mma_commit(BAR_O);
                     }
+                    issue_o(C::COL_O0, sP0, sVt, j > 0);
+                    mma_commit(more ? BAR_PV : BAR_O);
                     if (!mbar_wait(BAR_P + 8, p_iter & 1, ctl, kSitePFull)) { ok = false; break; }
                     tc_fence_after();
                     ++p_iter;
-                    issue_o(C::COL_O1, sP1, sVt, j > 0);
-                    mma_commit(bar_kve(vslot));
                     if (more) {
                         issue_s(C::COL_S1, sQ1, sK);
                         mma_commit(BAR_S + 8);
                         mma_commit(bar_kve(kslot));
+                    }
+                    issue_o(C::COL_O1, sP1, sVt, j > 0);
+                    mma_commit(bar_kve(vslot));
+                    if (more) {
+                        mma_commit(BAR_PV + 8);
                     } else {
                         mma_commit(BAR_O + 8);
                         mma_commit(BAR_QE);
@@ -367,9 +376,10 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         const uint32_t col_s = t ? C::COL_S1 : C::COL_S0;
         const uint32_t col_o = t ? C::COL_O1 : C::COL_O0;
         const uint32_t bar_s = BAR_S + 8 * t, bar_p = BAR_P + 8 * t, bar_o = BAR_O + 8 * t;
+        const uint32_t bar_pv = BAR_PV + 8 * t;
         uint8_t* prow = smem + C::OFF_P + t * C::TILE + r * 128;
         const int off = p.Nk - p.Nq;
-        uint32_t s_iter = 0, o_iter = 0;
+        uint32_t s_iter = 0, o_iter = 0, pv_iter = 0;
         for (int rd = 0; rd * (int)gridDim.x < p.num_work; ++rd) {
             const int w = persistent_work(rd, blockIdx.x, gridDim.x);
             if (w >= p.num_work) continue;
@@ -397,6 +407,11 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                 const float mraw = masked ? f8_row_max<true>(lane_addr + col_s, lim2)
                                           : f8_row_max<false>(lane_addr + col_s, lim2);
                 const float m_new = fmaxf(m_use, mraw * c);
+                if (j > 0) {  // P_t V_{j-1} must be done before O_t is rescaled or P_t rewritten
+                    if (!mbar_wait(bar_pv, pv_iter & 1, ctl, kSitePFull)) { ok = false; break; }
+                    ++pv_iter;
+                    tc_fence_after();
+                }
                 if (j == 0) {
                     m_use = m_new;
                 } else if (__any_sync(0xffffffffu, m_new > m_use + 8.f)) {
