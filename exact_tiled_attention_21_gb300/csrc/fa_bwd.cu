@@ -794,7 +794,7 @@ template <int D>
 cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t s, bool after_pre) {
     using C = Bwd<D>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = set_smem_limit_once<bwd_dkdv_kernel<D>>(C::SMEM);
     if (e != cudaSuccess) return e;
     const BwdParams p = make_params(a);
     cudaLaunchConfig_t cfg = {};
@@ -818,7 +818,7 @@ cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t s, bool after_pre) {
 template <int D>
 cudaError_t launch_dq_d(const BwdLaunch& a, cudaStream_t s, bool after_dkdv) {
     using C = Bwd<D>;
-    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = set_smem_limit_once<bwd_dq_kernel<D>>(C::SMEM);
     if (e != cudaSuccess) return e;
     const BwdParams p = make_params(a);
     cudaLaunchConfig_t cfg = {};

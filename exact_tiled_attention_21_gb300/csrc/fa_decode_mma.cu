@@ -567,8 +567,7 @@ cudaError_t launch_nh(const PagedDecodeLaunch& a, MmaParams p, cudaStream_t s) {
     const long long nitems = (long long)a.B * a.Hkv * p.ngrp * a.splits;
     if (nitems > 0x7FFFFFFFll) return cudaErrorInvalidValue;
     p.nitems = (int)nitems;
-    cudaError_t e = cudaFuncSetAttribute(decode_paged_mma_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Dm::SMEM);
+    cudaError_t e = set_smem_limit_once<decode_paged_mma_kernel<NH>>(Dm::SMEM);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<long long>(nitems, a.num_sms);
     decode_paged_mma_kernel<NH><<<grid, Dm::THREADS, Dm::SMEM, s>>>(a.map_q, a.map_k, a.map_v, p);

@@ -604,8 +604,7 @@ cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
     using C = Fwd<D>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
     static_assert(!SPLIT || (!WIN && !VL), "split-KV tiles are built for the plain forward only");
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, WIN, VL, SPLIT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = set_smem_limit_once<fwd_kernel<D, WIN, VL, SPLIT>>(C::SMEM);
     if (e != cudaSuccess) return e;
     FwdParams p;
     p.o = (__nv_bfloat16*)a.o;

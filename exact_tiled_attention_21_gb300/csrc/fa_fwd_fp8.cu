@@ -516,7 +516,7 @@ cudaError_t launch_fwd_fp8(const Fp8FwdLaunch& a, cudaStream_t s) {
     vt_kernel<<<tg, 256, 0, s>>>((const uint8_t*)a.v, (uint8_t*)a.vt, a.Nk, a.Nk_pad);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F8::SMEM);
+    e = set_smem_limit_once<fwd_fp8_kernel>(F8::SMEM);
     if (e != cudaSuccess) return e;
     F8Params p;
     p.o = (__nv_bfloat16*)a.o;

@@ -2,6 +2,7 @@
 // kernel translation units.  Arguments arrive here already validated.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -106,6 +107,22 @@ struct Fp8FwdLaunch {
     DevError* err;
     uint64_t timeout_ns;
 };
+
+// The dynamic shared-memory limit of kernel K, raised once per device: the
+// attribute stays with the function in the context, and setting it costs a
+// driver call per launch otherwise.
+template <auto K>
+cudaError_t set_smem_limit_once(int bytes) {
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // Each returns a cudaError_t of the launch (cudaSuccess when queued).
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);

@@ -26,7 +26,9 @@
  *    Every call is asynchronous on it; nothing is synchronised.
  *  - Ownership: the caller allocates and owns every buffer, workspaces
  *    included.  The library allocates no device memory and keeps no state
- *    besides a cached driver entry point and a device-side error word.
+ *    besides a device-side error word and host-side caches (the tensor-map
+ *    encoder's entry point, each device's SM count, and which kernels'
+ *    shared-memory limits have been raised on which device).
  *  - Errors: return codes only (fa_status); arguments are validated before
  *    anything is launched, and an invalid call launches nothing.  No fallback
  *    implementation exists: an unsupported shape is an error, never a slower
