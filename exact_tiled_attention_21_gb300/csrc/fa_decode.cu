@@ -70,12 +70,19 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 
     for (int p0 = k0; p0 < k1; p0 += kDecPiece) {
-        // ---- scores of this piece
-        uint4 kr[STEPS];
+        // ---- scores of this piece (the piece's V rows are loaded with its K rows, so both
+        // are in flight together)
+        uint4 kr[STEPS], vr[STEPS];
 #pragma unroll
         for (int s = 0; s < STEPS; ++s) {
             const int key = p0 + s * KPC + group;
             kr[s] = key < k1 ? __ldg(reinterpret_cast<const uint4*>(Kb + (size_t)key * D))
+                             : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int s = 0; s < STEPS; ++s) {
+            const int key = p0 + s * KPC + group;
+            vr[s] = key < k1 ? __ldg(reinterpret_cast<const uint4*>(Vb + (size_t)key * D))
                              : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -119,13 +126,6 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] *= alpha;
         // ---- value product of this piece
-        uint4 vr[STEPS];
-#pragma unroll
-        for (int s = 0; s < STEPS; ++s) {
-            const int key = p0 + s * KPC + group;
-            vr[s] = key < k1 ? __ldg(reinterpret_cast<const uint4*>(Vb + (size_t)key * D))
-                             : make_uint4(0, 0, 0, 0);
-        }
 #pragma unroll
         for (int s = 0; s < STEPS; ++s) {
             const float pj = s_p[s * KPC + group];  // 0 for keys past the split
