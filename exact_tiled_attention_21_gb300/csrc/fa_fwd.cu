@@ -43,13 +43,17 @@ struct Fwd {
     static constexpr int OFF_KV = 2 * Q_BYTES;
     static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_BYTES;
     // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2], o_final[2], teardown,
-    // merge_ready, merge_done (split-KV)
-    static constexpr int NBAR = 2 + 2 * NSLOT + 9;
+    // merge_ready, merge_done (split-KV), pv_done[2] (P in its own columns)
+    static constexpr int NBAR = 2 + 2 * NSLOT + 11;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr int THREADS = 320;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+    // d = 64 leaves 128 TMEM columns: P_t then gets its own 64 (bf16 pairs), so S_t of the next
+    // key block need not wait for P_t V_j (with 256-row tiles; split-KV tiles keep P over S)
+    static constexpr bool P_OWN = D == 64;
+    static constexpr uint32_t COL_P0 = 384, COL_P1 = 448;
     static constexpr uint32_t IDESC_S = idesc_bf16(128, BN, 0, 0);  // Q, K both K-major
     static constexpr uint32_t IDESC_O = idesc_bf16(128, D, 0, 1);   // P from TMEM, V MN-major
 };
@@ -143,10 +147,11 @@ __device__ __forceinline__ float row_max_pass(uint32_t taddr, int lim2, int lo2)
 }
 
 // Pass 2: p = 2^(s c - m) for the 128 columns, their sum, and bf16 P written
-// over the S columns already read (keys [32 q, 32 q + 32) to columns
-// [16 q, 16 q + 16); the load in flight is always of columns >= 32 (q + 1)).
+// to paddr: either over the S columns already read (paddr = taddr: keys
+// [32 q, 32 q + 32) to columns [16 q, 16 q + 16); the load in flight is always
+// of columns >= 32 (q + 1)), or to columns of its own.
 template <bool MASKED>
-__device__ __forceinline__ float exp_pass(uint32_t taddr, int lim2, int lo2, float c, float msub) {
+__device__ __forceinline__ float exp_pass(uint32_t taddr, uint32_t paddr, int lim2, int lo2, float c, float msub) {
     float2 rs = make_float2(0.f, 0.f);
     const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
     uint32_t va[32], vb[32];
@@ -170,7 +175,7 @@ __device__ __forceinline__ float exp_pass(uint32_t taddr, int lim2, int lo2, flo
             rs = fadd2(rs, e);
             pk[i] = pack_bf16(e.x, e.y);
         }
-        tmem_st16_async(taddr + q4 * 16, pk);
+        tmem_st16_async(paddr + q4 * 16, pk);
         if (q4 + 1 < 4) tmem_wait_ld(nx);
     }
     tmem_wait_st();
@@ -203,6 +208,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const uint32_t BAR_TD = BAR_O + 16;                // teardown
     const uint32_t BAR_MR = BAR_TD + 8;                // split-KV: warpgroup 1's (m, l) staged
     const uint32_t BAR_MD = BAR_MR + 8;                // split-KV: warpgroup 0 done with O_1 and (m, l)
+    const uint32_t BAR_PV = BAR_MD + 8;                // pv_done[t]: P_t V_j done (P in its own columns)
+    constexpr bool P_OWN = C::P_OWN && !SPLIT;
     uint32_t* tmem_slot = (uint32_t*)(smem + C::OFF_MISC);
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
@@ -225,6 +232,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         mbar_init(BAR_TD, 1);
         mbar_init(BAR_MR, 128);
         mbar_init(BAR_MD, 128);
+        mbar_init(BAR_PV, 1);
+        mbar_init(BAR_PV + 8, 1);
         fence_mbar_init();
         if ((s_base & 1023u) != 0) record_error(ctl, kErrTimeout, kSiteAlign, (int)(s_base & 1023u));
     }
@@ -397,6 +406,40 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     next();
                     const uint32_t sV = s_base + C::OFF_KV + vslot * C::KV_BYTES;
                     const bool more = j + 1 < n;
+                    if constexpr (P_OWN) {
+                        // P_t has its own columns: S_t of the next block first, then P_t V_j; the
+                        // softmax learns from pv_done[t] when P_t and O_t may be written again
+                        if (!mbar_wait(BAR_P, p_iter & 1, ctl, kSitePFull)) { ok = false; break; }
+                        tc_fence_after();
+                        if (more) {
+                            kslot = slot;
+                            if (!mbar_wait(bar_kvf(kslot), phase, ctl, kSiteKvFull)) { ok = false; break; }
+                            tc_fence_after();
+                            next();
+                            sK = s_base + C::OFF_KV + kslot * C::KV_BYTES;
+                            issue_s(C::COL_S0, sQ0, sK);
+                            mma_commit(BAR_S);
+                        }
+                        issue_o(C::COL_O0, C::COL_P0, sV, j > 0);
+                        mma_commit(more ? BAR_PV : BAR_O);
+                        if (!mbar_wait(BAR_P + 8, p_iter & 1, ctl, kSitePFull)) { ok = false; break; }
+                        tc_fence_after();
+                        ++p_iter;
+                        if (more) {
+                            issue_s(C::COL_S1, sQ1, sK);
+                            mma_commit(BAR_S + 8);
+                            mma_commit(bar_kve(kslot));
+                        }
+                        issue_o(C::COL_O1, C::COL_P1, sV, j > 0);
+                        mma_commit(bar_kve(vslot));
+                        if (more) {
+                            mma_commit(BAR_PV + 8);
+                        } else {
+                            mma_commit(BAR_O + 8);
+                            mma_commit(BAR_QE);
+                        }
+                        continue;
+                    }
                     if (!mbar_wait(BAR_P, p_iter & 1, ctl, kSitePFull)) { ok = false; break; }
                     tc_fence_after();
                     issue_o(C::COL_O0, C::COL_S0, sV, j > 0);
@@ -439,8 +482,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const uint32_t col_s = t ? C::COL_S1 : C::COL_S0;
         const uint32_t col_o = t ? C::COL_O1 : C::COL_O0;
         const uint32_t bar_s = BAR_S + 8 * t, bar_p = BAR_P + 8 * t, bar_o = BAR_O + 8 * t;
+        const uint32_t col_p = P_OWN ? (t ? C::COL_P1 : C::COL_P0) : col_s;
         const float c = p.scale_log2;
-        uint32_t s_iter = 0, o_iter = 0;
+        uint32_t s_iter = 0, o_iter = 0, pv_iter = 0;
         uint32_t o1_iter = 0, merge_iter = 0;  // split-KV: warpgroup 1's O handoffs, merges
         bool md_pending = false;               // split-KV (warpgroup 1): merge of the last tile not yet confirmed
         float2* stage = (float2*)(smem + C::OFF_Q + C::Q_BYTES);  // split-KV: warpgroup 1's (m, l) per row
@@ -483,6 +527,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 const float mraw = masked ? row_max_pass<true>(lane_addr + col_s, lim2, lo2)
                                           : row_max_pass<false>(lane_addr + col_s, lim2, lo2);
                 const float m_new = fmaxf(m_use, mraw * c);
+                if (P_OWN && j > j0) {  // P_t V_{j-1} must be done before O_t is rescaled or P_t rewritten
+                    if (!mbar_wait(BAR_PV + 8 * t, pv_iter & 1, ctl, kSitePFull)) { ok = false; break; }
+                    ++pv_iter;
+                    tc_fence_after();
+                }
                 if (j == j0) {
                     m_use = m_new;
                 } else if (__any_sync(0xffffffffu, m_new > m_use + 8.f)) {
@@ -501,8 +550,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 }
                 const float msub = (m_use == -INFINITY) ? 0.f : m_use;
                 // pass 2: p = 2^(s*c - m), row sum, bf16 P over the S columns already read
-                const float rsum = masked ? exp_pass<true>(lane_addr + col_s, lim2, lo2, c, msub)
-                                          : exp_pass<false>(lane_addr + col_s, lim2, lo2, c, msub);
+                const float rsum = masked ? exp_pass<true>(lane_addr + col_s, lane_addr + col_p, lim2, lo2, c, msub)
+                                          : exp_pass<false>(lane_addr + col_s, lane_addr + col_p, lim2, lo2, c, msub);
                 l += rsum;
                 tc_fence_before();
                 if (SPLIT && md_pending) {  // O_1 is free only once the last tile's merge has read it
