@@ -137,3 +137,40 @@ def test_backward_full_size_sweep(cuda_lib, N):
         check_grad(f64(dv[0, h]), rv, "dV N%d h%d" % (N, h))
     for g in (dq, dk, dv):
         assert torch.isfinite(g.float()).all()
+
+
+def test_forward_backward_in_cuda_graph(cuda_lib):
+    """fa_fwd and fa_bwd (with its programmatic dependent launches) captured in a
+    CUDA graph and replayed give the eager results bit for bit."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    B, H, N, d = 1, 8, 1024, 128
+    q, k, v, dO = (t.to(dev) for t in _inputs(77, B, H, N, N, d))
+    o, lse = torch.empty_like(q), torch.empty(B, H, N, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, N, d), dtype=torch.uint8, device=dev)
+
+    def step():
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, N, d, d ** -0.5, True)
+        fa.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, d ** -0.5, True, ws, ws.numel())
+
+    step()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (o, lse, dq, dk, dv)]
+    for t in (o, lse, dq, dk, dv):
+        t.fill_(float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up on the side stream before capture
+    torch.cuda.current_stream().wait_stream(s)
+    for t in (o, lse, dq, dk, dv):
+        t.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    g.replay()
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error()[0] == 0
+    for a, b in zip(ref, (o, lse, dq, dk, dv)):
+        assert torch.equal(a, b)
