@@ -480,31 +480,46 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 }
 
 // V [BH, Nk, 128] e4m3 -> V^T [BH, 128, Nk_pad] (keys past Nk are zero).
-// One CTA per (head, 128-key block): a 128 x 128 byte tile through shared memory.
+// One CTA per (head, 128-key block): a 128 x 128 byte tile through shared
+// memory as 32-bit words.  Each thread then transposes 4 x 4 byte blocks with
+// byte permutes: 16 keys of 4 features, written as four 16-byte pieces of V^T
+// rows; the 8 threads sharing a feature word cover 128 contiguous keys.
 __global__ void __launch_bounds__(256) vt_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt, int Nk,
                                                  int Nk_pad) {
-    __shared__ uint8_t tile[128][128 + 4];
+    // [key][feature word]: word w of key k sits in column (w + 4 (k / 16)) mod 32 of a 33-word row, which keeps
+    // both the row-wise fill and the column-wise read free of bank conflicts.
+    __shared__ uint32_t tw[128][33];
     const int bh = blockIdx.x, kb = blockIdx.y, tid = threadIdx.x;
     const uint8_t* src = v + (size_t)bh * Nk * 128;
     for (int i = tid; i < 128 * 8; i += 256) {  // 128 keys x 8 granules of 16 bytes
-        const int key = i >> 3, g = i & 7;
+        const int key = i >> 3, g = i & 7, rot = 4 * (key >> 4);
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
         if (kb * 128 + key < Nk) x = __ldg(reinterpret_cast<const uint4*>(src + (size_t)(kb * 128 + key) * 128) + g);
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int b = 0; b < 16; ++b) tile[key][g * 16 + b] = (uint8_t)(w[b >> 2] >> (8 * (b & 3)));
+        tw[key][(4 * g + rot) & 31] = x.x;
+        tw[key][(4 * g + 1 + rot) & 31] = x.y;
+        tw[key][(4 * g + 2 + rot) & 31] = x.z;
+        tw[key][(4 * g + 3 + rot) & 31] = x.w;
     }
     __syncthreads();
-    uint8_t* dst = vt + (size_t)bh * 128 * Nk_pad;
-    for (int i = tid; i < 128 * 8; i += 256) {  // 128 feature rows x 8 granules of 16 keys
-        const int f = i >> 3, g = i & 7;
-        const int key0 = kb * 128 + g * 16;
-        if (key0 >= Nk_pad) continue;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
+    const int kg = tid & 7, fw = tid >> 3;  // keys 16 kg .. 16 kg + 15 of the tile, features 4 fw .. 4 fw + 3
+    const int key0 = kb * 128 + kg * 16, col = (fw + 4 * kg) & 31;
+    if (key0 >= Nk_pad) return;
+    uint32_t out[4][4];  // [feature][4 keys]
 #pragma unroll
-        for (int b = 0; b < 16; ++b) w[b >> 2] |= (uint32_t)tile[g * 16 + b][f] << (8 * (b & 3));
-        *reinterpret_cast<uint4*>(dst + (size_t)f * Nk_pad + key0) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int q = 0; q < 4; ++q) {
+        const int k = kg * 16 + 4 * q;
+        const uint32_t a = tw[k][col], b = tw[k + 1][col], c = tw[k + 2][col], d = tw[k + 3][col];
+        const uint32_t ab_lo = __byte_perm(a, b, 0x5140), ab_hi = __byte_perm(a, b, 0x7362);  // a0 b0 a1 b1 / a2 b2 a3 b3
+        const uint32_t cd_lo = __byte_perm(c, d, 0x5140), cd_hi = __byte_perm(c, d, 0x7362);
+        out[0][q] = __byte_perm(ab_lo, cd_lo, 0x5410);  // a0 b0 c0 d0
+        out[1][q] = __byte_perm(ab_lo, cd_lo, 0x7632);  // a1 b1 c1 d1
+        out[2][q] = __byte_perm(ab_hi, cd_hi, 0x5410);
+        out[3][q] = __byte_perm(ab_hi, cd_hi, 0x7632);
     }
+    uint8_t* dst = vt + (size_t)bh * 128 * Nk_pad + key0;
+#pragma unroll
+    for (int f = 0; f < 4; ++f)
+        *reinterpret_cast<uint4*>(dst + (size_t)(4 * fw + f) * Nk_pad) = make_uint4(out[f][0], out[f][1], out[f][2], out[f][3]);
 }
 
 }  // namespace
