@@ -200,6 +200,7 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, __nv_bfloat16* dst
                                               bool zero, int c0) {
     taddr += c0;
     dst += c0;
+    const bool wide = ((uintptr_t)dst & 31) == 0;  // the same for every row: rows are 32-byte multiples
 #pragma unroll 1
     for (int q4 = 0; q4 < D / 64; ++q4) {
         uint32_t v[32];
@@ -213,11 +214,7 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, __nv_bfloat16* dst
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-        if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        if (valid) store_row64(dst + q4 * 32, pk, wide);
     }
 }
 

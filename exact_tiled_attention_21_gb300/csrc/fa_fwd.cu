@@ -43,10 +43,12 @@ struct Fwd {
     static constexpr int OFF_KV = 2 * Q_BYTES;
     static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_BYTES;
     // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2], o_final[2], teardown,
-    // merge_ready, merge_done (split-KV), pv_done[2] (P in its own columns)
-    static constexpr int NBAR = 2 + 2 * NSLOT + 11;
+    // merge_ready, merge_done (split-KV), pv_done[2] (P in its own columns), q_full/q_empty of the
+    // second query buffer (split-KV tiles double-buffer their one query tile)
+    static constexpr int NBAR = 2 + 2 * NSLOT + 13;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + alignment slack
+    static constexpr int OFF_STAGE = OFF_MISC + 16;  // split-KV: warpgroup 1's (m, l) per row
+    static constexpr int SMEM = OFF_STAGE + BM * 8 + 1024;  // + alignment slack
     static constexpr int THREADS = 320;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
@@ -209,6 +211,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const uint32_t BAR_MR = BAR_TD + 8;                // split-KV: warpgroup 1's (m, l) staged
     const uint32_t BAR_MD = BAR_MR + 8;                // split-KV: warpgroup 0 done with O_1 and (m, l)
     const uint32_t BAR_PV = BAR_MD + 8;                // pv_done[t]: P_t V_j done (P in its own columns)
+    const uint32_t BAR_QF1 = BAR_PV + 16, BAR_QE1 = BAR_PV + 24;  // split-KV: second query buffer
     constexpr bool P_OWN = C::P_OWN && !SPLIT;
     uint32_t* tmem_slot = (uint32_t*)(smem + C::OFF_MISC);
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
@@ -234,6 +237,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         mbar_init(BAR_MD, 128);
         mbar_init(BAR_PV, 1);
         mbar_init(BAR_PV + 8, 1);
+        mbar_init(BAR_QF1, 1);
+        mbar_init(BAR_QE1, 1);
         fence_mbar_init();
         if ((s_base & 1023u) != 0) record_error(ctl, kErrTimeout, kSiteAlign, (int)(s_base & 1023u));
     }
@@ -269,12 +274,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 const int jlo = fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk);
                 const int n = max(0, fwd_num_kv(p, row0, sl.nq, sl.nk) - jlo);
                 if (n == 0) continue;
-                if (q_iter > 0 && !mbar_wait(BAR_QE, (q_iter - 1) & 1, ctl, kSiteQEmpty)) break;
-                mbar_arrive_expect_tx(BAR_QF, (SPLIT ? 1 : 2) * C::Q_BYTES);
+                // split-KV tiles alternate between the two query buffers, so the next tile's Q
+                // loads while this one runs; a 256-row tile takes both
+                const int qb = SPLIT ? (int)(q_iter & 1) : 0;
+                const uint32_t qn = SPLIT ? (q_iter >> 1) : q_iter;  // earlier fills of buffer qb
+                const uint32_t qf = qb ? BAR_QF1 : BAR_QF, qe = qb ? BAR_QE1 : BAR_QE;
+                if (qn > 0 && !mbar_wait(qe, (qn - 1) & 1, ctl, kSiteQEmpty)) break;
+                mbar_arrive_expect_tx(qf, (SPLIT ? 1 : 2) * C::Q_BYTES);
                 for (int t = 0; t < (SPLIT ? 1 : 2); ++t)
                     for (int c = 0; c < C::KCH; ++c)
-                        tma_load_3d(s_base + C::OFF_Q + t * C::Q_BYTES + c * C::CHUNK_BYTES, &map_q,
-                                    BAR_QF, c * 64, row0 + t * 128, bh, pol_q);
+                        tma_load_3d(s_base + C::OFF_Q + (t + qb) * C::Q_BYTES + c * C::CHUNK_BYTES, &map_q,
+                                    qf, c * 64, row0 + t * 128, bh, pol_q);
                 ++q_iter;
                 for (int j = 0; j < n && ok; ++j) {
                     for (int kv = 0; kv < 2; ++kv) {
@@ -297,7 +307,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 }
             }
             if (*abort_flag) {  // let every load in flight land before the CTA exits
-                if (q_iter > 0) mbar_drain(BAR_QF, (q_iter - 1) & 1, ctl, kSiteTeardown);
+                if (SPLIT) {
+                    const uint32_t f0 = (q_iter + 1) >> 1, f1 = q_iter >> 1;  // fills of buffers 0 and 1
+                    if (f0 > 0) mbar_drain(BAR_QF, (f0 - 1) & 1, ctl, kSiteTeardown);
+                    if (f1 > 0) mbar_drain(BAR_QF1, (f1 - 1) & 1, ctl, kSiteTeardown);
+                } else if (q_iter > 0) {
+                    mbar_drain(BAR_QF, (q_iter - 1) & 1, ctl, kSiteTeardown);
+                }
                 for (int s = 0; s < C::NSLOT; ++s)
                     if (issued & (1u << s))
                         mbar_drain(bar_kvf(s), (issued_par >> s) & 1, ctl, kSiteTeardown);
@@ -344,7 +360,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 fwd_decode(p, w, bh, row0);
                 const int n = max(0, fwd_num_kv(p, row0, sl.nq, sl.nk) - fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk));
                 if (n == 0) continue;
-                if (!mbar_wait(BAR_QF, q_iter & 1, ctl, kSiteQFull)) break;
+                const int qb = SPLIT ? (int)(q_iter & 1) : 0;
+                const uint32_t qn = SPLIT ? (q_iter >> 1) : q_iter;
+                if (!mbar_wait(qb ? BAR_QF1 : BAR_QF, qn & 1, ctl, kSiteQFull)) break;
                 ++q_iter;
                 if constexpr (SPLIT) {
                     // Ring fill f holds K_{f/2} (f even) or V_{f/2} (f odd) of this tile; block j goes
@@ -356,11 +374,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                         return mbar_wait(bar_kvf(fslot(f)), (f / C::NSLOT) & 1, ctl, kSiteKvFull);
                     };
                     auto faddr = [&](uint32_t f) { return s_base + C::OFF_KV + fslot(f) * C::KV_BYTES; };
+                    const uint32_t sQ = qb ? sQ1 : sQ0;
                     for (int t = 0; t < 2 && t < n; ++t) {
                         const uint32_t f = F + 2 * t;
                         if (!fwait(f)) { ok = false; break; }
                         tc_fence_after();
-                        issue_s(t ? C::COL_S1 : C::COL_S0, sQ0, faddr(f));
+                        issue_s(t ? C::COL_S1 : C::COL_S0, sQ, faddr(f));
                         mma_commit(BAR_S + 8 * t);
                         mma_commit(bar_kve(fslot(f)));
                     }
@@ -378,7 +397,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                             const uint32_t fk = F + 2 * j + 4;
                             if (!fwait(fk)) { ok = false; break; }
                             tc_fence_after();
-                            issue_s(t ? C::COL_S1 : C::COL_S0, sQ0, faddr(fk));
+                            issue_s(t ? C::COL_S1 : C::COL_S0, sQ, faddr(fk));
                             mma_commit(BAR_S + 8 * t);
                             mma_commit(bar_kve(fslot(fk)));
                         } else {
@@ -386,7 +405,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                         }
                     }
                     if (!ok) break;
-                    mma_commit(BAR_QE);
+                    mma_commit(qb ? BAR_QE1 : BAR_QE);
                     fill = F + 2 * n;
                     continue;
                 }
@@ -487,7 +506,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         uint32_t s_iter = 0, o_iter = 0, pv_iter = 0;
         uint32_t o1_iter = 0, merge_iter = 0;  // split-KV: warpgroup 1's O handoffs, merges
         bool md_pending = false;               // split-KV (warpgroup 1): merge of the last tile not yet confirmed
-        float2* stage = (float2*)(smem + C::OFF_Q + C::Q_BYTES);  // split-KV: warpgroup 1's (m, l) per row
+        float2* stage = (float2*)(smem + C::OFF_STAGE);  // split-KV: warpgroup 1's (m, l) per row
         SeqLen sl_next = fwd_seqlen<VL>(p, persistent_work(0, blockIdx.x, gridDim.x));
         for (int rd = 0; rd * (int)gridDim.x < p.num_work; ++rd) {
             const int w = persistent_work(rd, blockIdx.x, gridDim.x);
@@ -600,6 +619,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
             const float w0 = a0 * inv, w1 = a1 * inv;
             __nv_bfloat16* orow = p.o + ((size_t)bh * p.Nq + (valid ? row : 0)) * D;
+            const bool o_wide = ((uintptr_t)p.o & 31) == 0;  // rows are 32-byte multiples
 #pragma unroll 1
             for (int q4 = 0; q4 < D / 32; ++q4) {
                 uint32_t v[32];
@@ -624,12 +644,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     for (int i = 0; i < 16; ++i)
                         pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * w0, __uint_as_float(v[2 * i + 1]) * w0);
                 }
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
+                if (valid) store_row64(orow + q4 * 32, pk, o_wide);
             }
             if (valid)
                 p.lse[(size_t)bh * p.Nq + row] =

@@ -444,6 +444,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             const bool valid = row < p.Nq;
             const float inv = (l > 0.f) ? __ldg(p.v_scale + bh) / l : 0.f;
             __nv_bfloat16* orow = p.o + ((size_t)bh * p.Nq + (valid ? row : 0)) * D;
+            const bool o_wide = ((uintptr_t)p.o & 31) == 0;  // rows are 32-byte multiples
 #pragma unroll 1
             for (int q4 = 0; q4 < D / 32; ++q4) {
                 uint32_t v[32];
@@ -457,12 +458,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
+                if (valid) store_row64(orow + q4 * 32, pk, o_wide);
             }
             if (valid)
                 p.lse[(size_t)bh * p.Nq + row] = (l > 0.f) ? (m_use + lg2(l)) * 0.69314718055994531f : -INFINITY;

@@ -364,6 +364,25 @@ __device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t (
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Stores 64 bytes (16 words) at dst: as two 32-byte stores when dst is 32-byte
+// aligned (`wide`), else as four 16-byte stores.  A thread writes a piece of its
+// own row, so a warp's store touches 32 rows at once; the wider store halves the
+// number of store instructions and of the cache lines they touch per byte.
+__device__ __forceinline__ void store_row64(void* dst, const uint32_t (&w)[16], bool wide) {
+    if (wide) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"((char*)dst + 32 * h),
+                         "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]),
+                         "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                         : "memory");
+    } else {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+}
+
 // registers -> TMEM, 32 lanes x 16 columns, completed before return.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(

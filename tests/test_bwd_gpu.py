@@ -113,6 +113,30 @@ def test_backward_matches_step_entry_points(cuda_lib, B, H, N):
     assert torch.equal(dk_seen, dk2) and torch.equal(dv_seen, dv2)
 
 
+@pytest.mark.parametrize("N,d", [(700, 128), (300, 64)])
+def test_backward_gradients_16_byte_aligned(cuda_lib, N, d):
+    """dQ, dK, dV written 16 bytes past a 32-byte boundary take the 16-byte
+    store path: the same bits as aligned outputs."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    B, H = 1, 2
+    q, k, v, dO = (t.to(dev) for t in _inputs(53, B, H, N, N, d))
+    o, lse = fa.forward(q, k, v, causal=True)
+    ref = fa.backward(q, k, v, o, lse, dO, causal=True)
+    outs = []
+    for _ in range(3):
+        buf = torch.empty(B * H * N * d + 16, dtype=torch.bfloat16, device=dev)
+        start = ((16 - buf.data_ptr() % 32) % 32) // 2
+        t = buf[start:start + B * H * N * d].view(B, H, N, d)
+        assert t.data_ptr() % 32 == 16
+        outs.append(t)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, N, d), dtype=torch.uint8, device=dev)
+    fa.fa_bwd(q, k, v, o, lse, dO, *outs, B, H, N, N, d, d ** -0.5, True, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error()[0] == 0
+    assert all(torch.equal(a, b) for a, b in zip(outs, ref))
+
+
 def test_backward_deterministic(cuda_lib):
     """No atomics anywhere: two runs give identical bits."""
     q, k, v, dO = _inputs(9, 1, 4, 640, 640, 128)

@@ -97,3 +97,23 @@ def test_fp8_rejects_d64(cuda_lib):
                       torch.ones(1, device=dev), torch.empty(1, 1, 8, 64, dtype=torch.bfloat16, device=dev),
                       torch.empty(1, 1, 8, device=dev), 1, 1, 8, 8, 64, 0.125, 0,
                       torch.empty(4096, dtype=torch.uint8, device=dev), 4096)
+
+
+def test_fp8_output_16_byte_aligned(cuda_lib):
+    """O written 16 bytes past a 32-byte boundary takes the 16-byte store path:
+    the same bits as an aligned O."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    B, H, N = 1, 2, 700
+    q8, k8, v8, sq, sk, sv = (t.to(dev) for t in _inputs(2333, B, H, N, N))
+    o_ref, lse_ref = fa.forward_fp8(q8, k8, v8, sq, sk, sv, causal=True)
+    buf = torch.empty(B * H * N * 128 + 16, dtype=torch.bfloat16, device=dev)
+    start = ((16 - buf.data_ptr() % 32) % 32) // 2
+    o = buf[start:start + B * H * N * 128].view(B, H, N, 128)
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty(B, H, N, device=dev)
+    ws = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, 128), dtype=torch.uint8, device=dev)
+    fa.fa_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, B, H, N, N, 128, 1 / math.sqrt(128), True, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error()[0] == 0
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)

@@ -107,6 +107,35 @@ def test_forward_tile_modes_agree(cuda_lib):
         assert (l_wide[:, :2] - l_split).abs().max() <= 1e-4
 
 
+def _offset16(shape, dtype, dev):
+    """A contiguous tensor whose data starts 16 bytes past a 32-byte boundary
+    (the C ABI asks for 16-byte alignment only)."""
+    elems = 16 // torch.empty(0, dtype=dtype).element_size()
+    n = int(np.prod(shape))
+    buf = torch.empty(n + 2 * elems, dtype=dtype, device=dev)
+    base = buf.data_ptr() % 32
+    start = ((16 - base) % 32) // buf.element_size()
+    t = buf[start:start + n].view(*shape)
+    assert t.data_ptr() % 32 == 16
+    return t
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [(1, 2, 300, 128, True), (1, 2, 700, 64, False), (1, 320, 768, 64, True)])
+def test_forward_output_16_byte_aligned(cuda_lib, B, H, N, d, causal):
+    """O written at an address that is 16- but not 32-byte aligned takes the
+    16-byte store path: the same bits as an aligned O, in both tile modes."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    q, k, v = (t.to(dev) for t in _inputs(47, B, H, N, N, d))
+    o_ref, lse_ref = fa.forward(q, k, v, causal=causal)
+    o = _offset16((B, H, N, d), torch.bfloat16, dev)
+    lse = torch.empty(B, H, N, device=dev)
+    fa.fa_fwd(q, k, v, o, lse, B, H, N, N, d, d ** -0.5, causal)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error()[0] == 0
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+
+
 def test_forward_scale_argument(cuda_lib):
     """A non-default scale reaches the kernel (LSE shifts with it).  Off the
     workloads' scale the max-abs bound is the one derived from the two bf16
