@@ -119,6 +119,9 @@ bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restr
     constexpr int LPR = D / 8, RPW = 32 / LPR, STEPS = 4;
     // the dK/dV pass launched after this grid may set up (and load K, V) meanwhile
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // launched as a programmatic dependent of the kernel before it: O and dO may come from that
+    // kernel, and D may still be read by it (the dQ pass of an earlier backward)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row0 = (long long)blockIdx.x * kPreRowsPerBlock<D> + (long long)warp * RPW * STEPS + lane / LPR;
     const int part = lane % LPR;
@@ -780,9 +783,18 @@ BwdParams make_params(const BwdLaunch& a) {
 template <int D>
 cudaError_t launch_pre_d(const BwdLaunch& a, cudaStream_t s) {
     const long long rows = (long long)a.B * a.H * a.Nq;
-    bwd_pre_kernel<D><<<(unsigned)((rows + kPreRowsPerBlock<D> - 1) / kPreRowsPerBlock<D>), 256, 0, s>>>(
-        (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, a.delta, rows);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + kPreRowsPerBlock<D> - 1) / kPreRowsPerBlock<D>));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol in the kernel
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_pre_kernel<D>, (const __nv_bfloat16*)a.o,
+                                             (const __nv_bfloat16*)a.dO, a.delta, rows);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // after_pre: launched right after the preprocess on the same stream, as its

@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(kDecThreads)
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
                     const __nv_bfloat16* __restrict__ vc, float* __restrict__ part_o,
                     float* __restrict__ part_lse, int Nk, int splits, int chunk, float scale_log2) {
+    pdl_launch_dependents();
+    pdl_wait();  // the cache and q may come from the kernel before; it may still read part_o
     constexpr int LPK = D / 8;              // lanes per key row
     constexpr int KPW = 32 / LPK;           // keys per warp per load
     constexpr int KPC = KPW * (kDecThreads / 32);  // keys per CTA per load step
@@ -157,6 +159,8 @@ template <int D>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int BH, int splits) {
+    pdl_launch_dependents();
+    pdl_wait();  // the partials of the split pass
     constexpr int PER = D / 32;  // output columns per lane
     const int bh = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -200,14 +204,13 @@ cudaError_t launch_decode_d(const DecodeLaunch& a, cudaStream_t s) {
     const int BH = a.B * a.H;
     const long long ctas = (long long)BH * a.splits;
     if (ctas > 0x7FFFFFFFll) return cudaErrorInvalidValue;
-    decode_split_kernel<D><<<(unsigned)ctas, kDecThreads, 0, s>>>(
-        (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kc, (const __nv_bfloat16*)a.vc, a.part_o,
-        a.part_lse, a.Nk, a.splits, a.chunk, a.scale * 1.4426950408889634f);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(decode_split_kernel<D>, dim3((unsigned)ctas), dim3(kDecThreads), 0, s,
+                                     (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kc,
+                                     (const __nv_bfloat16*)a.vc, a.part_o, a.part_lse, a.Nk, a.splits, a.chunk,
+                                     a.scale * 1.4426950408889634f);
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<D><<<(BH + 3) / 4, 128, 0, s>>>(a.part_o, a.part_lse, (__nv_bfloat16*)a.o,
-                                                          a.lse, BH, a.splits);
-    return cudaGetLastError();
+    return launch_dependent(decode_combine_kernel<D>, dim3((BH + 3) / 4), dim3(128), 0, s, (const float*)a.part_o,
+                            (const float*)a.part_lse, (__nv_bfloat16*)a.o, a.lse, BH, a.splits);
 }
 
 
@@ -230,6 +233,8 @@ decode_paged_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
                           const int* __restrict__ lens, float* __restrict__ part_o,
                           float* __restrict__ part_lse, int Hq, int Hkv, int page, int max_pages,
                           int num_pages, int splits, int groups, float scale_log2, DevError* err) {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int LPK = D / 8, KPW = 32 / LPK, KPC = KPW * (kDecThreads / 32), STEPS = kDecPiece / KPC;
     __shared__ float s_p[G][kDecPiece];
     __shared__ float s_red[kDecThreads / 32][G];
@@ -422,16 +427,15 @@ cudaError_t launch_paged_dg(const PagedDecodeLaunch& a, cudaStream_t s) {
     const int groups = (a.Hq / a.Hkv) / G;
     const long long ctas = (long long)a.B * a.Hkv * a.splits * groups;
     if (ctas > 0x7FFFFFFFll) return cudaErrorInvalidValue;
-    decode_paged_split_kernel<D, G><<<(unsigned)ctas, kDecThreads, 0, s>>>(
-        (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kp, (const __nv_bfloat16*)a.vp, a.table, a.lens,
-        a.part_o, a.part_lse, a.Hq, a.Hkv, a.page, a.max_pages, a.num_pages, a.splits, groups,
-        a.scale * 1.4426950408889634f, a.err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(decode_paged_split_kernel<D, G>, dim3((unsigned)ctas), dim3(kDecThreads), 0, s,
+                                     (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kp,
+                                     (const __nv_bfloat16*)a.vp, a.table, a.lens, a.part_o, a.part_lse, a.Hq,
+                                     a.Hkv, a.page, a.max_pages, a.num_pages, a.splits, groups,
+                                     a.scale * 1.4426950408889634f, a.err);
     if (e != cudaSuccess) return e;
     const int BH = a.B * a.Hq;
-    decode_combine_kernel<D><<<(BH + 3) / 4, 128, 0, s>>>(a.part_o, a.part_lse, (__nv_bfloat16*)a.o, a.lse, BH,
-                                                          a.splits);
-    return cudaGetLastError();
+    return launch_dependent(decode_combine_kernel<D>, dim3((BH + 3) / 4), dim3(128), 0, s, (const float*)a.part_o,
+                            (const float*)a.part_lse, (__nv_bfloat16*)a.o, a.lse, BH, a.splits);
 }
 
 template <int D>
@@ -456,10 +460,10 @@ cudaError_t launch_decode_paged(const PagedDecodeLaunch& a, cudaStream_t s) {
 cudaError_t launch_decode_combine(const float* part_o, const float* part_lse, void* o, float* lse, int BH,
                                   int splits, int d, cudaStream_t s) {
     if (d == 128)
-        decode_combine_kernel<128><<<(BH + 3) / 4, 128, 0, s>>>(part_o, part_lse, (__nv_bfloat16*)o, lse, BH, splits);
-    else
-        decode_combine_kernel<64><<<(BH + 3) / 4, 128, 0, s>>>(part_o, part_lse, (__nv_bfloat16*)o, lse, BH, splits);
-    return cudaGetLastError();
+        return launch_dependent(decode_combine_kernel<128>, dim3((BH + 3) / 4), dim3(128), 0, s, part_o, part_lse,
+                                (__nv_bfloat16*)o, lse, BH, splits);
+    return launch_dependent(decode_combine_kernel<64>, dim3((BH + 3) / 4), dim3(128), 0, s, part_o, part_lse,
+                            (__nv_bfloat16*)o, lse, BH, splits);
 }
 
 }  // namespace fa

@@ -197,6 +197,8 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
         tmem_alloc(smem_u32(tmem_slot), Dm::TMEM_COLS);
         tmem_relinquish();
     }
+    pdl_launch_dependents();
+    pdl_wait();  // the setup above may overlap the kernel before; its writes are visible from here
     // sequence lengths, clamped to the table (every role reads them per item)
     int* s_lens = reinterpret_cast<int*>(smem + Dm::OFF_LENS);
     for (int b = tid; b < p.B; b += Dm::THREADS) {
@@ -570,8 +572,8 @@ cudaError_t launch_nh(const PagedDecodeLaunch& a, MmaParams p, cudaStream_t s) {
     cudaError_t e = set_smem_limit_once<decode_paged_mma_kernel<NH>>(Dm::SMEM);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<long long>(nitems, a.num_sms);
-    decode_paged_mma_kernel<NH><<<grid, Dm::THREADS, Dm::SMEM, s>>>(a.map_q, a.map_k, a.map_v, p);
-    return cudaGetLastError();
+    return launch_dependent(decode_paged_mma_kernel<NH>, dim3(grid), dim3(Dm::THREADS), Dm::SMEM, s, a.map_q, a.map_k,
+                            a.map_v, p);
 }
 
 }  // namespace

@@ -250,6 +250,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent of the kernel before it on the stream, this grid may
+    // start while that one finishes: the setup above overlaps its end, and every thread waits for
+    // it to complete (griddepcontrol.wait) before touching global memory.  A kernel launched after
+    // this one the same way may likewise start its setup on SMs this grid leaves.
+    pdl_launch_dependents();
 
     if (warp == 8) {
         // ------------------------------------------------------------ TMA producer
@@ -257,6 +262,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             tma_prefetch_desc(&map_q);
             tma_prefetch_desc(&map_k);
             tma_prefetch_desc(&map_v);
+            if (VL) pdl_wait();  // the sequence lengths
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
             int slot = 0;
@@ -274,6 +280,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 const int jlo = fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk);
                 const int n = max(0, fwd_num_kv(p, row0, sl.nq, sl.nk) - jlo);
                 if (n == 0) continue;
+                if (!VL && q_iter == 0) pdl_wait();
                 // split-KV tiles alternate between the two query buffers, so the next tile's Q
                 // loads while this one runs; a 256-row tile takes both
                 const int qb = SPLIT ? (int)(q_iter & 1) : 0;
@@ -321,6 +328,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
+        pdl_wait();  // (only its error reports touch global memory)
         if (lane == 0 && !*abort_flag) {
             int slot = 0;
             uint32_t phase = 0, q_iter = 0, p_iter = 0;
@@ -495,6 +503,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
+        pdl_wait();
         const int t = warp >> 2;                   // query tile of this warpgroup
         const int r = ((warp & 3) << 5) + lane;    // row within the tile = TMEM lane
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -688,8 +697,8 @@ cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
     p.err = a.err;
     p.timeout_ns = a.timeout_ns;
     const int grid = p.num_work < a.num_sms ? p.num_work : a.num_sms;
-    fwd_kernel<D, WIN, VL, SPLIT><<<grid, C::THREADS, C::SMEM, s>>>(a.map_q, a.map_k, a.map_v, p);
-    return cudaGetLastError();
+    return launch_dependent(fwd_kernel<D, WIN, VL, SPLIT>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, s, a.map_q,
+                            a.map_k, a.map_v, p);
 }
 
 // Tile mode for the plain forward.  The grid is persistent with a static

@@ -224,6 +224,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+    pdl_wait();  // the setup above overlaps the V transpose; its V^T is visible from here
 
     if (warp == 8) {
         // ------------------------------------------------------------ TMA producer
@@ -486,6 +488,8 @@ __global__ void __launch_bounds__(256) vt_kernel(const uint8_t* __restrict__ v, 
     // both the row-wise fill and the column-wise read free of bank conflicts.
     __shared__ uint32_t tw[128][33];
     const int bh = blockIdx.x, kb = blockIdx.y, tid = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait();  // V may come from the kernel before, which may still read the workspace
     const uint8_t* src = v + (size_t)bh * Nk * 128;
     for (int i = tid; i < 128 * 8; i += 256) {  // 128 keys x 8 granules of 16 bytes
         const int key = i >> 3, g = i & 7, rot = 4 * (key >> 4);
@@ -524,8 +528,8 @@ cudaError_t launch_fwd_fp8(const Fp8FwdLaunch& a, cudaStream_t s) {
     const int BH = a.B * a.H;
     if ((a.Nk_pad + 127) / 128 > 65535) return cudaErrorInvalidValue;
     dim3 tg(BH, (a.Nk_pad + 127) / 128);
-    vt_kernel<<<tg, 256, 0, s>>>((const uint8_t*)a.v, (uint8_t*)a.vt, a.Nk, a.Nk_pad);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(vt_kernel, tg, dim3(256), 0, s, (const uint8_t*)a.v, (uint8_t*)a.vt, a.Nk,
+                                     a.Nk_pad);
     if (e != cudaSuccess) return e;
     e = set_smem_limit_once<fwd_fp8_kernel>(F8::SMEM);
     if (e != cudaSuccess) return e;
@@ -547,8 +551,7 @@ cudaError_t launch_fwd_fp8(const Fp8FwdLaunch& a, cudaStream_t s) {
     p.err = a.err;
     p.timeout_ns = a.timeout_ns;
     const int grid = p.num_work < a.num_sms ? p.num_work : a.num_sms;
-    fwd_fp8_kernel<<<grid, F8::THREADS, F8::SMEM, s>>>(a.map_q, a.map_k, a.map_vt, p);
-    return cudaGetLastError();
+    return launch_dependent(fwd_fp8_kernel, dim3(grid), dim3(F8::THREADS), F8::SMEM, s, a.map_q, a.map_k, a.map_vt, p);
 }
 
 }  // namespace fa

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <atomic>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -122,6 +123,29 @@ cudaError_t set_smem_limit_once(int bytes) {
     e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
+}
+
+// Launches kernel k as a programmatic dependent of the kernel before it on
+// stream s: its CTAs may start (and run their setup) while that kernel
+// finishes.  Every kernel launched this way executes griddepcontrol.wait
+// before its first access to global memory, which returns once the kernel
+// before it has completed and its writes are visible, and
+// griddepcontrol.launch_dependents early, which lets the next one start.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Each returns a cudaError_t of the launch (cudaSuccess when queued).

@@ -364,6 +364,13 @@ __device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t (
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Programmatic dependent launch: let the grid launched after this one start
+// its CTAs, and wait until the grid before this one has completed (its writes
+// visible).  The wait returns at once for a grid launched without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Stores 64 bytes (16 words) at dst: as two 32-byte stores when dst is 32-byte
 // aligned (`wide`), else as four 16-byte stores.  A thread writes a piece of its
 // own row, so a warp's store touches 32 rows at once; the wider store halves the
