@@ -23,7 +23,11 @@
  *    j <= i + (Nk - Nq).  A query that sees no key gets O = 0, LSE = -inf and
  *    zero gradients.
  *  - stream: a cudaStream_t passed as void* (NULL = the legacy default stream).
- *    Every call is asynchronous on it; nothing is synchronised.
+ *    Every call is asynchronous on it; nothing is synchronised.  Kernels are
+ *    launched as programmatic dependents of the work before them on the stream
+ *    (their setup may overlap its end), but each waits for that work to
+ *    complete before it reads or writes any buffer, so stream order holds as
+ *    for ordinary launches.
  *  - Ownership: the caller allocates and owns every buffer, workspaces
  *    included.  The library allocates no device memory and keeps no state
  *    besides a device-side error word and host-side caches (the tensor-map
