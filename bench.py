@@ -179,6 +179,29 @@ def oracle_sample(seconds, max_rows=None, seed=2):
     return flops, secs, done
 
 
+def oracle_sample_o2(seconds, seed=2):
+    """Time the C two-pass oracle (forward only, one thread per host core) on
+    256-row query blocks of the fwd workload until ``seconds`` have passed.
+    Returns (flops, secs, rows, threads)."""
+    import numpy as np
+    from exact_tiled_attention_21_gb300 import synthetic as syn
+    from oracle import twopass
+    threads = os.cpu_count() or 1
+    flops, done, secs = 0.0, 0, 0.0
+    for h in range(H):
+        q, k, v = (syn.head(seed, tag, 0, h, N, D).double().numpy() for tag in (syn.TAG_Q, syn.TAG_K, syn.TAG_V))
+        t0 = time.perf_counter()
+        for blk in np.random.default_rng(seed + h).permutation(N // 256):
+            rows = np.arange(blk * 256, blk * 256 + 256)
+            twopass.forward(q[rows], k, v, SCALE, True, rows=rows, Nq=N, nthreads=threads)
+            flops += 4.0 * D * float((rows + 1).sum())
+            done += 256
+            if secs + time.perf_counter() - t0 >= seconds:
+                return flops, secs + time.perf_counter() - t0, done, threads
+        secs += time.perf_counter() - t0
+    return flops, secs, done, threads
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -554,6 +577,10 @@ def run_ours(args, rank, world, local_rank):
             "value": f / t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
             "sample": "numpy fp64 naive fwd+bwd of %d query rows (256-row blocks of heads (0,0), "
                       "(0,1), ...), N=8192 causal, %.1f s" % (r, t)}
+        f2, t2, r2, th2 = oracle_sample_o2(args.cpu_seconds / 3)
+        line["cpu_baseline"]["o2_fwd"] = {
+            "value": f2 / t2 / 1e12, "unit": "TFLOP/s", "cores": th2, "kind": "oracle (C two-pass, forward)",
+            "sample": "forward of %d query rows (256-row blocks), N=8192 causal, %.1f s" % (r2, t2)}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
