@@ -78,8 +78,8 @@ static_assert(Dm::SMEM <= 232448, "shared memory budget");
 static_assert(Dm::OFF_Q % 1024 == 0 && Dm::OFF_P % 1024 == 0, "operand tiles need 1024-byte alignment");
 
 struct MmaParams {
-    const int* table;
-    const int* lens;
+    const int* table;  // null: the identity table (page b * max_pages + i) of a contiguous cache
+    const int* lens;   // null: every sequence is max_pages * page long
     float* part_o;
     float* part_lse;
     int B, Hq, Hkv, g, page, max_pages, num_pages, splits, ngrp, nitems;
@@ -202,7 +202,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
     // sequence lengths, clamped to the table (every role reads them per item)
     int* s_lens = reinterpret_cast<int*>(smem + Dm::OFF_LENS);
     for (int b = tid; b < p.B; b += Dm::THREADS) {
-        const int raw = __ldg(p.lens + b);
+        const int raw = p.lens ? __ldg(p.lens + b) : p.max_pages * p.page;
         const int len = clamp_len(p, raw);
         s_lens[b] = len;
         if (len != raw && blockIdx.x == 0 && atomicCAS(&p.err->code, 0, kErrInvalid) == 0) {
@@ -243,7 +243,8 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             if (w2 >= p.nitems) return 0;
             const Item n = item_of<NH>(p, w2, s_lens);
             const int pi = n.k0 / p.page + lane;
-            return (n.k0 < n.k1 && pi < p.max_pages) ? __ldg(p.table + (size_t)n.b * p.max_pages + pi) : 0;
+            if (!(n.k0 < n.k1 && pi < p.max_pages)) return 0;
+            return p.table ? __ldg(p.table + (size_t)n.b * p.max_pages + pi) : n.b * p.max_pages + pi;
         };
         int tb0 = first_entries(first), tb1 = first_entries(first + grid);
         for (int w = first; w < p.nitems && ok; w += grid) {
@@ -267,7 +268,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 if (!ok) break;
                 ++qn;
             }
-            const int* trow = p.table + (size_t)it.b * p.max_pages;
+            const int* trow = p.table ? p.table + (size_t)it.b * p.max_pages : nullptr;
             const int rows = min(p.page, 128);
             int tbl_base = it.k0 / p.page;  // tbl (lane i) = entry of page tbl_base + i
             for (int key0 = it.k0; key0 < it.k1; key0 += Dm::BK, ++g) {
@@ -278,7 +279,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 if (pfirst + npg > tbl_base + 32) {
                     tbl_base = pfirst;
                     const int pi = pfirst + lane;
-                    tbl = pi < p.max_pages ? __ldg(trow + pi) : 0;
+                    tbl = pi < p.max_pages ? (trow ? __ldg(trow + pi) : it.b * p.max_pages + pi) : 0;
                 }
                 int pg = __shfl_sync(0xffffffffu, tbl, (pfirst - tbl_base + lane) & 31);
                 if (lane < npg && (pg < 0 || pg >= p.num_pages)) {

@@ -198,7 +198,12 @@ size_t fa_decode_workspace_bytes(int B, int H, int Nk, int d, int num_splits);
  * ceil(Nk / num_splits) keys; each chunk yields a partial output and partial
  * LSE, and the partials are merged with the max-shifted rescaling of the
  * online-softmax recurrence (wiki.ai-engineering.at "Flash Attention",
- * "Lösung: Online Softmax").  q [B,H,d], kcache/vcache [B,H,Nk,d] bf16 in;
+ * "Lösung: Online Softmax").  With d = 128, Nk a multiple of 128 and
+ * B <= 2048 the chunks are read by the tensor-core kernel of
+ * fa_decode_paged (the cache as one page per sequence), whose chunks are
+ * rounded up to whole 128-key stages, so trailing chunks may be empty; every
+ * other shape takes a kernel of 16-byte loads.  The result is the same up to
+ * rounding either way.  q [B,H,d], kcache/vcache [B,H,Nk,d] bf16 in;
  * o [B,H,d] bf16 out; lse [B,H] fp32 out, may be NULL.  num_splits <= 0 lets
  * the library choose; otherwise 1 <= num_splits <= 256.  workspace: at least
  * fa_decode_workspace_bytes(B,H,Nk,d,num_splits) bytes. */

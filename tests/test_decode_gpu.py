@@ -27,7 +27,14 @@ def _run(fa, q, kc, vc, scale, splits):
 
 # (B, H, Nk, d, splits): chunks of several 128-key pieces, ragged chunks,
 # empty trailing splits (Nk < splits), a single key, automatic split count.
+# d = 128 with Nk a multiple of 128 runs on the tensor-core kernel (whole
+# 128-key stages per split, so trailing splits can be empty there too); every
+# other shape on the 16-byte-load kernel.
 CASES = [
+    (1, 2, 128, 128, 1),
+    (2, 3, 256, 128, 16),
+    (3, 2, 384, 128, 0),
+    (2, 2, 8192, 128, 7),
     (2, 3, 4096, 128, 16),
     (2, 3, 1000, 128, 16),
     (1, 4, 37, 128, 16),
