@@ -14,7 +14,7 @@ def pytest_configure(config):
 
 @pytest.fixture(scope="session")
 def cuda_lib():
-    """The built C-ABI library on a GPU machine; GPU tests fail loudly without it."""
+    """The built C-ABI library on a machine with a CUDA GPU; GPU tests fail loudly without it."""
     import torch
     import exact_tiled_attention_21_gb300 as fa
     assert torch.cuda.is_available(), "GPU test run without a CUDA device"
