@@ -3,11 +3,14 @@ fixed scratch array instead of a caller workspace, for callers that may not
 allocate device memory (a plugin host that hands over only its input and
 output buffers, a real-time loop that must not enter the allocator).
 
-It is called through the C ABI and checked against fa_decode (the entry point
-with a workspace) on two calls in a row, with the parity tolerances of the
-other decode tests.  This file is collected last on purpose.
+It is called through the C ABI.  It runs the same kernels with the same split
+count as fa_decode (the entry point with a workspace) and writes its partials
+in the same layout, so its outputs must equal fa_decode's bit for bit; each
+case is also checked against the fp64 oracle.  Every call shares the array,
+so the tests also run a call whose partials are all NaN right before a clean
+call of the same shape: the clean call must not see them.  This file is
+collected last on purpose.
 """
-import ctypes
 import math
 
 import pytest
@@ -15,6 +18,7 @@ import torch
 
 import exact_tiled_attention_21_gb300 as fa
 from exact_tiled_attention_21_gb300 import synthetic as syn
+from oracle import naive
 from tests.parity import check_out, f64
 
 pytestmark = pytest.mark.gpu
@@ -23,9 +27,13 @@ LIMIT = 16 << 20  # FA_DECODE_NOALLOC_SCRATCH_BYTES in include/fa.h
 
 
 def _case(seed, B, H, Nk, d):
+    return (syn.bhd(seed, syn.TAG_Q, B, H, d), syn.bhnd(seed, syn.TAG_K, B, H, Nk, d),
+            syn.bhnd(seed, syn.TAG_V, B, H, Nk, d))
+
+
+def _dev(*ts):
     dev = torch.device("cuda", 0)
-    return (syn.bhd(seed, syn.TAG_Q, B, H, d).to(dev), syn.bhnd(seed, syn.TAG_K, B, H, Nk, d).to(dev),
-            syn.bhnd(seed, syn.TAG_V, B, H, Nk, d).to(dev))
+    return tuple(t.to(dev) for t in ts)
 
 
 def _with_workspace(q, kc, vc, scale, splits):
@@ -47,28 +55,52 @@ def _no_alloc(q, kc, vc, scale, splits):
     return o, lse
 
 
+def _check(q, kc, vc, scale, splits, what):
+    """fa_decode_noalloc equals fa_decode bit for bit and the oracle within tolerance."""
+    qd, kd, vd = _dev(q, kc, vc)
+    o, lse = _no_alloc(qd, kd, vd, scale, splits)
+    o_ref, lse_ref = _with_workspace(qd, kd, vd, scale, splits)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all(), "%s: non-finite output" % what
+    assert torch.equal(o, o_ref), "%s: O differs from fa_decode" % what
+    assert torch.equal(lse, lse_ref), "%s: LSE differs from fa_decode" % what
+    oo, ll = naive.decode(f64(q), f64(kc), f64(vc), scale)
+    check_out(f64(o.cpu()), f64(lse.cpu()), oo, ll, what)
+
+
 def test_no_alloc_decode_matches_workspace_decode_twice(cuda_lib):
-    # two calls in a row with different shapes: the second sees the first's
-    # partials still in the shared array and must not depend on them
+    # two calls in a row: the B=32, H=32, Nk=4096 workload on the tensor-core
+    # kernel, then a d=64 ragged shape on the 16-byte-load kernel
     for seed, (B, H, Nk, d, splits) in ((41, (32, 32, 4096, 128, 16)), (42, (3, 5, 1000, 64, 7))):
         q, kc, vc = _case(seed, B, H, Nk, d)
-        scale = 1.0 / math.sqrt(d)
-        o_ref, lse_ref = _with_workspace(q, kc, vc, scale, splits)
-        o, lse = _no_alloc(q, kc, vc, scale, splits)
-        torch.cuda.synchronize()
-        check_out(f64(o.cpu()), f64(lse.cpu()), f64(o_ref.cpu()), f64(lse_ref.cpu()),
-                  "no-alloc vs workspace B%d H%d Nk%d d%d S%d" % (B, H, Nk, d, splits))
+        _check(q, kc, vc, 1.0 / math.sqrt(d), splits, "B%d H%d Nk%d d%d S%d" % (B, H, Nk, d, splits))
+
+
+@pytest.mark.parametrize("B,H,Nk,d,splits", [(4, 8, 1024, 128, 8), (4, 8, 1000, 64, 8)])
+def test_no_alloc_decode_ignores_stale_partials(cuda_lib, B, H, Nk, d, splits):
+    # same shape twice: the first call's V is all NaN, so every partial slot it
+    # writes in the shared array holds NaN; the second, clean call must not read
+    # any of them (first case: tensor-core kernel; second: 16-byte-load kernel)
+    q, kc, vc = _case(43 + d, B, H, Nk, d)
+    scale = 1.0 / math.sqrt(d)
+    qd, kd = _dev(q, kc)
+    vnan = torch.full((B, H, Nk, d), float("nan"), dtype=torch.bfloat16, device=qd.device)
+    o_nan, _ = _no_alloc(qd, kd, vnan, scale, splits)
+    torch.cuda.synchronize()
+    assert torch.isnan(o_nan).all()
+    _check(q, kc, vc, scale, splits, "after a NaN call B%d H%d Nk%d d%d S%d" % (B, H, Nk, d, splits))
 
 
 def test_no_alloc_decode_rejects_problems_beyond_the_scratch(cuda_lib):
-    B, H, Nk, d, splits = 64, 64, 4096, 128, 16  # partials need 32 MiB + 256 KiB
-    assert fa.fa_decode_workspace_bytes(B, H, Nk, d, splits) > LIMIT
-    vp = ctypes.c_void_p
-    lib = fa.load()
     with pytest.raises(fa.FAError) as err:
-        fa.fa_decode_noalloc(None, None, None, None, None, B, H, Nk, d, 0.1, splits)
+        fa.fa_decode_noalloc(None, None, None, None, None, 1, 1, 128, 128, 0.1, 1)
     assert err.value.status == fa.FA_ERR_INVALID_ARG  # null pointers are checked first
-    # argtypes were set by the binding's first call above; the pointers are
-    # never dereferenced because the size check comes before any launch
-    st = lib.fa_decode_noalloc(vp(256), vp(256), vp(256), vp(256), None, B, H, Nk, d, 0.1, splits, None)
-    assert st == fa.FA_ERR_WORKSPACE
+    # real buffers: 16 x 16 heads, 256 keys, 256 splits need 32 MiB + 256 KiB of partials
+    B, H, Nk, d, splits = 16, 16, 256, 128, 256
+    assert fa.fa_decode_workspace_bytes(B, H, Nk, d, splits) > LIMIT
+    q, kc, vc = _dev(*_case(44, B, H, Nk, d))
+    with pytest.raises(fa.FAError) as err:
+        _no_alloc(q, kc, vc, 1.0 / math.sqrt(d), splits)
+    assert err.value.status == fa.FA_ERR_WORKSPACE
+    # the same problem with fewer splits fits and still runs
+    _check(*_case(44, B, H, Nk, d), 1.0 / math.sqrt(d), 16, "B16 H16 Nk256 S16 after the rejection")
