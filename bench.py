@@ -257,7 +257,9 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
     B=32, H=32 for d=128 with Nk=4096 and Nk=4000 and for d=64.  Each entry is
     the median over calls bracketed by CUDA events on the launching stream.  L2
     is flushed (a 256 MiB write) before every call whose inputs would otherwise
-    stay in it; decode caches (>= 1 GiB) are larger than L2."""
+    stay in it; decode caches (>= 1 GiB) are larger than L2.  Decode runs first
+    and the long forward last, so the seconds-long full load of the latter
+    cannot pull the clocks of the others down."""
     import torch
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -281,6 +283,25 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
            "timing": "median of per-call CUDA-event times on the launching stream; L2 flushed before each "
                      "fwd/bwd call (256 MiB write, outside the events)",
            "_windows": {}}
+    # decode shapes (the cache is read once per call; >= 1 GiB, larger than L2)
+    t0 = time.time()
+    for nk, d in ((4096, 128), (4000, 128), (4096, 64)):
+        q = rnd(DEC_B, DEC_H, d)
+        kc, vc = rnd(DEC_B, DEC_H, nk, d), rnd(DEC_B, DEC_H, nk, d)
+        o = torch.empty_like(q)
+        lse = torch.empty(DEC_B, DEC_H, device=dev, dtype=torch.float32)
+        ws = torch.empty(fa.fa_decode_workspace_bytes(DEC_B, DEC_H, nk, d, DEC_SPLITS), dtype=torch.uint8,
+                         device=dev)
+        call = lambda: fa.fa_decode(q, kc, vc, o, lse, DEC_B, DEC_H, nk, d, 1.0 / math.sqrt(d), DEC_SPLITS, ws,
+                                    ws.numel(), stream)
+        for _ in range(3):
+            call()
+        ms = timed(call, 20, False)
+        byt = 2.0 * DEC_B * DEC_H * nk * d * 2
+        out["decode_B32_H32"].append({"Nk": nk, "d": d, "splits": DEC_SPLITS, "ms": ms,
+                                      "gbs": byt / (ms * 1e-3) / 1e9})
+        del q, kc, vc, o, lse, ws
+    out["_windows"]["decode"] = (t0, time.time())
     t0 = time.time()
     for n in SWEEP_N:
         q, k, v, dO = (rnd(1, H, n, D) for _ in range(4))
@@ -315,51 +336,42 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
         del q, k, v, o, lse
     out["_windows"]["short"] = (t0, time.time())
 
-    # long causal forward: peak device memory over the inputs' own footprint
+    # long causal forward (last: its seconds of full load can bring the power cap in).  Its
+    # memory: the device's used bytes (cudaMemGetInfo, which sees every allocation, the
+    # library's included) and the torch allocator's peak, both over the inputs' own
+    # footprint; the library allocates nothing, so both stay at the floor.
     barrier()
     torch.cuda.empty_cache()
-    torch.cuda.reset_peak_memory_stats(dev)
     base = torch.cuda.memory_allocated(dev)
     q, k, v = (rnd(1, H, LONG_N, D, std=0.5) for _ in range(3))
     o = torch.empty_like(q)
     lse = torch.empty(1, H, LONG_N, device=dev, dtype=torch.float32)
     floor = 4 * q.numel() * 2 + lse.numel() * 4
     fwd = lambda: fa.fa_fwd(q, k, v, o, lse, 1, H, LONG_N, LONG_N, D, SCALE, True, stream)
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats(dev)
+    free0 = torch.cuda.mem_get_info(dev)[0]
     fwd()
     torch.cuda.synchronize(dev)
     tl0 = time.time()
     l_ms = timed(fwd, 5, False)
     tl1 = time.time()
+    free1 = torch.cuda.mem_get_info(dev)[0]
     peak = torch.cuda.max_memory_allocated(dev) - base
     fl = 4.0 * H * LONG_N * LONG_N * D / 2
     out["fwd_long_causal_B1_H32_N131072_d128"] = {
         "fwd_ms": l_ms, "fwd_tflops": fl / (l_ms * 1e-3) / 1e12, "inputs": "N(0, 0.5^2) bf16",
         "peak_mib": peak / 2**20, "floor_mib": floor / 2**20,
-        "memory_note": "max_memory_allocated over the call minus what was allocated before its inputs; "
-                       "floor = Q, K, V, O bf16 + LSE fp32 (a materialised S would be 2 TiB)"}
+        "device_used_delta_mib": (free0 - free1) / 2**20,
+        "memory_note": "peak_mib: the torch allocator's peak during the calls (counted from after the inputs "
+                       "were made) minus what was allocated before the inputs; device_used_delta_mib: the "
+                       "device's used memory after the calls minus before them (cudaMemGetInfo); floor = Q, K, "
+                       "V, O bf16 + LSE fp32 (a materialised S would be 2 TiB)"}
     out["_windows"]["long"] = (tl0, tl1)
     del q, k, v, o, lse
     torch.cuda.empty_cache()
 
-    # decode shapes (the cache is read once per call; >= 1 GiB, larger than L2)
-    t0 = time.time()
-    for nk, d in ((4096, 128), (4000, 128), (4096, 64)):
-        q = rnd(DEC_B, DEC_H, d)
-        kc, vc = rnd(DEC_B, DEC_H, nk, d), rnd(DEC_B, DEC_H, nk, d)
-        o = torch.empty_like(q)
-        lse = torch.empty(DEC_B, DEC_H, device=dev, dtype=torch.float32)
-        ws = torch.empty(fa.fa_decode_workspace_bytes(DEC_B, DEC_H, nk, d, DEC_SPLITS), dtype=torch.uint8,
-                         device=dev)
-        call = lambda: fa.fa_decode(q, kc, vc, o, lse, DEC_B, DEC_H, nk, d, 1.0 / math.sqrt(d), DEC_SPLITS, ws,
-                                    ws.numel(), stream)
-        for _ in range(3):
-            call()
-        ms = timed(call, 20, False)
-        byt = 2.0 * DEC_B * DEC_H * nk * d * 2
-        out["decode_B32_H32"].append({"Nk": nk, "d": d, "splits": DEC_SPLITS, "ms": ms,
-                                      "gbs": byt / (ms * 1e-3) / 1e9})
-        del q, kc, vc, o, lse, ws
-    out["_windows"]["decode"] = (t0, time.time())
     del flush_buf
     torch.cuda.empty_cache()
     return out

@@ -92,7 +92,7 @@ int make_map_nd(CUtensorMap* m, const void* base, int rank, const cuuint64_t* di
 // Page sizes the tensor-core paged decode takes: whole 8-row swizzle atoms
 // per page, and pages that tile a 128-key stage (or stages that tile a page).
 bool paged_mma_ok(int B, int d, int page) {
-    if (B > 2048 || d != 128 || page % 8 != 0) return false;  // lengths of up to 2048 sequences staged on chip
+    if (B > 2048 || (d != 64 && d != 128) || page % 8 != 0) return false;  // lengths of up to 2048 sequences staged on chip
     return page <= 128 ? (128 % page == 0) : (page % 128 == 0);
 }
 
@@ -426,21 +426,26 @@ int paged_mma_maps(PagedDecodeLaunch& a) {
     const cuuint64_t vs[4] = {(cuuint64_t)d * 2, 128, (cuuint64_t)page_size * d * 2,
                               (cuuint64_t)a.Hkv * page_size * d * 2};
     const cuuint32_t vb[5] = {64, (cuuint32_t)std::min(page_size, 128), 2, 1, 1};
+    // d = 64: a row is one 128-byte swizzle row, so V takes the same 4-D form as K
     if (make_map_nd(&a.map_q, a.q, 3, qd, qs, qb) || make_map_nd(&a.map_k, a.kp, 4, kd, ks, kb) ||
-        make_map_nd(&a.map_v, a.vp, 5, vd, vs, vb))
+        (d == 128 ? make_map_nd(&a.map_v, a.vp, 5, vd, vs, vb) : make_map_nd(&a.map_v, a.vp, 4, kd, ks, kb)))
         return FA_ERR_CUDA;
     return FA_OK;
 }
 
 // Contiguous decode (fa_decode, fa_decode_noalloc) with d = 128 and Nk a multiple of 128 runs on the
-// tensor-core paged kernel: the cache [B, H, Nk, d] is the paged layout with one page of Nk tokens
-// per sequence (page b of sequence b, implicit in the kernel), one kv head per query head.  Its TMA
-// stages read the cache at ~7 TB/s against ~6.3 TB/s for the 16-byte-load kernel.  Returns false when
+// tensor-core paged kernel: the cache [B, H, Nk, d] is the paged layout with one page of Nk tokens per
+// sequence (page b of sequence b, implicit in the kernel), one kv head per query head.  Its TMA stages
+// read the cache at ~6.8 TB/s against ~6.3 TB/s for the 16-byte-load kernel.  Other shapes are faster
+// on the 16-byte-load kernel (measured at B=32, H=32, 16 splits): with one query head per kv head
+// every work item is a split of two 128-key stages, and the kernel's fixed cost per item and per
+// stage, which d = 128 hides behind 64 KB of cache per stage, shows at d = 64 (4.0 against 5.8 TB/s
+// at Nk = 4096) and on a ragged last stage (6.0 against 6.2 TB/s at Nk = 4000).  Returns false when
 // the shape takes the 16-byte-load kernel.
 bool contiguous_on_mma(int B, int Nk, int d) { return d == 128 && Nk % 128 == 0 && paged_mma_ok(B, d, Nk); }
 
 int launch_contiguous_on_mma(const void* q, const void* kcache, const void* vcache, void* o, float* lse, int B,
-                             int H, int Nk, float scale, int splits, float* part_o, void* stream) {
+                             int H, int Nk, int d, float scale, int splits, float* part_o, void* stream) {
     PagedDecodeLaunch a;
     int st = device_state(&a.err, &a.num_sms);
     if (st != FA_OK) return st;
@@ -453,14 +458,14 @@ int launch_contiguous_on_mma(const void* q, const void* kcache, const void* vcac
     a.o = o;
     a.lse = lse;
     a.part_o = part_o;
-    a.part_lse = part_o + (size_t)B * H * splits * 128;  // the layout of the fa_decode workspace
+    a.part_lse = part_o + (size_t)B * H * splits * d;  // the layout of the fa_decode workspace
     a.B = B;
     a.Hq = H;
     a.Hkv = H;
     a.page = Nk;
     a.max_pages = 1;
     a.num_pages = B;
-    a.d = 128;
+    a.d = d;
     a.splits = splits;
     a.scale = scale;
     a.timeout_ns = g_timeout_ns.load();
@@ -487,7 +492,7 @@ int fa_decode(const void* q, const void* kcache, const void* vcache, void* o, fl
     if (!workspace || workspace_bytes < decode_ws_bytes(B, H, d, splits)) return FA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
     if (contiguous_on_mma(B, Nk, d))
-        return launch_contiguous_on_mma(q, kcache, vcache, o, lse, B, H, Nk, scale, splits,
+        return launch_contiguous_on_mma(q, kcache, vcache, o, lse, B, H, Nk, d, scale, splits,
                                         static_cast<float*>(workspace), stream);
     st = device_state(nullptr, nullptr);
     if (st != FA_OK) return st;
@@ -681,7 +686,7 @@ extern "C" int fa_decode_noalloc(const void* q, const void* kcache, const void* 
         scratch = g_scratch_addr[dev];
     }
     if (contiguous_on_mma(B, Nk, d))
-        return launch_contiguous_on_mma(q, kcache, vcache, o, lse, B, H, Nk, scale, splits,
+        return launch_contiguous_on_mma(q, kcache, vcache, o, lse, B, H, Nk, d, scale, splits,
                                         static_cast<float*>(scratch), stream);
     DecodeLaunch a;
     a.q = q;

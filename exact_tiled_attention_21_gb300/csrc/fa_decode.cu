@@ -20,7 +20,12 @@ namespace fa {
 namespace {
 
 constexpr int kDecThreads = 128;
-constexpr int kDecPiece = 128;  // keys per online-softmax step
+// keys per online-softmax step: 128 at d = 128 (64 KB of K and V in flight per CTA); 256 at
+// d = 64, so that a CTA keeps as many bytes in flight and pays its reductions and barriers
+// once per 64 KB there too
+template <int D>
+constexpr int kDecPiece = D == 64 ? 256 : 128;
+constexpr int kPagedPiece = 128;  // keys per step of the paged general kernel
 
 template <int D>
 __global__ void __launch_bounds__(kDecThreads)
@@ -29,11 +34,13 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
                     float* __restrict__ part_lse, int Nk, int splits, int chunk, float scale_log2) {
     pdl_launch_dependents();
     pdl_wait();  // the cache and q may come from the kernel before; it may still read part_o
+    constexpr int PIECE = kDecPiece<D>;
+    constexpr int KPT = PIECE / kDecThreads;  // scores per thread in the softmax of a piece
     constexpr int LPK = D / 8;              // lanes per key row
     constexpr int KPW = 32 / LPK;           // keys per warp per load
     constexpr int KPC = KPW * (kDecThreads / 32);  // keys per CTA per load step
-    constexpr int STEPS = kDecPiece / KPC;  // load steps per piece
-    __shared__ float s_p[kDecPiece];
+    constexpr int STEPS = PIECE / KPC;      // load steps per piece
+    __shared__ float s_p[PIECE];
     __shared__ float s_red[kDecThreads / 32];
     __shared__ float s_acc[KPC][D + 4];
 
@@ -71,7 +78,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 
-    for (int p0 = k0; p0 < k1; p0 += kDecPiece) {
+    for (int p0 = k0; p0 < k1; p0 += PIECE) {
         // ---- scores of this piece (the piece's V rows are loaded with its K rows, so both
         // are in flight together)
         uint4 kr[STEPS], vr[STEPS];
@@ -103,8 +110,13 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
             if (slice == 0) s_p[kl] = (p0 + kl < k1) ? dot : -INFINITY;
         }
         __syncthreads();
-        // ---- piece maximum (CTA), new running max
-        float mx = s_p[tid];  // kDecThreads == kDecPiece
+        // ---- piece maximum (CTA), new running max; thread tid owns scores tid + 128 i
+        float sc[KPT];
+#pragma unroll
+        for (int i = 0; i < KPT; ++i) sc[i] = s_p[tid + kDecThreads * i];
+        float mx = sc[0];
+#pragma unroll
+        for (int i = 1; i < KPT; ++i) mx = fmaxf(mx, sc[i]);
         for (int w = 16; w >= 1; w >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, w));
         if (lane == 0) s_red[warp] = mx;
         __syncthreads();
@@ -113,11 +125,16 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
         for (int w = 1; w < kDecThreads / 32; ++w) mx = fmaxf(mx, s_red[w]);
         const float m_new = fmaxf(m_run, mx);  // finite: every piece holds >= 1 key
         const float alpha = ex2(m_run - m_new);  // m_run = -inf on the first piece -> 0
-        const float pv = ex2(s_p[tid] - m_new);
-        float ps = pv;
+        float ps = 0.f;
+#pragma unroll
+        for (int i = 0; i < KPT; ++i) {
+            sc[i] = ex2(sc[i] - m_new);
+            ps += sc[i];
+        }
         for (int w = 16; w >= 1; w >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, w);
         __syncthreads();  // s_red, s_p reads done
-        s_p[tid] = pv;
+#pragma unroll
+        for (int i = 0; i < KPT; ++i) s_p[tid + kDecThreads * i] = sc[i];
         if (lane == 0) s_red[warp] = ps;
         __syncthreads();
         float psum = 0.f;
@@ -235,11 +252,11 @@ decode_paged_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
                           int num_pages, int splits, int groups, float scale_log2, DevError* err) {
     pdl_launch_dependents();
     pdl_wait();
-    constexpr int LPK = D / 8, KPW = 32 / LPK, KPC = KPW * (kDecThreads / 32), STEPS = kDecPiece / KPC;
-    __shared__ float s_p[G][kDecPiece];
+    constexpr int LPK = D / 8, KPW = 32 / LPK, KPC = KPW * (kDecThreads / 32), STEPS = kPagedPiece / KPC;
+    __shared__ float s_p[G][kPagedPiece];
     __shared__ float s_red[kDecThreads / 32][G];
     __shared__ float s_acc[KPC][D + 4];
-    __shared__ long long s_row[kDecPiece];  // element offset of each key row of the piece (-1: bad page)
+    __shared__ long long s_row[kPagedPiece];  // element offset of each key row of the piece (-1: bad page)
     __shared__ int s_bad;
 
     int idx = blockIdx.x;
@@ -293,7 +310,7 @@ decode_paged_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
         for (int i = 0; i < 8; ++i) acc[hh][i] = 0.f;
     }
     bool bad = false;
-    for (int p0 = k0; p0 < k1; p0 += kDecPiece) {
+    for (int p0 = k0; p0 < k1; p0 += kPagedPiece) {
         {   // one block-table lookup per key of the piece (thread = key), shared by the K and V loads
             const int key = p0 + tid;
             long long off = -1;

@@ -43,14 +43,15 @@
 namespace fa {
 namespace {
 
+template <int D_>
 struct Dm {
-    static constexpr int D = 128;
+    static constexpr int D = D_;                  // 128 or 64
     static constexpr int BK = 128;                // keys per stage
-    static constexpr int NG = 16;                 // query heads per work item (MMA N)
-    static constexpr int SLOT = BK * D * 2;       // one K or V stage, 32 KB
-    static constexpr int CHUNK = BK * 128;        // 64 features x 128 keys
-    static constexpr int NSLOT = 3;               // stages in flight, K and V rings each
-    static constexpr int Q_BYTES = NG * D * 2;    // 4 KB
+    static constexpr int NG = 16;                 // query heads per work item (MMA N of the scores)
+    static constexpr int SLOT = BK * D * 2;       // one K or V stage: 32 KB (d = 128), 16 KB (d = 64)
+    static constexpr int CHUNK = BK * 128;        // 64 features x 128 keys (the two halves of d = 128)
+    static constexpr int NSLOT = D == 128 ? 3 : 6;  // stages in flight, K and V rings each (192 KB either way)
+    static constexpr int Q_BYTES = NG * D * 2;
     static constexpr int QCHUNK = NG * 128;       // 64 features x 16 rows
     static constexpr int P_BYTES = NG * BK * 2;   // 4 KB
     static constexpr int PCHUNK = NG * 128;       // 64 keys x 16 heads
@@ -59,7 +60,8 @@ struct Dm {
     static constexpr int OFF_Q = 2 * NSLOT * SLOT;  // 2 buffers
     static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;  // 2 buffers
     static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;  // fp32 max [2][4][16], sums [4][16]
-    static constexpr int OFF_LENS = OFF_RED + (2 * 4 * 16 + 4 * 16) * 4;  // int32 [MAX_B]
+    static constexpr int OFF_X = OFF_RED + (2 * 4 * 16 + 4 * 16) * 4;  // d = 64: the second O^T half, [64][16] fp32
+    static constexpr int OFF_LENS = OFF_X + (D == 64 ? 64 * 16 * 4 : 0);  // int32 [MAX_B]
     static constexpr int MAX_B = 2048;
     static constexpr int OFF_BAR = OFF_LENS + MAX_B * 4;
     // k_full, k_empty, v_full, v_empty [NSLOT each], q_full[2], q_empty[2], s_full[2], p_ready[2], pv_done[2],
@@ -70,12 +72,16 @@ struct Dm {
     static constexpr int THREADS = 224;
     static constexpr uint32_t TMEM_COLS = 64;
     static constexpr uint32_t COL_S = 0;          // two 16-column S^T buffers
-    static constexpr uint32_t COL_O = 32;         // O^T, 16 columns
+    static constexpr uint32_t COL_O = 32;         // O^T: 16 columns (d = 128) or 32 (d = 64, below)
+    // d = 64: the value product runs with M = 128 rows = (64 features) x (keys 0-63 | keys 64-127)
+    // and N = 32 columns = (16 heads) x (the same two key halves); only the two diagonal blocks
+    // are used, and O^T[f][h] = D[f][h] + D[64 + f][16 + h]
+    static constexpr int NO = D == 128 ? NG : 2 * NG;
     static constexpr uint32_t IDESC_S = idesc_bf16(128, NG, 0, 0);  // K, Q both K-major
-    static constexpr uint32_t IDESC_O = idesc_bf16(128, NG, 1, 0);  // V^T MN-major, P^T K-major
+    static constexpr uint32_t IDESC_O = idesc_bf16(128, NO, 1, 0);  // V^T MN-major, P^T K-major
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "operand tiles need 1024-byte alignment");
 };
-static_assert(Dm::SMEM <= 232448, "shared memory budget");
-static_assert(Dm::OFF_Q % 1024 == 0 && Dm::OFF_P % 1024 == 0, "operand tiles need 1024-byte alignment");
 
 struct MmaParams {
     const int* table;  // null: the identity table (page b * max_pages + i) of a contiguous cache
@@ -152,11 +158,12 @@ __device__ __forceinline__ float bfly(const float (&v)[NH], int lane) {
     return d;
 }
 
-template <int NH>
-__global__ void __launch_bounds__(Dm::THREADS, 1)
+template <int D, int NH>
+__global__ void __launch_bounds__(Dm<D>::THREADS, 1)
 decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v, const MmaParams p) {
     static_assert(NH == 4 || NH == 8 || NH == 16, "heads per item");
+    using Dm = fa::Dm<D>;
     constexpr int LPH = 32 / NH;  // lanes per head after the butterfly
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -259,7 +266,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                     if (qn >= 2) ok = mbar_wait(BAR_QE + 8 * qb, ((qn >> 1) - 1) & 1, ctl, kSitePagedQ);
                     if (ok) {
                         mbar_arrive_expect_tx(BAR_QF + 8 * qb, Dm::Q_BYTES);
-                        for (int c = 0; c < 2; ++c)
+                        for (int c = 0; c < D / 64; ++c)
                             tma_load_3d(s_base + Dm::OFF_Q + qb * Dm::Q_BYTES + c * Dm::QCHUNK, &map_q,
                                         BAR_QF + 8 * qb, c * 64, it.b * p.Hq + it.h0, 0, pol_q);
                     }
@@ -292,18 +299,21 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 }
                 if (lane == 0) {
                     ok = mbar_wait(bar_empty(kv, g), ring_par(g) ^ 1, ctl, kSitePagedKv);
-                    if (ok) mbar_arrive_expect_tx(bar_full(kv, g), (uint32_t)(npg * rows * 256));
+                    if (ok) mbar_arrive_expect_tx(bar_full(kv, g), (uint32_t)(npg * rows * D * 2));
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 if (lane < npg) {
                     if (!kv) {
                         const uint32_t dst = s_base + Dm::OFF_K + (g % Dm::NSLOT) * Dm::SLOT + (uint32_t)(lane * rows * 128);
-                        for (int c = 0; c < 2; ++c)
+                        for (int c = 0; c < D / 64; ++c)
                             tma_load_4d(dst + c * Dm::CHUNK, &map_k, bar_full(0, g), c * 64, prow0, it.kvh, pg, pol_kv);
-                    } else {
+                    } else if constexpr (D == 128) {
                         const uint32_t dst = s_base + Dm::OFF_V + (g % Dm::NSLOT) * Dm::SLOT + (uint32_t)(lane * rows * 256);
                         tma_load_5d(dst, &map_v, bar_full(1, g), 0, prow0, 0, it.kvh, pg, pol_kv);
+                    } else {  // d = 64: a page's rows are whole 128-byte rows, back to back
+                        const uint32_t dst = s_base + Dm::OFF_V + (g % Dm::NSLOT) * Dm::SLOT + (uint32_t)(lane * rows * 128);
+                        tma_load_4d(dst, &map_v, bar_full(1, g), 0, prow0, it.kvh, pg, pol_kv);
                     }
                 }
                 issued |= 1u << (g % Dm::NSLOT);
@@ -382,11 +392,20 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                         tc_fence_after();
                         const uint32_t sV = s_base + Dm::OFF_V + (cv.g % Dm::NSLOT) * Dm::SLOT;
                         const uint32_t sP = s_base + Dm::OFF_P + (cv.g & 1) * Dm::P_BYTES;
+                        if constexpr (D == 128) {
 #pragma unroll
-                        for (int k = 0; k < Dm::BK / 16; ++k)
-                            mma_ss(tmem + Dm::COL_O, sdesc_sw128(sV + v_off[k], v_lbo, v_sbo),
-                                   sdesc_sw128(sP + (k >> 2) * Dm::PCHUNK + (k & 3) * 32, 16, 1024), Dm::IDESC_O,
-                                   (cv.j > 0 || k > 0) ? 1u : 0u);
+                            for (int k = 0; k < Dm::BK / 16; ++k)
+                                mma_ss(tmem + Dm::COL_O, sdesc_sw128(sV + v_off[k], v_lbo, v_sbo),
+                                       sdesc_sw128(sP + (k >> 2) * Dm::PCHUNK + (k & 3) * 32, 16, 1024), Dm::IDESC_O,
+                                       (cv.j > 0 || k > 0) ? 1u : 0u);
+                        } else {
+                            // M-block 0: keys 16k.. (rows of 128 B), M-block 1: keys 64 + 16k.. (LBO
+                            // 8 KB); B: 32 rows = both 64-key chunks of P^T, contiguous
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_ss(tmem + Dm::COL_O, sdesc_sw128(sV + 2048 * k, 64 * 128, 1024),
+                                       sdesc_sw128(sP + 32 * k, 16, 1024), Dm::IDESC_O, (cv.j > 0 || k > 0) ? 1u : 0u);
+                        }
                         mma_commit(BAR_PV + 8 * (cv.g & 1));
                         mma_commit(bar_empty(1, cv.g));
                         if (++cv.j == cv.nst) {
@@ -429,8 +448,9 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             const Item it = item_of<NH>(p, w, s_lens);
             const size_t head0 = (size_t)it.b * p.Hq + it.h0;
             if (it.k0 >= it.k1) {  // empty split: weight 0 in the combine
-                for (int h = 0; h < it.gcount; ++h)
-                    p.part_o[((head0 + h) * p.splits + it.split) * Dm::D + r] = 0.f;
+                if (r < D)
+                    for (int h = 0; h < it.gcount; ++h)
+                        p.part_o[((head0 + h) * p.splits + it.split) * Dm::D + r] = 0.f;
                 if (r < it.gcount) p.part_lse[(head0 + r) * p.splits + it.split] = -INFINITY;
                 continue;
             }
@@ -482,11 +502,22 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                     ok = __all_sync(0xffffffffu, ok);
                     tc_fence_after();
                     if (ok) {
-                        uint32_t ov[16];
-                        tmem_ld16(lane_addr + Dm::COL_O, ov);
+                        if constexpr (D == 128) {
+                            uint32_t ov[16];
+                            tmem_ld16(lane_addr + Dm::COL_O, ov);
 #pragma unroll
-                        for (int h = 0; h < NH; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-                        tmem_st16(lane_addr + Dm::COL_O, ov);
+                            for (int h = 0; h < NH; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+                            tmem_st16(lane_addr + Dm::COL_O, ov);
+                        } else {  // both key halves of every head
+                            uint32_t ov[32];
+                            tmem_ld32(lane_addr + Dm::COL_O, ov);
+#pragma unroll
+                            for (int h = 0; h < NH; ++h) {
+                                ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+                                ov[16 + h] = __float_as_uint(__uint_as_float(ov[16 + h]) * alpha[h]);
+                            }
+                            tmem_st32(lane_addr + Dm::COL_O, ov);
+                        }
                     }
 #pragma unroll
                     for (int h = 0; h < NH; ++h) lp[h] *= alpha[h], m_run[h] = m_new[h];
@@ -507,12 +538,12 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                     if (ok) ok = mbar_wait(bar_full(1, gs), ring_par(gs), ctl, kSitePagedKv);
                     if (!valid) {
                         uint4* row = reinterpret_cast<uint4*>(smem + Dm::OFF_V + (gs % Dm::NSLOT) * Dm::SLOT +
-                                                              (r / R) * (R * 256) + (r % R) * 128);
+                                                              (r / R) * (R * 2 * D) + (r % R) * 128);
                         const int half = R * 128 / 16;  // uint4s from a row of one half to the other
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             row[i] = make_uint4(0u, 0u, 0u, 0u);
-                            row[half + i] = make_uint4(0u, 0u, 0u, 0u);
+                            if (D == 128) row[half + i] = make_uint4(0u, 0u, 0u, 0u);
                         }
                     }
                 }
@@ -540,17 +571,45 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             ++items;
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
-            uint32_t ov[16];
-            if (ok) {
-                tmem_ld16(lane_addr + Dm::COL_O, ov);
-            } else {
-#pragma unroll
-                for (int h = 0; h < 16; ++h) ov[h] = 0u;
-            }
             float* po = p.part_o + (head0 * p.splits + it.split) * Dm::D + r;
+            if constexpr (D == 128) {
+                uint32_t ov[16];
+                if (ok) {
+                    tmem_ld16(lane_addr + Dm::COL_O, ov);
+                } else {
 #pragma unroll
-            for (int h = 0; h < NH; ++h)
-                if (h < it.gcount) po[(size_t)h * p.splits * Dm::D] = __uint_as_float(ov[h]) * inv_l[h];
+                    for (int h = 0; h < 16; ++h) ov[h] = 0u;
+                }
+#pragma unroll
+                for (int h = 0; h < NH; ++h)
+                    if (h < it.gcount) po[(size_t)h * p.splits * Dm::D] = __uint_as_float(ov[h]) * inv_l[h];
+            } else {
+                // feature r < 64: its keys 0-63 part in its own lane (columns h), its keys 64-127
+                // part in lane 64 + r (columns 16 + h), handed over through shared memory
+                uint32_t ov[32];
+                if (ok) {
+                    tmem_ld32(lane_addr + Dm::COL_O, ov);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) ov[h] = 0u;
+                }
+                float* xo = reinterpret_cast<float*>(smem + Dm::OFF_X);
+                if (r >= 64) {
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) xo[(r - 64) * 16 + ((h + r) & 15)] = __uint_as_float(ov[16 + h]);
+                }
+                if (!bar_and(1, 128, ok)) {
+                    failed = true;
+                    break;
+                }
+                if (r < 64) {
+#pragma unroll
+                    for (int h = 0; h < NH; ++h)
+                        if (h < it.gcount)
+                            po[(size_t)h * p.splits * Dm::D] =
+                                (__uint_as_float(ov[h]) + xo[r * 16 + ((h + r) & 15)]) * inv_l[h];
+                }
+            }
             if (r < it.gcount) p.part_lse[(head0 + r) * p.splits + it.split] = lse;
         }
     }
@@ -564,23 +623,30 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
     }
 }
 
-template <int NH>
+template <int D, int NH>
 cudaError_t launch_nh(const PagedDecodeLaunch& a, MmaParams p, cudaStream_t s) {
+    using C = Dm<D>;
     p.ngrp = (p.g + NH - 1) / NH;
     const long long nitems = (long long)a.B * a.Hkv * p.ngrp * a.splits;
     if (nitems > 0x7FFFFFFFll) return cudaErrorInvalidValue;
     p.nitems = (int)nitems;
-    cudaError_t e = set_smem_limit_once<decode_paged_mma_kernel<NH>>(Dm::SMEM);
+    cudaError_t e = set_smem_limit_once<decode_paged_mma_kernel<D, NH>>(C::SMEM);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<long long>(nitems, a.num_sms);
-    return launch_dependent(decode_paged_mma_kernel<NH>, dim3(grid), dim3(Dm::THREADS), Dm::SMEM, s, a.map_q, a.map_k,
-                            a.map_v, p);
+    return launch_dependent(decode_paged_mma_kernel<D, NH>, dim3(grid), dim3(C::THREADS), C::SMEM, s, a.map_q,
+                            a.map_k, a.map_v, p);
+}
+
+template <int D>
+cudaError_t launch_d(const PagedDecodeLaunch& a, const MmaParams& p, cudaStream_t s) {
+    // heads per work item: the group, in MMA columns of 4, 8 or 16
+    return p.g <= 4 ? launch_nh<D, 4>(a, p, s) : p.g <= 8 ? launch_nh<D, 8>(a, p, s) : launch_nh<D, 16>(a, p, s);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_paged_mma(const PagedDecodeLaunch& a, cudaStream_t s) {
-    if (a.B > Dm::MAX_B) return cudaErrorInvalidValue;
+    if (a.B > Dm<128>::MAX_B || (a.d != 64 && a.d != 128)) return cudaErrorInvalidValue;
     MmaParams p;
     p.B = a.B;
     p.table = a.table;
@@ -597,8 +663,7 @@ cudaError_t launch_decode_paged_mma(const PagedDecodeLaunch& a, cudaStream_t s) 
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
     p.timeout_ns = a.timeout_ns;
-    // heads per work item: the group, in MMA columns of 4, 8 or 16
-    cudaError_t e = p.g <= 4 ? launch_nh<4>(a, p, s) : p.g <= 8 ? launch_nh<8>(a, p, s) : launch_nh<16>(a, p, s);
+    cudaError_t e = a.d == 128 ? launch_d<128>(a, p, s) : launch_d<64>(a, p, s);
     if (e != cudaSuccess) return e;
     return launch_decode_combine(a.part_o, a.part_lse, a.o, a.lse, a.B * a.Hq, a.splits, a.d, s);
 }

@@ -44,6 +44,15 @@ CASES = [
     (1, 2, 5000, 64, 0),
     (1, 2, 70000, 128, 0),
     (1, 1, 777, 128, 256),
+    (2, 3, 4001, 128, 16),
+    (1, 2, 129, 128, 4),
+    (2, 3, 4096, 64, 16),
+    (2, 2, 1000, 64, 0),
+    (1, 1, 777, 64, 256),
+    (1, 2, 64, 64, 4),
+    (1, 2, 8, 128, 1),
+    (1, 2, 100, 128, 4),
+    (2, 3, 70000, 64, 0),
 ]
 
 

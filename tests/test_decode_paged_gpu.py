@@ -54,6 +54,12 @@ CASES = [
     (1, 8, 2, 16, [20000], 128, 1),             # one split: 157 stages through the ring
     (32, 32, 8, 16, [4096] * 30 + [1, 777], 128, 0),  # automatic split count (tensor-core path)
     (3, 8, 2, 48, [1000, 3, 480], 128, 0),      # automatic split count (general path)
+    (2, 32, 2, 8, [1000, 129], 64, 5),          # d = 64 on the tensor cores: 8-token pages, group of 16
+    (2, 8, 2, 256, [1000, 300], 64, 2),         # d = 64, pages longer than a stage
+    (1, 40, 2, 32, [333], 64, 2),               # d = 64, group of 20
+    (1, 8, 2, 16, [20000], 64, 1),              # d = 64, 157 stages through the ring
+    (32, 32, 8, 16, [4096] * 30 + [1, 777], 64, 0),  # d = 64, automatic split count
+    (2, 8, 2, 48, [500, 77], 64, 3),            # d = 64, general path (48-token pages)
 ]
 
 
@@ -102,13 +108,13 @@ def test_paged_decode_rejects_bad_page_index_on_device(cuda_lib):
     assert cuda_lib.fa_get_last_device_error()[0] == 0
 
 
-@pytest.mark.parametrize("P", [16, 48, 256])
-def test_paged_decode_ignores_unused_slots(cuda_lib, P):
+@pytest.mark.parametrize("P,d", [(16, 128), (48, 128), (256, 128), (16, 64), (256, 64)])
+def test_paged_decode_ignores_unused_slots(cuda_lib, P, d):
     """Tokens past seq_lens[b] in the last page, and pages no table names,
     may hold anything (NaN here): the result depends only on the tokens in
     range."""
     lens = [P * 3 + 5, 1, 2 * P]
-    q, kp, vp, table, L = _case(31 + P, 3, 8, 2, P, lens, 128)
+    q, kp, vp, table, L = _case(31 + P, 3, 8, 2, P, lens, d)
     kp_bad, vp_bad = kp.clone(), vp.clone()
     used = np.zeros((kp.shape[0], P), dtype=bool)
     for b, n in enumerate(lens):
@@ -118,23 +124,24 @@ def test_paged_decode_ignores_unused_slots(cuda_lib, P):
     kp_bad[mask] = float("nan")
     vp_bad[mask] = float("nan")
     o, lse = _run(cuda_lib, q, kp_bad, vp_bad, table, L, 4)
-    o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(128))
+    o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(d))
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
-    check_out(f64(o), f64(lse), o_ref, lse_ref, "unused slots P%d" % P)
+    check_out(f64(o), f64(lse), o_ref, lse_ref, "unused slots P%d d%d" % (P, d))
 
 
-def test_paged_decode_growing_scores(cuda_lib):
+@pytest.mark.parametrize("d", [128, 64])
+def test_paged_decode_growing_scores(cuda_lib, d):
     """Key norms that grow along the sequence raise every head's running
     maximum by far more than 2^8 between stages, so the output accumulator
     is rescaled many times within one split."""
     B, Hq, Hkv, P, n = 1, 8, 2, 16, 3000
-    q, kp, vp, table, L = _case(44, B, Hq, Hkv, P, [n], 128)
+    q, kp, vp, table, L = _case(44, B, Hq, Hkv, P, [n], d)
     ramp = torch.zeros(kp.shape[0], 1, P, 1)
     for t in range(n):
         ramp[table[0, t // P], 0, t % P, 0] = 0.5 + 12.0 * t / n
     kp = (kp.float() * ramp).to(torch.bfloat16)
     o, lse = _run(cuda_lib, q, kp, vp, table, L, 1)
-    o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(128))
+    o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(d))
     # late keys dominate (|O| ~ |v|): the rounding bound per element applies
     vmax = float(np.abs(f64(vp)).max())
     check_out_elementwise(f64(o), f64(lse), o_ref, lse_ref, vmax, "growing scores")
