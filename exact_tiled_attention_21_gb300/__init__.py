@@ -69,10 +69,16 @@ def load():
     lib.fa_bwd_workspace_bytes.restype = sz
     lib.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_fused_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.fa_bwd_fused_workspace_bytes.restype = sz
+    lib.fa_bwd_fused.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp, sz, vp]
+    lib.fa_bwd_fused.restype = i
     lib.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
     lib.fa_bwd_preprocess.restype = i
     lib.fa_bwd_dkdv.argtypes = [vp] * 8 + [i, i, i, i, i, f, i, vp]
     lib.fa_bwd_dkdv.restype = i
+    lib.fa_bwd_dkdv_pair.argtypes = [vp] * 8 + [i, i, i, i, i, f, i, vp]
+    lib.fa_bwd_dkdv_pair.restype = i
     lib.fa_bwd_dq.argtypes = [vp] * 7 + [i, i, i, i, i, f, i, vp]
     lib.fa_bwd_dq.restype = i
     lib.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i]
@@ -301,6 +307,18 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, work
                          _ptr(workspace), int(workspace_bytes), _stream(stream)), "fa_bwd")
 
 
+def fa_bwd_fused_workspace_bytes(B, H, Nq, Nk, d):
+    return load().fa_bwd_fused_workspace_bytes(B, H, Nq, Nk, d)
+
+
+def fa_bwd_fused(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace,
+                 workspace_bytes, stream=None):
+    """fa_bwd in one pass over the key tiles (dQ by fp32 reduce-adds; d = 128)."""
+    _raise(load().fa_bwd_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                               _ptr(dv), B, H, Nq, Nk, d, float(scale), int(causal), _ptr(workspace),
+                               int(workspace_bytes), _stream(stream)), "fa_bwd_fused")
+
+
 def fa_bwd_preprocess(o, dO, delta, B, H, Nq, d, stream=None):
     _raise(load().fa_bwd_preprocess(_ptr(o), _ptr(dO), _ptr(delta), B, H, Nq, d, _stream(stream)),
            "fa_bwd_preprocess")
@@ -310,6 +328,13 @@ def fa_bwd_dkdv(q, k, v, lse, delta, dO, dk, dv, B, H, Nq, Nk, d, scale, causal,
     _raise(load().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(dO), _ptr(dk),
                               _ptr(dv), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
                               _stream(stream)), "fa_bwd_dkdv")
+
+
+def fa_bwd_dkdv_pair(q, k, v, lse, delta, dO, dk, dv, B, H, Nq, Nk, d, scale, causal, stream=None):
+    """fa_bwd_dkdv on CTA pairs (cta_group::2 products; d = 128)."""
+    _raise(load().fa_bwd_dkdv_pair(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(dO), _ptr(dk),
+                                   _ptr(dv), B, H, Nq, Nk, d, float(scale), int(causal), _stream(stream)),
+           "fa_bwd_dkdv_pair")
 
 
 def fa_bwd_dq(q, k, v, lse, delta, dO, dq, B, H, Nq, Nk, d, scale, causal, stream=None):
@@ -373,15 +398,18 @@ def forward(q, k, v, scale=None, causal=False, stream=None, seqlens_q=None, seql
 
 
 def backward(q, k, v, o, lse, dO, scale=None, causal=False, stream=None, workspace=None, seqlens_q=None,
-             seqlens_k=None):
-    """dQ, dK, dV (bf16) for the forward output o / lse and upstream gradient dO."""
+             seqlens_k=None, fused=False):
+    """dQ, dK, dV (bf16) for the forward output o / lse and upstream gradient dO.
+    fused=True: fa_bwd_fused (one pass, dQ by fp32 reduce-adds; d = 128)."""
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     for t, n, s in ((q, "q", (B, H, Nq, d)), (k, "k", (B, H, Nk, d)), (v, "v", (B, H, Nk, d)),
                     (o, "o", (B, H, Nq, d)), (dO, "dO", (B, H, Nq, d))):
         _check(t, n, s)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    nbytes = fa_bwd_workspace_bytes(B, H, Nq, Nk, d)
+    if fused and (seqlens_q is not None or seqlens_k is not None):
+        raise ValueError("fused=True takes no sequence lengths")
+    nbytes = (fa_bwd_fused_workspace_bytes if fused else fa_bwd_workspace_bytes)(B, H, Nq, Nk, d)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -391,8 +419,8 @@ def backward(q, k, v, o, lse, dO, scale=None, causal=False, stream=None, workspa
         fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal,
                       workspace, workspace.numel() * workspace.element_size(), stream)
     else:
-        fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace,
-               workspace.numel() * workspace.element_size(), stream)
+        (fa_bwd_fused if fused else fa_bwd)(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal,
+                                            workspace, workspace.numel() * workspace.element_size(), stream)
     return dq, dk, dv
 
 

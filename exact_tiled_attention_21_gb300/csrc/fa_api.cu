@@ -61,13 +61,13 @@ int encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 
 // 3-D map over a contiguous (BH, N, d) bf16 tensor: dims (d, N, BH), box
 // (64, 128, 1), 128-byte swizzle (matches the MMA shared-memory descriptors).
-int make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+int make_map(CUtensorMap* m, const void* base, int BH, int N, int d, unsigned box_rows = 128) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     int st = encoder(&enc);
     if (st != FA_OK) return st;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                      es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -274,6 +274,11 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
     return bwd_ws_bytes(B, H, Nq, d);
 }
 
+size_t fa_bwd_fused_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+    if (check_shape(B, H, Nq, Nk, d) != FA_OK || d != 128) return 0;
+    return bwd_ws_bytes(B, H, Nq, d) + (((size_t)B * H * Nq * d * 4 + 255) & ~(size_t)255);
+}
+
 }  // extern "C"
 
 namespace {
@@ -296,6 +301,8 @@ int bwd_prepare(BwdLaunch* a, const void* q, const void* k, const void* v, const
     if (need_maps && (make_map(&a->map_q, q, BH, Nq, d) || make_map(&a->map_k, k, BH, Nk, d) ||
                       make_map(&a->map_v, v, BH, Nk, d) || make_map(&a->map_do, dO, BH, Nq, d)))
         return FA_ERR_CUDA;
+    if (need_maps && d == 128 && (make_map(&a->map_q2, q, BH, Nq, d, 64) || make_map(&a->map_do2, dO, BH, Nq, d, 64)))
+        return FA_ERR_CUDA;
     a->q = q;
     a->k = k;
     a->o = o;
@@ -305,6 +312,7 @@ int bwd_prepare(BwdLaunch* a, const void* q, const void* k, const void* v, const
     a->dk = dk;
     a->dv = dv;
     a->delta = const_cast<float*>(delta);
+    a->dqacc = nullptr;
     a->B = B;
     a->H = H;
     a->Nq = Nq;
@@ -324,12 +332,14 @@ int launched(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
              void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
              int window, const int* lens_q, const int* lens_k, void* workspace, size_t workspace_bytes,
-             void* stream) {
+             void* stream, bool fused = false) {
     if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     if ((lens_q && !aligned4(lens_q)) || (lens_k && !aligned4(lens_k))) return FA_ERR_ALIGNMENT;
     int st = check_shape(B, H, Nq, Nk, d);
     if (st != FA_OK) return st;
-    if (!workspace || workspace_bytes < bwd_ws_bytes(B, H, Nq, d)) return FA_ERR_WORKSPACE;
+    if (fused && d != 128) return FA_ERR_UNSUPPORTED;
+    const size_t ws_need = fused ? fa_bwd_fused_workspace_bytes(B, H, Nq, Nk, d) : bwd_ws_bytes(B, H, Nq, d);
+    if (!workspace || workspace_bytes < ws_need) return FA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
     BwdLaunch a;
     st = bwd_prepare(&a, q, k, v, o, lse, static_cast<float*>(workspace), dO, dq, dk, dv, B, H, Nq, Nk, d,
@@ -339,6 +349,11 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     a.lens_q = lens_q;
     a.lens_k = lens_k;
     cudaStream_t s = (cudaStream_t)stream;
+    if (fused) {  // the fp32 dQ accumulator follows D in the workspace
+        a.dqacc = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_ws_bytes(B, H, Nq, d));
+        if ((st = launched(launch_bwd_pre(a, s))) != FA_OK) return st;
+        return launched(launch_bwd_fused(a, s));
+    }
     if ((st = launched(launch_bwd_pre(a, s))) != FA_OK) return st;
     if ((st = launched(launch_bwd_dkdv(a, s, true))) != FA_OK) return st;
     return launched(launch_bwd_dq(a, s, true));
@@ -353,6 +368,13 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            void* workspace, size_t workspace_bytes, void* stream) {
     return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, 0, nullptr, nullptr,
                     workspace, workspace_bytes, stream);
+}
+
+int fa_bwd_fused(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                 void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, 0, nullptr, nullptr,
+                    workspace, workspace_bytes, stream, true);
 }
 
 int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
@@ -389,6 +411,18 @@ int fa_bwd_dkdv(const void* q, const void* k, const void* v, const float* lse, c
                          true);
     if (st != FA_OK) return st;
     return launched(launch_bwd_dkdv(a, (cudaStream_t)stream));
+}
+
+int fa_bwd_dkdv_pair(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                     const void* dO, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale,
+                     int causal, void* stream) {
+    if (!q || !k || !v || !lse || !delta || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
+    if (d == 64) return FA_ERR_UNSUPPORTED;  // other d: the shape check below
+    BwdLaunch a;
+    int st = bwd_prepare(&a, q, k, v, nullptr, lse, delta, dO, nullptr, dk, dv, B, H, Nq, Nk, d, scale, causal,
+                         true);
+    if (st != FA_OK) return st;
+    return launched(launch_bwd_dkdv_pair(a, (cudaStream_t)stream));
 }
 
 int fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse, const float* delta, const void* dO,

@@ -74,6 +74,9 @@ struct BwdParams {
     const int* lens_k;
     int H;
     int hc_kv, hc_q;  // heads per scheduling chunk of the dK/dV and dQ grids
+    int n_pt;         // key-tile pairs per head (CTA-pair dK/dV grid)
+    int hc_fu;        // heads per scheduling chunk of the single-pass grid
+    float* dqacc;     // single pass: fp32 dQ accumulator [BH, Nq, D]
     float scale, scale_log2;
     DevError* err;
     uint64_t timeout_ns;
@@ -115,7 +118,7 @@ constexpr int kPreRowsPerBlock = 8 * (32 / (D / 8)) * 4;
 template <int D>
 __global__ void __launch_bounds__(256)
 bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
-               float* __restrict__ delta, long long rows) {
+               float* __restrict__ delta, float* __restrict__ dqacc, long long rows) {
     constexpr int LPR = D / 8, RPW = 32 / LPR, STEPS = 4;
     // the dK/dV pass launched after this grid may set up (and load K, V) meanwhile
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -150,6 +153,12 @@ bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restr
         for (int w = LPR / 2; w >= 1; w >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
         const long long row = row0 + st * RPW;
         if (part == 0 && row < rows) delta[row] = sum;
+        // the single-pass backward accumulates dQ in fp32 here: every row starts at zero
+        if (dqacc && row < rows) {
+            float4* z = reinterpret_cast<float4*>(dqacc + row * D + part * 8);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
 }
 
@@ -221,8 +230,10 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, __nv_bfloat16* dst
     }
 }
 
-// Shared prologue: barriers, TMEM.  Returns the TMEM base.
-template <int D>
+// Shared prologue: barriers, TMEM.  Returns the TMEM base.  A CTA pair
+// allocates its columns collectively (one warp of each CTA) and both CTAs'
+// barriers are initialised before either uses the other's.
+template <int D, bool PAIR = false>
 __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t bar0, const WaitCtl& ctl,
                                               const uint32_t* counts, int nbar) {
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -234,32 +245,113 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t bar0, cons
         if ((smem_u32(smem) & 1023u) != 0) record_error(ctl, kErrTimeout, kSiteAlign, 0);
     }
     if (warp == Bwd<D>::MMA) {
-        tmem_alloc(smem_u32(tmem_slot), Bwd<D>::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), Bwd<D>::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), Bwd<D>::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();
+    else
+        __syncthreads();
     tc_fence_after();
     return *tmem_slot;
 }
 
-template <int D>
+// Every wait of the kernel is bounded, so every thread of both CTAs of a pair
+// arrives here; the collective free follows the last use of either CTA's TMEM.
+template <int D, bool PAIR = false>
 __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();
+    else
+        __syncthreads();
     tc_fence_after();
     if ((threadIdx.x >> 5) == Bwd<D>::MMA) {
         __syncwarp();
-        tmem_dealloc(tmem, Bwd<D>::TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem, Bwd<D>::TMEM_COLS);
+        else
+            tmem_dealloc(tmem, Bwd<D>::TMEM_COLS);
     }
 }
 
-// ------------------------------------------------------------------ dK, dV (KV-tile parallel)
+template <bool PAIR>
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int site) {
+    if constexpr (PAIR)
+        return mbar_wait_cl(bar, parity, ctl, site);
+    else
+        return mbar_wait(bar, parity, ctl, site);
+}
+template <bool PAIR>
+__device__ __forceinline__ bool bdrain(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int site) {
+    if constexpr (PAIR)
+        return mbar_drain_cl(bar, parity, ctl, site);
+    else
+        return mbar_drain(bar, parity, ctl, site);
+}
+// A commit of the issuing thread: in a pair it arrives on both CTAs' copies of `bar`.
+template <bool PAIR>
+__device__ __forceinline__ void bcommit(uint32_t bar) {
+    if constexpr (PAIR)
+        mma_commit_pair(bar);
+    else
+        mma_commit(bar);
+}
+
+// The pair's score products: A = this CTA's K (or V) tile, 128 keys x D; B = its
+// 64 query rows of Q (or dO) in two 64-feature quadrants (X0, X1), one M = 256
+// product over both CTAs.
+constexpr uint32_t kQuad = 64 * 128;  // one 64-row x 64-feature bf16 quadrant, 8 KB
 template <int D>
+__device__ __forceinline__ void issue_ss_pair(uint32_t d_tmem, uint32_t sA, uint32_t sB) {
+    constexpr uint32_t ID = idesc_bf16(256, 128, 0, 0);
+    const uint64_t a0 = sdesc_sw128(sA, 16, 1024), b0 = sdesc_sw128(sB, 16, 1024);
+    mma2_ss_first(d_tmem, a0, b0, ID);
+#pragma unroll
+    for (int k = 1; k < D / 16; ++k)
+        mma2_ss_acc(d_tmem, sdesc_add(a0, (k >> 2) * Bwd<D>::CHUNK + (k & 3) * 32),
+                    sdesc_add(b0, (k >> 2) * kQuad + (k & 3) * 32), ID);
+}
+// The pair's dV / dK products: A = P^T or dS^T from this CTA's TMEM (as in
+// issue_ts); B = this CTA's 64-feature half of dO (or Q) over all 128 queries
+// (quadrants Y0, Y1, back to back, MN-major): N = D over both CTAs.
+template <int D>
+__device__ __forceinline__ void issue_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint32_t sY, bool acc) {
+    constexpr uint32_t ID = idesc_bf16(256, D, 0, 1);
+    const uint64_t b0 = sdesc_sw128(sY, 2 * kQuad, 1024);
+    mma2_ts(d_tmem, a_tmem, b0, ID, acc ? 1u : 0u);
+#pragma unroll
+    for (int k = 1; k < 8; ++k) mma2_ts_acc(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), sdesc_add(b0, k * 2048), ID);
+}
+
+// ------------------------------------------------------------------ dK, dV (KV-tile parallel)
+// PAIR (d = 128): the two CTAs of a cluster take key tiles 2t and 2t + 1 of a
+// head and run every product as one M = 256 tcgen05.mma (cta_group::2) issued
+// by the even CTA.  Each CTA keeps its own K, V tile (A of the score products,
+// its 128 of the 256 rows) and loads, per query tile, the parts of Q and dO
+// that the products take from it as B.  The score products S^T = K Q^T and
+// dP^T = V dO^T split B by query rows (rank r: queries 64r..64r+63, all
+// features); dV += P^T dO and dK += dS^T Q split it by features (rank r:
+// features 64r..64r+63, all queries).  So each CTA stages four 64 x 64
+// quadrants of each operand: X0, X1 (its query rows, feature halves 0 and 1)
+// and Y0, Y1 (its feature half, query rows 0-63 and 64-127); per k-step a
+// product reads 2 KB of B from its shared memory instead of 4 KB.  The
+// barriers the issuing thread waits on are the even CTA's (the odd CTA's loads
+// and arrivals reach them through the cluster); its commits arrive on both
+// CTAs' copies.  The loop runs over the query tiles either key tile sees; a
+// tile one key tile does not see is masked out for it (P = 0).
+template <int D, bool PAIR>
 __global__ void __launch_bounds__(Bwd<D>::THREADS_DKDV, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                 const BwdParams p) {
+    static_assert(!PAIR || D == 128, "CTA pairs at d = 128");
     using C = Bwd<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw;  // 1024-aligned (checked in bwd_setup)
@@ -272,27 +364,51 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // TD, TD2: teardown of issuer 1 and 2
     const uint32_t B_KV = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_DP = bar0 + 48,
                    B_DS = bar0 + 56, B_ACC = bar0 + 64, B_TD = bar0 + 72, B_SF = bar0 + 80, B_TD2 = bar0 + 88;
-    const uint32_t counts[12] = {1, 32, 32, 2, 2, 1, 1, 256, 1, 1, 256, 1};
+    // STF: the producer's 32 lanes (of each CTA of a pair); SF, DS: every compute thread, or in a
+    // pair one elected thread per compute warp of each CTA
+    constexpr uint32_t N_STF = PAIR ? 64 : 32, N_SD = PAIR ? 16 : 256;
+    const uint32_t counts[12] = {1, N_STF, N_STF, 2, 2, 1, 1, N_SD, 1, 1, N_SD, 1};
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
-    const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 12);
+    const uint32_t tmem = bwd_setup<D, PAIR>(smem, bar0, ctl, counts, 12);
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;
+    const bool lead = rank == 0;  // the CTA whose thread issues the products
+    // a barrier the issuing thread waits on, as addressed from this CTA
+    auto lead_bar = [&](uint32_t b) { return PAIR ? mapa_shared(b, 0) : b; };
+    auto arrive_lead = [&](uint32_t b) {
+        if constexpr (PAIR)
+            mbar_arrive_cluster(mapa_shared(b, 0));
+        else
+            mbar_arrive(b);
+    };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int bh, kt;  // key tile 0 (the most query tiles when causal) first, heads in L2-sized chunks
-    chunked_order(blockIdx.x, p.n_kt, p.BH, p.hc_kv, bh, kt);
+    if constexpr (PAIR) {
+        int pt;
+        chunked_order(blockIdx.x >> 1, p.n_pt, p.BH, p.hc_kv, bh, pt);
+        kt = 2 * pt + (int)rank;
+    } else {
+        chunked_order(blockIdx.x, p.n_kt, p.BH, p.hc_kv, bh, kt);
+    }
     int nq, nk;
     bwd_seqlen(p, bh, nq, nk);
     const int off = nk - nq;
+    const int kt_lo = kt - (int)rank, kt_hi = PAIR ? kt_lo + 1 : kt;  // the key tiles sharing the loop
     int i0 = 0;
     if (p.causal) {
-        const int first_q = kt * 128 - off;  // smallest query that sees key kt*128
+        const int first_q = kt_lo * 128 - off;  // smallest query that sees key kt_lo*128
         i0 = first_q <= 0 ? 0 : first_q / 128;
     }
-    int i_end = kt * 128 < nk ? (nq + 127) / 128 : 0;  // no query tile past the sequence
-    if (p.window > 0) {  // the last query that sees the tile's last key
-        const long long qlast = (long long)kt * 128 + 127 - off + p.window - 1;
-        i_end = qlast < 0 ? 0 : (int)min((long long)i_end, qlast / 128 + 1);
-    }
+    auto tile_end = [&](int t) {  // one past the last query tile that sees key tile t
+        int e = t * 128 < nk ? (nq + 127) / 128 : 0;  // no query tile past the sequence
+        if (p.window > 0) {  // the last query that sees the tile's last key
+            const long long qlast = (long long)t * 128 + 127 - off + p.window - 1;
+            e = qlast < 0 ? 0 : (int)min((long long)e, qlast / 128 + 1);
+        }
+        return e;
+    };
+    const int i_end = max(tile_end(kt_lo), tile_end(kt_hi));
     const int n = i0 < i_end ? i_end - i0 : 0;
     const uint32_t sK = s_base + C::OFF_FIXED, sV = sK + C::TILE;
     auto sQ = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
@@ -300,10 +416,16 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     float* vec = (float*)(smem + C::OFF_VEC);  // stage s: lse2 at [s*256], delta at [s*256 + 128]
     const bool kv_issued = warp == C::PRODUCER && lane == 0 && n > 0 && !*abort_flag;
     if (kv_issued) {  // K and V do not come from the preprocess: they load before the wait for it
-        mbar_arrive_expect_tx(B_KV, 2 * C::TILE);
+        if (lead) mbar_arrive_expect_tx(B_KV, (PAIR ? 4 : 2) * C::TILE);
+        const uint32_t kvb = lead_bar(B_KV);
         for (int c = 0; c < C::KCH; ++c) {
-            tma_load_3d(sK + c * C::CHUNK, &map_k, B_KV, c * 64, kt * 128, bh, l2_policy_evict_last());
-            tma_load_3d(sV + c * C::CHUNK, &map_v, B_KV, c * 64, kt * 128, bh, l2_policy_evict_last());
+            if constexpr (PAIR) {
+                tma_load_3d_pair(sK + c * C::CHUNK, &map_k, kvb, c * 64, kt * 128, bh, l2_policy_evict_last());
+                tma_load_3d_pair(sV + c * C::CHUNK, &map_v, kvb, c * 64, kt * 128, bh, l2_policy_evict_last());
+            } else {
+                tma_load_3d(sK + c * C::CHUNK, &map_k, kvb, c * 64, kt * 128, bh, l2_policy_evict_last());
+                tma_load_3d(sV + c * C::CHUNK, &map_v, kvb, c * 64, kt * 128, bh, l2_policy_evict_last());
+            }
         }
     }
     // Launched as a programmatic dependent of the preprocess, this grid may start before D is
@@ -341,12 +463,26 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             fetch_vec(i0);
             for (int ii = 0; ii < n; ++ii) {
                 const int st = ii & 1, i = i0 + ii;
-                if (!mbar_wait(B_STE + 8 * st, ((ii >> 1) & 1) ^ 1, ctl, kSiteBwdQEmpty)) break;
+                if (!bwait<PAIR>(B_STE + 8 * st, ((ii >> 1) & 1) ^ 1, ctl, kSiteBwdQEmpty)) break;
                 if (lane == 0) {  // byte count first (no arrival), then the copies
-                    mbar_expect_tx(B_STF + 8 * st, 2 * C::TILE);
-                    for (int c = 0; c < C::KCH; ++c) {
-                        tma_load_3d(sQ(st) + c * C::CHUNK, &map_q, B_STF + 8 * st, c * 64, i * 128, bh, pol);
-                        tma_load_3d(sDO(st) + c * C::CHUNK, &map_do, B_STF + 8 * st, c * 64, i * 128, bh, pol);
+                    if (lead) mbar_expect_tx(B_STF + 8 * st, (PAIR ? 4 : 2) * C::TILE);
+                    if constexpr (PAIR) {
+                        const uint32_t fb = lead_bar(B_STF + 8 * st);
+                        const int qr = i * 128 + 64 * (int)rank, fc = 64 * (int)rank;
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const CUtensorMap* m = t ? &map_do : &map_q;
+                            const uint32_t dst = t ? sDO(st) : sQ(st);
+                            tma_load_3d_pair(dst, m, fb, 0, qr, bh, pol);                      // X0
+                            tma_load_3d_pair(dst + kQuad, m, fb, 64, qr, bh, pol);             // X1
+                            tma_load_3d_pair(dst + 2 * kQuad, m, fb, fc, i * 128, bh, pol);    // Y0
+                            tma_load_3d_pair(dst + 3 * kQuad, m, fb, fc, i * 128 + 64, bh, pol);  // Y1
+                        }
+                    } else {
+                        for (int c = 0; c < C::KCH; ++c) {
+                            tma_load_3d(sQ(st) + c * C::CHUNK, &map_q, B_STF + 8 * st, c * 64, i * 128, bh, pol);
+                            tma_load_3d(sDO(st) + c * C::CHUNK, &map_do, B_STF + 8 * st, c * 64, i * 128, bh, pol);
+                        }
                     }
                 }
 #pragma unroll
@@ -354,69 +490,86 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     vec[st * 256 + lane + 32 * t] = nl2[t];
                     vec[st * 256 + 128 + lane + 32 * t] = ndl[t];
                 }
-                mbar_arrive(B_STF + 8 * st);  // all 32 lanes, after their writes
+                arrive_lead(B_STF + 8 * st);  // all 32 lanes, after their writes
                 issued |= 1u << st;
                 issued_par = (issued_par & ~(1u << st)) | ((uint32_t)((ii >> 1) & 1) << st);
                 if (ii + 1 < n) fetch_vec(i + 1);
             }
-            if (*abort_flag && lane == 0) {  // let the loads in flight land before exit
-                if (kv_issued) mbar_drain(B_KV, 0, ctl, kSiteTeardown);
+            // let the loads in flight land before exit (in a pair, the even CTA's barriers
+            // count the odd CTA's loads too)
+            if (*abort_flag && lane == 0 && lead) {
+                if (kv_issued) bdrain<PAIR>(B_KV, 0, ctl, kSiteTeardown);
                 for (int st = 0; st < 2; ++st)
-                    if (issued & (1u << st)) mbar_drain(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
+                    if (issued & (1u << st))
+                        bdrain<PAIR>(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
             }
         }
     } else if (warp == C::MMA) {
         // ------------------------------------------------------------ MMA issuer 1: S^T
         // S^T(i) once S^T(i-1) has been read out of TMEM and stage i is loaded
-        if (lane == 0 && !*abort_flag && n > 0) {
-            bool ok = mbar_wait(B_KV, 0, ctl, kSiteBwdKvFull);
+        if (lane == 0 && lead && !*abort_flag && n > 0) {
+            bool ok = bwait<PAIR>(B_KV, 0, ctl, kSiteBwdKvFull);
             for (int ii = 0; ii < n && ok; ++ii) {
                 const int st = ii & 1;
-                if (ii > 0 && !(ok = mbar_wait(B_SF, (ii - 1) & 1, ctl, kSiteBwdS))) break;
-                if (!(ok = mbar_wait(B_STF + 8 * st, (ii >> 1) & 1, ctl, kSiteBwdQFull))) break;
+                if (ii > 0 && !(ok = bwait<PAIR>(B_SF, (ii - 1) & 1, ctl, kSiteBwdS))) break;
+                if (!(ok = bwait<PAIR>(B_STF + 8 * st, (ii >> 1) & 1, ctl, kSiteBwdQFull))) break;
                 tc_fence_after();
-                issue_ss<D>(tmem + C::COL_A, sK, sQ(st));
-                mma_commit(B_S);
-                mma_commit(B_STE + 8 * st);
+                if constexpr (PAIR)
+                    issue_ss_pair<D>(tmem + C::COL_A, sK, sQ(st));
+                else
+                    issue_ss<D>(tmem + C::COL_A, sK, sQ(st));
+                bcommit<PAIR>(B_S);
+                bcommit<PAIR>(B_STE + 8 * st);
             }
             if (*abort_flag) {
-                mma_commit(B_TD);
-                mbar_drain(B_TD, 0, ctl, kSiteTeardown);
+                bcommit<PAIR>(B_TD);
+                bdrain<PAIR>(B_TD, 0, ctl, kSiteTeardown);
             }
         }
     } else if (warp == C::MMA2) {
         // ------------------------------------------------------------ MMA issuer 2: dP^T, dV, dK
         // dV(i) and dK(i) once P^T(i) and dS^T(i) are in TMEM; dP^T(i+1) over them (this
         // thread's products run in issue order, so it overwrites them only after both)
-        if (lane == 0 && !*abort_flag && n > 0) {
-            bool ok = mbar_wait(B_KV, 0, ctl, kSiteBwdKvFull);
-            if (ok) ok = mbar_wait(B_STF, 0, ctl, kSiteBwdQFull);
+        if (lane == 0 && lead && !*abort_flag && n > 0) {
+            bool ok = bwait<PAIR>(B_KV, 0, ctl, kSiteBwdKvFull);
+            if (ok) ok = bwait<PAIR>(B_STF, 0, ctl, kSiteBwdQFull);
             if (ok) {
                 tc_fence_after();
-                issue_ss<D>(tmem + C::COL_B, sV, sDO(0));
-                mma_commit(B_DP);
+                if constexpr (PAIR)
+                    issue_ss_pair<D>(tmem + C::COL_B, sV, sDO(0));
+                else
+                    issue_ss<D>(tmem + C::COL_B, sV, sDO(0));
+                bcommit<PAIR>(B_DP);
             }
             for (int ii = 0; ii < n && ok; ++ii) {
                 const int st = ii & 1;
-                if (!(ok = mbar_wait(B_DS, ii & 1, ctl, kSiteBwdDS))) break;
+                if (!(ok = bwait<PAIR>(B_DS, ii & 1, ctl, kSiteBwdDS))) break;
                 tc_fence_after();
-                issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sDO(st), ii > 0);      // dV += P^T dO
-                issue_ts<D>(tmem + C::COL_ACC1, tmem + C::COL_B + 32, sQ(st), ii > 0);  // dK += dS^T Q
-                mma_commit(B_STE + 8 * st);
+                if constexpr (PAIR) {
+                    issue_ts_pair<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sDO(st) + 2 * kQuad, ii > 0);      // dV
+                    issue_ts_pair<D>(tmem + C::COL_ACC1, tmem + C::COL_B + 32, sQ(st) + 2 * kQuad, ii > 0);  // dK
+                } else {
+                    issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sDO(st), ii > 0);      // dV += P^T dO
+                    issue_ts<D>(tmem + C::COL_ACC1, tmem + C::COL_B + 32, sQ(st), ii > 0);  // dK += dS^T Q
+                }
+                bcommit<PAIR>(B_STE + 8 * st);
                 if (ii + 1 < n) {
-                    if (!(ok = mbar_wait(B_STF + 8 * (st ^ 1), ((ii + 1) >> 1) & 1, ctl, kSiteBwdQFull))) break;
+                    if (!(ok = bwait<PAIR>(B_STF + 8 * (st ^ 1), ((ii + 1) >> 1) & 1, ctl, kSiteBwdQFull))) break;
                     tc_fence_after();
-                    issue_ss<D>(tmem + C::COL_B, sV, sDO(st ^ 1));  // dP^T of the next query tile
-                    mma_commit(B_DP);
+                    if constexpr (PAIR)
+                        issue_ss_pair<D>(tmem + C::COL_B, sV, sDO(st ^ 1));
+                    else
+                        issue_ss<D>(tmem + C::COL_B, sV, sDO(st ^ 1));  // dP^T of the next query tile
+                    bcommit<PAIR>(B_DP);
                 }
             }
-            if (ok) mma_commit(B_ACC);
+            if (ok) bcommit<PAIR>(B_ACC);
             if (*abort_flag) {
-                mma_commit(B_TD2);
-                mbar_drain(B_TD2, 0, ctl, kSiteTeardown);
+                bcommit<PAIR>(B_TD2);
+                bdrain<PAIR>(B_TD2, 0, ctl, kSiteTeardown);
             }
         }
-    } else {
+    } else if (warp < C::PRODUCER) {
         // ------------------------------------------------------------ P^T, dS^T, epilogue
         // Two warpgroups: warpgroup h handles query columns [64h, 64h + 64) of every key row.
         const int h = warp >> 2;
@@ -427,6 +580,21 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t colA = C::COL_A + 64 * h, colB = C::COL_B + 64 * h;
         const float sc = p.scale_log2;
+        // in a pair every wait is made warp-uniform (the TMEM loads that follow are warp-collective),
+        // and each warp's arrival is one elected thread's, after the warp's TMEM accesses
+        auto wait_c = [&](uint32_t b, uint32_t par, int site) {
+            bool w = bwait<PAIR>(b, par, ctl, site);
+            if constexpr (PAIR) w = __all_sync(0xffffffffu, w);
+            return w;
+        };
+        auto arrive_c = [&](uint32_t b) {
+            if constexpr (PAIR) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(b, 0));
+            } else {
+                mbar_arrive(b);
+            }
+        };
         bool ok = true;
         for (int ii = 0; ii < n; ++ii) {
             const int st = ii & 1, i = i0 + ii;
@@ -434,7 +602,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const float* dl = l2 + 128;
             // key kg is visible to query q iff kg <= q + off, i.e. column c >= cmin
             const int cmin = p.causal ? kg - off - i * 128 - 64 * h : -1;
-            if (!(ok = mbar_wait(B_S, ii & 1, ctl, kSiteBwdS))) break;
+            if (!(ok = wait_c(B_S, ii & 1, kSiteBwdS))) break;
             tc_fence_after();
             uint32_t pp[32];
             uint32_t va[32], vb[32];
@@ -444,7 +612,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             tmem_wait_ld(va);
             tmem_wait_ld(vb);
             tc_fence_before();
-            mbar_arrive(B_SF);
+            arrive_c(B_SF);
             // masked entries: rows past Nk (whole row) and, causal, columns c < cmin.
             // Tiles with none in the warp take the instantiation without the test.
             const int cmin_eff = key_ok ? cmin : (1 << 30);
@@ -478,7 +646,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 p_phase(std::true_type{});
             else
                 p_phase(std::false_type{});
-            if (!(ok = mbar_wait(B_DP, ii & 1, ctl, kSiteBwdDP))) break;
+            if (!(ok = wait_c(B_DP, ii & 1, kSiteBwdDP))) break;
             tc_fence_after();
             // this warpgroup's 64 dP^T columns; once both chunks are in registers, its bf16 P^T
             // goes over the first 32 of them and dS^T over the last 32
@@ -508,12 +676,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(B_DS);
+            arrive_c(B_DS);
         }
         if (ok) {
             bool have = n > 0;
             if (have) {
-                ok = mbar_wait(B_ACC, 0, ctl, kSiteBwdDone);
+                ok = wait_c(B_ACC, 0, kSiteBwdDone);
                 tc_fence_after();
             }
             if (ok) {
@@ -523,7 +691,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
         }
     }
-    bwd_teardown<D>(tmem);
+    if constexpr (PAIR) {  // a CTA that gave up stops its partner's waits too
+        if (tid == 0 && *abort_flag) st_cluster_u32(mapa_shared(smem_u32((const void*)abort_flag), rank ^ 1u), 1u);
+    }
+    bwd_teardown<D, PAIR>(tmem);
 }
 
 // ------------------------------------------------------------------ dQ (Q-tile parallel)
@@ -748,6 +919,426 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ single pass: dK, dV and dQ
+// One CTA per (b, h, 128-key tile), as the dK/dV pass, over query tiles of 64
+// rows, with the fifth product in the same pass: dQ_i += scale dS_ij K_j is
+// computed as its transpose dQ^T = K^T dS^T (M = the 128 features, N = 64
+// queries, K = the 128 keys), staged in shared memory as [64 queries][128
+// features] fp32 and added to an fp32 accumulator in global memory by one bulk
+// reduce-add (cp.reduce.async.bulk ... add.f32: the tile's rows are contiguous
+// there too) per tile, so no pass recomputes S and dP for dQ.  dS^T is staged
+// once in shared memory ([128 keys][64 queries] bf16, 128-byte swizzle), where
+// it is both the K-major A operand of dK += dS^T Q and the MN-major B operand
+// of dQ^T; K^T is the resident K tile read MN-major.  The order of the fp32
+// additions into dQ varies from run to run (the result does not otherwise).
+//   TMEM: S^T 64 | dP^T two buffers x 64 (P^T bf16 over each) | dQ^T 64 | dV 128 | dK 128
+//   issuer 1 (warp 9): S^T(i) once S^T(i-1) has been read out.
+//   issuer 2 (warp 10): dP^T(i+1) into buffer (i+1) & 1 as soon as its stage is
+//     loaded (P^T(i-1) there was read by dV(i-1), issued before it: this
+//     thread's products run in issue order); then dV(i), dK(i) once P^T(i),
+//     dS^T(i) are written; then dQ^T(i) once the compute threads have read
+//     dQ^T(i-1) out.  So the next tile's dP^T never waits for this tile's
+//     dV and dK.
+//   compute (warps 0-7, thread = key row; warpgroup h: query columns 32h..32h+31):
+//     P phase, dS phase (P^T to TMEM, dS^T to shared memory), then the read-out
+//     of dQ^T(i-1) (thread = feature row) into the staging tile, whose
+//     reduce-add one of them then issues; dV, dK epilogue.
+struct Fu {
+    static constexpr int D = 128;
+    static constexpr int BQ = 64;                    // query rows per tile
+    static constexpr int NST = 3;                    // Q / dO stages
+    static constexpr int KV_TILE = 128 * D * 2;      // 32 KB
+    static constexpr int CHUNK = 128 * 128;          // 64 features x 128 keys
+    static constexpr int QT = BQ * D * 2;            // one Q or dO tile, 16 KB
+    static constexpr int QCH = BQ * 128;             // 64 features x 64 rows
+    static constexpr int OFF_K = 0, OFF_V = KV_TILE;
+    static constexpr int OFF_ST = 2 * KV_TILE;       // stage s: Q at + 2s QT, dO after it
+    static constexpr int DS_BYTES = 128 * BQ * 2;    // dS^T [128 keys][64 queries] bf16
+    static constexpr int OFF_DS = OFF_ST + NST * 2 * QT;  // two dS^T buffers
+    static constexpr int OFF_DQS = OFF_DS + 2 * DS_BYTES;  // dQ staging [64 queries][128 features] fp32
+    static constexpr int OFF_VEC = OFF_DQS + BQ * D * 4;   // stage s: 64 lse2 at [128 s], 64 delta after
+    static constexpr int OFF_BAR = OFF_VEC + NST * 2 * BQ * 4;
+    static constexpr int NBAR = 21;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 16;
+    static constexpr int THREADS = 352;
+    static constexpr int PRODUCER = 8, MMA = 9, MMA2 = 10;
+    static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DQ = 192, COL_DV = 256, COL_DK = 384;  // dP^T b at 64 + 64 b
+    static constexpr uint32_t ID_S = idesc_bf16(128, BQ, 0, 0);    // S^T, dP^T: K-major A and B
+    static constexpr uint32_t ID_VK = idesc_bf16(128, D, 0, 1);    // dV, dK: B (dO, Q) MN-major
+    static constexpr uint32_t ID_Q = idesc_bf16(128, BQ, 1, 1);    // dQ^T: K^T and dS^T both MN-major
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(OFF_ST % 1024 == 0 && OFF_DS % 1024 == 0 && OFF_DQS % 128 == 0, "tile alignment");
+};
+
+__global__ void __launch_bounds__(Fu::THREADS, 1)
+bwd_fused_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                 const BwdParams p) {
+    using C = Fu;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw;
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t bar0 = s_base + C::OFF_BAR;
+    const uint32_t B_KV = bar0, B_STF = bar0 + 8, B_STE = bar0 + 32, B_S = bar0 + 56, B_SF = bar0 + 64,
+                   B_DP = bar0 + 72, B_DS = bar0 + 88, B_DSF = bar0 + 96, B_DQ = bar0 + 112, B_QF = bar0 + 120,
+                   B_ACC = bar0 + 128, B_TD = bar0 + 136, B_TD2 = bar0 + 144, B_QSF = bar0 + 152,
+                   B_QSW = bar0 + 160;
+    // KV, STF[3] (producer lanes), STE[3] (both issuers), S, SF (compute threads), DP[2], DS
+    // (compute), DSF[2], DQ, QF (compute), ACC, TD, TD2, QSF (dQ staging free: thread 0),
+    // QSW (dQ staging written: compute threads)
+    const uint32_t counts[C::NBAR] = {1, 32, 32, 32, 2, 2, 2, 1, 256, 1, 1, 256, 1, 1, 1, 256, 1, 1, 1, 1, 256};
+    uint32_t* tmem_slot = (uint32_t*)(smem + C::OFF_MISC);
+    volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
+    const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int b = 0; b < C::NBAR; ++b) mbar_init(bar0 + 8 * b, counts[b]);
+        fence_mbar_init();
+        if ((s_base & 1023u) != 0) record_error(ctl, kErrTimeout, kSiteAlign, 0);
+    }
+    if (warp == C::MMA) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int bh, kt;  // key tile 0 (the most query tiles when causal) first, heads in L2-sized chunks
+    chunked_order(blockIdx.x, p.n_kt, p.BH, p.hc_fu, bh, kt);
+    int nq, nk;
+    bwd_seqlen(p, bh, nq, nk);
+    const int off = nk - nq;
+    int i0 = 0;
+    if (p.causal) {
+        const int first_q = kt * 128 - off;  // smallest query that sees key kt*128
+        i0 = first_q <= 0 ? 0 : first_q / C::BQ;
+    }
+    int i_end = kt * 128 < nk ? (nq + C::BQ - 1) / C::BQ : 0;
+    if (p.window > 0) {
+        const long long qlast = (long long)kt * 128 + 127 - off + p.window - 1;
+        i_end = qlast < 0 ? 0 : (int)min((long long)i_end, qlast / C::BQ + 1);
+    }
+    const int n = i0 < i_end ? i_end - i0 : 0;
+    const uint32_t sK = s_base + C::OFF_K, sV = s_base + C::OFF_V;
+    auto sQ = [&](int st) { return s_base + C::OFF_ST + st * 2 * C::QT; };
+    auto sDO = [&](int st) { return s_base + C::OFF_ST + st * 2 * C::QT + C::QT; };
+    auto sDS = [&](int b) { return s_base + C::OFF_DS + b * C::DS_BYTES; };
+    float* vec = (float*)(smem + C::OFF_VEC);
+    const bool kv_issued = warp == C::PRODUCER && lane == 0 && n > 0 && !*abort_flag;
+    if (kv_issued) {  // K and V do not come from the preprocess: they load before the wait for it
+        mbar_arrive_expect_tx(B_KV, 2 * C::KV_TILE);
+        for (int c = 0; c < 2; ++c) {
+            tma_load_3d(sK + c * C::CHUNK, &map_k, B_KV, c * 64, kt * 128, bh, l2_policy_evict_last());
+            tma_load_3d(sV + c * C::CHUNK, &map_v, B_KV, c * 64, kt * 128, bh, l2_policy_evict_last());
+        }
+    }
+    // D and the zeroed dQ accumulator come from the preprocess
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp == C::PRODUCER) {
+        // ------------------------------------------------------------ producer (whole warp)
+        if (!*abort_flag && n > 0) {
+            const uint64_t pol = l2_policy_evict_last();
+            if (lane == 0) {
+                tma_prefetch_desc(&map_q);
+                tma_prefetch_desc(&map_do);
+            }
+            uint32_t issued = 0, issued_par = 0;
+            float nl2[2], ndl[2];
+            auto fetch_vec = [&](int i) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int q = i * C::BQ + lane + 32 * t;
+                    nl2[t] = INFINITY;
+                    ndl[t] = 0.f;
+                    if (q < nq) {
+                        const float L = p.lse[(size_t)bh * p.Nq + q];
+                        nl2[t] = (L == -INFINITY) ? INFINITY : L * kLog2e;
+                        ndl[t] = p.delta[(size_t)bh * p.Nq + q];
+                    }
+                }
+            };
+            fetch_vec(i0);
+            for (int ii = 0; ii < n; ++ii) {
+                const int st = ii % C::NST, i = i0 + ii;
+                const uint32_t use = (uint32_t)(ii / C::NST);
+                if (!mbar_wait(B_STE + 8 * st, (use & 1) ^ 1, ctl, kSiteBwdQEmpty)) break;
+                if (lane == 0) {
+                    mbar_expect_tx(B_STF + 8 * st, 2 * C::QT);
+                    for (int c = 0; c < 2; ++c) {
+                        tma_load_3d(sQ(st) + c * C::QCH, &map_q, B_STF + 8 * st, c * 64, i * C::BQ, bh, pol);
+                        tma_load_3d(sDO(st) + c * C::QCH, &map_do, B_STF + 8 * st, c * 64, i * C::BQ, bh, pol);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    vec[st * 128 + lane + 32 * t] = nl2[t];
+                    vec[st * 128 + 64 + lane + 32 * t] = ndl[t];
+                }
+                mbar_arrive(B_STF + 8 * st);
+                issued |= 1u << st;
+                issued_par = (issued_par & ~(1u << st)) | ((use & 1) << st);
+                if (ii + 1 < n) fetch_vec(i + 1);
+            }
+            if (*abort_flag && lane == 0) {
+                if (kv_issued) mbar_drain(B_KV, 0, ctl, kSiteTeardown);
+                for (int st = 0; st < C::NST; ++st)
+                    if (issued & (1u << st)) mbar_drain(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
+            }
+        }
+    } else if (warp == C::MMA) {
+        // ------------------------------------------------------------ issuer 1: S^T
+        if (lane == 0 && !*abort_flag && n > 0) {
+            bool ok = mbar_wait(B_KV, 0, ctl, kSiteBwdKvFull);
+            for (int ii = 0; ii < n && ok; ++ii) {
+                const int st = ii % C::NST;
+                if (ii >= 1 && !(ok = mbar_wait(B_SF, (ii - 1) & 1, ctl, kSiteBwdS))) break;
+                if (!(ok = mbar_wait(B_STF + 8 * st, (ii / C::NST) & 1, ctl, kSiteBwdQFull))) break;
+                tc_fence_after();
+                const uint64_t a0 = sdesc_sw128(sK, 16, 1024), b0 = sdesc_sw128(sQ(st), 16, 1024);
+                const uint32_t d = tmem + C::COL_S;
+                mma_ss_first(d, a0, b0, C::ID_S);
+#pragma unroll
+                for (int k = 1; k < 8; ++k)
+                    mma_ss_acc(d, sdesc_add(a0, (k >> 2) * C::CHUNK + (k & 3) * 32),
+                               sdesc_add(b0, (k >> 2) * C::QCH + (k & 3) * 32), C::ID_S);
+                mma_commit(B_S);
+                mma_commit(B_STE + 8 * st);
+            }
+            if (*abort_flag) {
+                mma_commit(B_TD);
+                mbar_drain(B_TD, 0, ctl, kSiteTeardown);
+            }
+        }
+    } else if (warp == C::MMA2) {
+        // ------------------------------------------------------------ issuer 2: dP^T, dV, dK, dQ^T
+        if (lane == 0 && !*abort_flag && n > 0) {
+            auto issue_dp = [&](int jj) {  // dP^T of tile jj into buffer jj & 1, once its stage is loaded
+                const int st = jj % C::NST;
+                if (!mbar_wait(B_STF + 8 * st, (jj / C::NST) & 1, ctl, kSiteBwdQFull)) return false;
+                tc_fence_after();
+                const uint64_t a0 = sdesc_sw128(sV, 16, 1024), b0 = sdesc_sw128(sDO(st), 16, 1024);
+                const uint32_t d = tmem + C::COL_DP + 64 * (jj & 1);
+                mma_ss_first(d, a0, b0, C::ID_S);
+#pragma unroll
+                for (int k = 1; k < 8; ++k)
+                    mma_ss_acc(d, sdesc_add(a0, (k >> 2) * C::CHUNK + (k & 3) * 32),
+                               sdesc_add(b0, (k >> 2) * C::QCH + (k & 3) * 32), C::ID_S);
+                mma_commit(B_DP + 8 * (jj & 1));
+                return true;
+            };
+            bool ok = mbar_wait(B_KV, 0, ctl, kSiteBwdKvFull);
+            if (ok) ok = issue_dp(0);
+            for (int ii = 0; ii < n && ok; ++ii) {
+                const int st = ii % C::NST, b = ii & 1;
+                if (ii + 1 < n && !(ok = issue_dp(ii + 1))) break;
+                if (!(ok = mbar_wait(B_DS, ii & 1, ctl, kSiteBwdDS))) break;
+                tc_fence_after();
+                const bool acc = ii > 0;
+                {   // dV += P^T dO: A = P^T (TMEM; k-step k = queries 16k.., warpgroup k / 2's
+                    // columns), B = dO MN-major (64-feature blocks 8 KB apart, 16 rows per k-step)
+                    const uint64_t bv = sdesc_sw128(sDO(st), C::QCH, 1024);
+                    const uint64_t bq = sdesc_sw128(sQ(st), C::QCH, 1024);
+                    const uint64_t ad = sdesc_sw128(sDS(b), 16, 1024);  // dS^T K-major: 16 queries per k-step
+                    const uint32_t pcol = tmem + C::COL_DP + 64 * b;
+                    mma_ts(tmem + C::COL_DV, pcol, bv, C::ID_VK, acc ? 1u : 0u);
+#pragma unroll
+                    for (int k = 1; k < 4; ++k)
+                        mma_ts_acc(tmem + C::COL_DV, pcol + 32 * (k >> 1) + 8 * (k & 1), sdesc_add(bv, k * 2048),
+                                   C::ID_VK);
+                    // dK += dS^T Q: A = dS^T from shared memory (K-major), B = Q MN-major
+                    mma_ss(tmem + C::COL_DK, ad, bq, C::ID_VK, acc ? 1u : 0u);
+#pragma unroll
+                    for (int k = 1; k < 4; ++k)
+                        mma_ss_acc(tmem + C::COL_DK, sdesc_add(ad, k * 32), sdesc_add(bq, k * 2048), C::ID_VK);
+                }
+                mma_commit(B_STE + 8 * st);
+                // dQ^T(ii) = K^T dS^T once dQ^T(ii-1) has been read out: A = K MN-major (feature
+                // blocks 16 KB apart, 16 keys per k-step), B = dS^T MN-major (16 keys per k-step)
+                if (ii > 0 && !(ok = mbar_wait(B_QF, (ii - 1) & 1, ctl, kSiteBwdDQ))) break;
+                tc_fence_after();
+                {
+                    const uint64_t ak = sdesc_sw128(sK, C::CHUNK, 1024), bs = sdesc_sw128(sDS(b), 8192, 1024);
+                    mma_ss_first(tmem + C::COL_DQ, ak, bs, C::ID_Q);
+#pragma unroll
+                    for (int k = 1; k < 8; ++k)
+                        mma_ss_acc(tmem + C::COL_DQ, sdesc_add(ak, k * 2048), sdesc_add(bs, k * 2048), C::ID_Q);
+                }
+                mma_commit(B_DQ);
+                mma_commit(B_DSF + 8 * b);
+            }
+            if (ok) mma_commit(B_ACC);
+            if (*abort_flag) {
+                mma_commit(B_TD2);
+                mbar_drain(B_TD2, 0, ctl, kSiteTeardown);
+            }
+        }
+    } else if (warp < C::PRODUCER) {
+        // ------------------------------------------------------------ compute: P, dS, dQ read-out, epilogue
+        const int h = warp >> 2;
+        const int r = ((warp & 3) << 5) + lane;  // key row (TMEM lane) = feature row of dQ^T
+        const int kg = kt * 128 + r;
+        const bool row_ok = kg < p.Nk;
+        const bool key_ok = kg < nk;
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const float sc = p.scale_log2;
+        uint8_t* ds_row = smem + C::OFF_DS + r * 128;  // row r of a dS^T buffer (+ b * DS_BYTES)
+        float* dqs = reinterpret_cast<float*>(smem + C::OFF_DQS) + r;  // column r of the dQ staging tile
+        auto read_dq = [&](int jj) {  // dQ^T of tile jj: this thread's feature r, queries 32h..32h+31
+            bool w = mbar_wait(B_DQ, jj & 1, ctl, kSiteBwdDQ);
+            if (!__all_sync(0xffffffffu, w)) return false;  // every lane votes: the TMEM load is warp-collective
+            tc_fence_after();
+            uint32_t v[32];
+            tmem_ld32(lane_addr + C::COL_DQ + 32 * h, v);
+            tc_fence_before();
+            mbar_arrive(B_QF);  // dQ^T(jj + 1) may be issued over it
+            // the staging tile is free once the previous reduce-add has read it (thread 0 issued
+            // it and waits for its reads; every handshake here is a bounded mbarrier wait)
+            if (tid == 0) {
+                bulk_wait_group_read0();
+                mbar_arrive(B_QSF);
+            }
+            w = mbar_wait(B_QSF, jj & 1, ctl, kSiteBwdDQ);
+            if (!__all_sync(0xffffffffu, w)) return false;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) dqs[(32 * h + c) * C::D] = __uint_as_float(v[c]);  // a warp: one 128-byte row
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(B_QSW);
+            bool issued = true;
+            if (tid == 0) {  // rows past Nq are not added (they belong to the next head); rows past a
+                             // shorter sequence hold zeros (P = 0 there)
+                issued = mbar_wait(B_QSW, jj & 1, ctl, kSiteBwdDQ);
+                const int q0 = (i0 + jj) * C::BQ;
+                const int rows = min(C::BQ, p.Nq - q0);
+                if (issued && (rows <= 0 || bh >= p.BH)) {  // never: the tile range stays inside the head
+                    record_error(ctl, kErrInvalid, kSiteBwdDQ, q0);
+                    issued = false;
+                }
+                if (issued) {
+                    bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.Nq + q0) * C::D, s_base + C::OFF_DQS,
+                                        (uint32_t)rows * C::D * 4);
+                    bulk_commit_group();
+                }
+            }
+            return __all_sync(0xffffffffu, issued) != 0;  // the same answer in every lane of the warp
+        };
+        bool ok = true;
+        for (int ii = 0; ii < n; ++ii) {
+            const int b = ii & 1, st = ii % C::NST, i = i0 + ii;
+            const float* l2 = vec + st * 128 + 32 * h;
+            const float* dl = l2 + 64;
+            const int cmin = p.causal ? kg - off - i * C::BQ - 32 * h : -1;  // visible iff column c >= cmin
+            ok = mbar_wait(B_S, ii & 1, ctl, kSiteBwdS);
+            if (!__all_sync(0xffffffffu, ok)) break;  // every lane votes: the TMEM loads are warp-collective
+            tc_fence_after();
+            uint32_t va[32], pp[16];
+            tmem_ld32(lane_addr + C::COL_S + 32 * h, va);
+            tc_fence_before();
+            mbar_arrive(B_SF);
+            const int cmin_eff = key_ok ? cmin : (1 << 30);
+            const int cmax_w = p.window > 0 ? kg - off + p.window - 1 - i * C::BQ - 32 * h : (1 << 30);
+            auto p_phase = [&](auto MASK) {
+                float lv[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 t = reinterpret_cast<const float4*>(l2)[e];
+                    lv[4 * e] = t.x, lv[4 * e + 1] = t.y, lv[4 * e + 2] = t.z, lv[4 * e + 3] = t.w;
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int c0 = 2 * e;
+                    const float2 x = ffma2(make_float2(__uint_as_float(va[2 * e]), __uint_as_float(va[2 * e + 1])),
+                                           make_float2(sc, sc), make_float2(-lv[2 * e], -lv[2 * e + 1]));
+                    float a = ex2(x.x), bb = ex2(x.y);
+                    if constexpr (decltype(MASK)::value) {
+                        if (c0 < cmin_eff || c0 > cmax_w) a = 0.f;
+                        if (c0 + 1 < cmin_eff || c0 + 1 > cmax_w) bb = 0.f;
+                    }
+                    pp[e] = pack_bf16(a, bb);
+                }
+            };
+            if (__any_sync(0xffffffffu, cmin_eff > 0 || cmax_w < 31))
+                p_phase(std::true_type{});
+            else
+                p_phase(std::false_type{});
+            // the dS^T buffer of this tile is free once dK and dQ^T of tile ii - 2 are done
+            ok = ii < 2 || mbar_wait(B_DSF + 8 * b, ((ii >> 1) & 1) ^ 1, ctl, kSiteBwdDS);
+            if (ok) ok = mbar_wait(B_DP + 8 * b, (ii >> 1) & 1, ctl, kSiteBwdDP);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            tmem_ld32(lane_addr + C::COL_DP + 64 * b + 32 * h, va);
+            tmem_st16_async(lane_addr + C::COL_DP + 64 * b + 32 * h, pp);  // P^T over the dP^T columns just read
+            {
+                float dv[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 t = reinterpret_cast<const float4*>(dl)[e];
+                    dv[4 * e] = t.x, dv[4 * e + 1] = t.y, dv[4 * e + 2] = t.z, dv[4 * e + 3] = t.w;
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const uint32_t pr = pp[e];
+                    pk[e] = pack_bf16(bf_lo(pr) * (__uint_as_float(va[2 * e]) - dv[2 * e]),
+                                      bf_hi(pr) * (__uint_as_float(va[2 * e + 1]) - dv[2 * e + 1]));
+                }
+                // dS^T row r, queries 32h..32h+31: 16-byte chunks 4h..4h+3, swizzled by row
+                uint8_t* row = ds_row + b * C::DS_BYTES;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4*>(row + (((4 * h + u) ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(B_DS);
+            if (ii > 0 && !(ok = read_dq(ii - 1))) break;
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && n > 0) ok = read_dq(n - 1);
+        if (ok) {
+            const bool have = n > 0;
+            if (have) {
+                ok = mbar_wait(B_ACC, 0, ctl, kSiteBwdDone);
+                tc_fence_after();
+            }
+            if (ok) {
+                const size_t base = ((size_t)bh * p.Nk + (row_ok ? kg : 0)) * C::D;
+                store_acc_row<128>(lane_addr + C::COL_DV, p.dv + base, 1.f, row_ok, !have, h * 64);
+                store_acc_row<128>(lane_addr + C::COL_DK, p.dk + base, p.scale, row_ok, !have, h * 64);
+            }
+        }
+    }
+    if (tid == 0) bulk_wait_group0();  // the last reduce-add has landed before the grid completes
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == C::MMA) {
+        __syncwarp();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// dQ = bf16(scale * dQacc): 8 elements per thread and step (two 16-byte loads,
+// one 16-byte store).  Launched as a programmatic dependent of the single pass.
+__global__ void __launch_bounds__(256)
+bwd_dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long long n8, float scale) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+        const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+        const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+        reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
+                                                     pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
+    }
+}
+
 BwdParams make_params(const BwdLaunch& a) {
     BwdParams p;
     p.q = (const __nv_bfloat16*)a.q;
@@ -773,6 +1364,10 @@ BwdParams make_params(const BwdLaunch& a) {
     p.hc_q = (int)std::max(1ll, std::min((long long)p.BH, budget / per_q));
     p.n_qt = (a.Nq + 127) / 128;
     p.n_kt = (a.Nk + 127) / 128;
+    p.n_pt = (p.n_kt + 1) / 2;
+    const long long per_fu = (long long)a.Nq * a.d * 8;  // Q, dO bf16 and the fp32 dQ rows of a head
+    p.hc_fu = (int)std::max(1ll, std::min((long long)p.BH, budget / per_fu));
+    p.dqacc = a.dqacc;
     p.scale = a.scale;
     p.scale_log2 = a.scale * kLog2e;
     p.err = a.err;
@@ -793,30 +1388,45 @@ cudaError_t launch_pre_d(const BwdLaunch& a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_pre_kernel<D>, (const __nv_bfloat16*)a.o,
-                                             (const __nv_bfloat16*)a.dO, a.delta, rows);
+                                             (const __nv_bfloat16*)a.dO, a.delta, a.dqacc, rows);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // after_pre: launched right after the preprocess on the same stream, as its
 // programmatic dependent (setup and the K/V loads overlap the preprocess's end).
-template <int D>
+// PAIR (d = 128): CTA pairs (clusters of two; a key tile past Nk pads an odd
+// count) instead of single CTAs.
+template <int D, bool PAIR>
 cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t s, bool after_pre) {
     using C = Bwd<D>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
-    cudaError_t e = set_smem_limit_once<bwd_dkdv_kernel<D>>(C::SMEM);
+    cudaError_t e = set_smem_limit_once<bwd_dkdv_kernel<D, PAIR>>(C::SMEM);
     if (e != cudaSuccess) return e;
     const BwdParams p = make_params(a);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.n_kt * p.BH));
+    cfg.gridDim = dim3((unsigned)(PAIR ? 2 * p.n_pt * p.BH : p.n_kt * p.BH));
     cfg.blockDim = dim3(C::THREADS_DKDV);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (PAIR) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (after_pre) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = after_pre ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<D>, a.map_q, a.map_k, a.map_v, a.map_do, p);
+    cfg.numAttrs = na;
+    // the pair's Q and dO maps load 64-row quadrants
+    e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<D, PAIR>, PAIR ? a.map_q2 : a.map_q, a.map_k, a.map_v,
+                           PAIR ? a.map_do2 : a.map_do, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -844,13 +1454,34 @@ cudaError_t launch_dq_d(const BwdLaunch& a, cudaStream_t s, bool after_dkdv) {
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// The single pass after the preprocess (programmatic dependent), then the dQ
+// conversion after it.  d = 128.
+cudaError_t launch_fused_d(const BwdLaunch& a, cudaStream_t s) {
+    cudaError_t e = set_smem_limit_once<bwd_fused_kernel>(Fu::SMEM);
+    if (e != cudaSuccess) return e;
+    const BwdParams p = make_params(a);
+    e = launch_dependent(bwd_fused_kernel, dim3((unsigned)(p.n_kt * p.BH)), dim3(Fu::THREADS), Fu::SMEM, s,
+                         a.map_q2, a.map_k, a.map_v, a.map_do2, p);
+    if (e != cudaSuccess) return e;
+    const long long n8 = (long long)a.B * a.H * a.Nq * a.d / 8;
+    const long long blocks = std::min<long long>((n8 + 255) / 256, (long long)a.num_sms * 8);
+    return launch_dependent(bwd_dq_convert_kernel, dim3((unsigned)std::max(1ll, blocks)), dim3(256), 0, s,
+                            (const float*)a.dqacc, (__nv_bfloat16*)a.dq, n8, a.scale);
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s) {
     return a.d == 128 ? launch_pre_d<128>(a, s) : launch_pre_d<64>(a, s);
 }
 cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s, bool after_pre) {
-    return a.d == 128 ? launch_dkdv_d<128>(a, s, after_pre) : launch_dkdv_d<64>(a, s, after_pre);
+    return a.d == 128 ? launch_dkdv_d<128, false>(a, s, after_pre) : launch_dkdv_d<64, false>(a, s, after_pre);
+}
+cudaError_t launch_bwd_fused(const BwdLaunch& a, cudaStream_t s) {
+    return a.d == 128 ? launch_fused_d(a, s) : cudaErrorInvalidValue;
+}
+cudaError_t launch_bwd_dkdv_pair(const BwdLaunch& a, cudaStream_t s) {
+    return a.d == 128 ? launch_dkdv_d<128, true>(a, s, false) : cudaErrorInvalidValue;
 }
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s, bool after_dkdv) {
     return a.d == 128 ? launch_dq_d<128>(a, s, after_dkdv) : launch_dq_d<64>(a, s, after_dkdv);

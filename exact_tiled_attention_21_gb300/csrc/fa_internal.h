@@ -37,6 +37,7 @@ struct FwdLaunch {
 
 struct BwdLaunch {
     CUtensorMap map_q, map_k, map_v, map_do;  // same geometry as the forward maps
+    CUtensorMap map_q2, map_do2;              // d = 128: Q and dO with box (64, 64, 1) (CTA-pair dK/dV pass)
     const void* q;
     const void* k;
     const void* o;
@@ -46,6 +47,7 @@ struct BwdLaunch {
     void* dk;
     void* dv;
     float* delta;   // fp32 [B,H,Nq] (the workspace)
+    float* dqacc;   // fp32 [B,H,Nq,d] (single-pass backward: zeroed by the preprocess), else null
     int B, H, Nq, Nk, d;
     float scale;
     int causal;
@@ -158,6 +160,8 @@ bool fwd_use_split(const FwdLaunch& a);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s);   // D = rowsum(dO o O)
 cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s, bool after_pre = false);  // dK, dV; after_pre:
                                                                                         // overlaps the preprocess's end
+cudaError_t launch_bwd_dkdv_pair(const BwdLaunch& a, cudaStream_t s);  // dK, dV on CTA pairs (d = 128)
+cudaError_t launch_bwd_fused(const BwdLaunch& a, cudaStream_t s);  // dK, dV, dQ in one pass + dQ convert (d = 128)
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s, bool after_dkdv = false);  // dQ; after_dkdv:
                                                                                      // overlaps the dK/dV grid's end
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);

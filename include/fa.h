@@ -148,6 +148,28 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            int B, int H, int Nq, int Nk, int d, float scale, int causal,
            void *workspace, size_t workspace_bytes, void *stream);
 
+/* Bytes of workspace fa_bwd_fused needs: D [B,H,Nq] as for fa_bwd, then an
+ * fp32 dQ accumulator [B,H,Nq,d].  Returns 0 for invalid sizes and for
+ * d != 128. */
+size_t fa_bwd_fused_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+
+/* The same backward as fa_bwd (same arguments, outputs and tolerance) in one
+ * pass over the key tiles instead of two: besides dK and dV, each 128-key
+ * CTA computes its share of dQ = scale dS K as dQ^T = K^T dS^T on the tensor
+ * cores and adds it to the fp32 accumulator in the workspace with reduce-adds,
+ * so S and dP are rebuilt once per tile pair instead of twice (johe.ru, section
+ * "Стадии вычисления", pass 2; the dQ product is one of the five).  The order
+ * of those fp32 additions varies from run to run, so dq is not bit-for-bit
+ * reproducible (dk and dv are).  Launches: the preprocess (which also zeroes
+ * the accumulator), the pass, and a conversion of the accumulator to bf16 dq.
+ * d = 128 only (FA_ERR_UNSUPPORTED otherwise).  workspace must hold at least
+ * fa_bwd_fused_workspace_bytes(B,H,Nq,Nk,d) bytes, 16-byte aligned; its
+ * contents on entry do not matter. */
+int fa_bwd_fused(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                 const void *dO, void *dq, void *dk, void *dv,
+                 int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
 /* Backward of fa_fwd_window (same window, same conventions as fa_bwd). */
 int fa_bwd_window(const void *q, const void *k, const void *v, const void *o, const float *lse,
                   const void *dO, void *dq, void *dk, void *dv,
@@ -185,6 +207,20 @@ int fa_bwd_dkdv(const void *q, const void *k, const void *v, const float *lse, c
 int fa_bwd_dq(const void *q, const void *k, const void *v, const float *lse, const float *delta,
               const void *dO, void *dq, int B, int H, int Nq, int Nk, int d, float scale, int causal,
               void *stream);
+
+/* fa_bwd_dkdv on CTA pairs (d = 128 only; FA_ERR_UNSUPPORTED for d = 64):
+ * the two CTAs of a cluster take key tiles 2t and 2t + 1 of a head and issue
+ * every product once for both as a tcgen05.mma with cta_group::2 (M = 256
+ * keys), each CTA loading only the half of the B operand that it contributes.
+ * Same arguments, outputs and tolerance as fa_bwd_dkdv (the same sums, split
+ * differently across the tensor cores).  It needs more synchronisation
+ * between the two CTAs than it saves in shared-memory reads, so it is slower
+ * than fa_bwd_dkdv, which fa_bwd uses (johe.ru "Flash Attention: ...",
+ * section "Flash Attention 4": kernels for the newest tensor cores).  The
+ * caller's stream must allow cluster launches (every CUDA stream does). */
+int fa_bwd_dkdv_pair(const void *q, const void *k, const void *v, const float *lse, const float *delta,
+                     const void *dO, void *dk, void *dv, int B, int H, int Nq, int Nk, int d, float scale,
+                     int causal, void *stream);
 
 /* Bytes of fp32 workspace fa_decode needs for num_splits partials (<= 0:
  * the number the library would choose for this Nk).  Returns 0 for invalid

@@ -68,6 +68,11 @@ def test_backward_and_decode_validation(lib):
     assert lib.fa_bwd(*p, 1, 1, 8, 8, 64, 0.125, 0, vp(8), ws_need, None) == fa.FA_ERR_ALIGNMENT
     assert lib.fa_bwd(*([vp(0)] + p[1:]), 1, 1, 8, 8, 64, 0.125, 0, vp(16), ws_need, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_bwd(*p, 1, 1, 8, 8, 80, 0.125, 0, vp(16), ws_need, None) == fa.FA_ERR_UNSUPPORTED
+    pr = [vp(16)] * 8
+    assert lib.fa_bwd_dkdv_pair(*([vp(0)] + pr[1:]), 1, 1, 8, 8, 128, 0.125, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_bwd_dkdv_pair(*pr, 1, 1, 8, 8, 64, 0.125, 0, None) == fa.FA_ERR_UNSUPPORTED  # pairs: d = 128
+    assert lib.fa_bwd_dkdv_pair(*pr, 1, 1, 8, 8, 80, 0.125, 0, None) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_bwd_dkdv_pair(*pr, 1, 1, 8, 8, 128, 0.125, 2, None) == fa.FA_ERR_INVALID_ARG
     d_need = fa.fa_decode_workspace_bytes(2, 2, 100, 128, 16)
     q = [vp(16)] * 5
     assert lib.fa_decode(*q, 2, 2, 100, 128, 0.1, 16, vp(16), d_need - 4, None) == fa.FA_ERR_WORKSPACE

@@ -19,11 +19,11 @@ def _inputs(seed, B, H, Nq, Nk, d):
             syn.bhnd(seed, syn.TAG_V, B, H, Nk, d), syn.bhnd(seed, syn.TAG_DO, B, H, Nq, d))
 
 
-def _run(fa, q, k, v, dO, scale, causal):
+def _run(fa, q, k, v, dO, scale, causal, fused=False):
     dev = torch.device("cuda", 0)
     qd, kd, vd, dOd = (t.to(dev) for t in (q, k, v, dO))
     o, lse = fa.forward(qd, kd, vd, scale=scale, causal=causal)
-    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dOd, scale=scale, causal=causal)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dOd, scale=scale, causal=causal, fused=fused)
     torch.cuda.synchronize()
     st, detail = fa.fa_get_last_device_error()
     assert st == 0, detail
@@ -44,17 +44,26 @@ CASES = [
     (1, 2, 1, 300, 128, False),
     (1, 2, 300, 1, 64, True),
     (2, 3, 77, 1031, 64, True),
+    (1, 2, 128, 128, 128, True),
+    (1, 2, 128, 128, 128, False),
+    (1, 2, 300, 1, 128, False),
+    (3, 2, 129, 129, 128, True),
+    (1, 3, 640, 384, 128, True),
 ]
 
 
-@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", CASES)
-def test_backward_parity(cuda_lib, B, H, Nq, Nk, d, causal):
+FUSED_CASES = [c + (True,) for c in CASES if c[4] == 128]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal,fused", [c + (False,) for c in CASES] + FUSED_CASES)
+def test_backward_parity(cuda_lib, B, H, Nq, Nk, d, causal, fused):
+    """fa_bwd (two passes) and fa_bwd_fused (one pass, dQ by fp32 reduce-adds)."""
     seed = 500 + Nq * 3 + Nk + d + causal
     q, k, v, dO = _inputs(seed, B, H, Nq, Nk, d)
     scale = 1.0 / math.sqrt(d)
-    dq, dk, dv = _run(cuda_lib, q, k, v, dO, scale, causal)
+    dq, dk, dv = _run(cuda_lib, q, k, v, dO, scale, causal, fused)
     rq, rk, rv = naive.backward(f64(q), f64(k), f64(v), f64(dO), scale, causal)
-    tag = "B%d H%d Nq%d Nk%d d%d c%d" % (B, H, Nq, Nk, d, causal)
+    tag = "B%d H%d Nq%d Nk%d d%d c%d%s" % (B, H, Nq, Nk, d, causal, " fused" if fused else "")
     dp_max = np.abs(f64(dO) @ np.swapaxes(f64(v), -1, -2)).max()
     cancel = scale * dp_max * max(np.abs(f64(k)).max(), np.abs(f64(q)).max())
     check_grad(f64(dq), rq, "dQ " + tag, cancel_scale=cancel)
@@ -113,6 +122,52 @@ def test_backward_matches_step_entry_points(cuda_lib, B, H, N):
     assert torch.equal(dk_seen, dk2) and torch.equal(dv_seen, dv2)
 
 
+# fa_bwd_dkdv_pair takes key tiles two at a time: one key tile (the odd CTA's
+# tile lies wholly past Nk), odd and even tile counts, ragged and Nq != Nk.
+PAIR_CASES = [
+    (1, 2, 128, 128, True),
+    (1, 2, 128, 128, False),
+    (1, 2, 300, 300, True),
+    (2, 2, 513, 257, False),
+    (1, 2, 257, 513, True),
+    (1, 2, 700, 200, True),
+    (3, 2, 129, 129, True),
+    (1, 3, 640, 384, True),
+    (1, 32, 2048, 2048, True),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", PAIR_CASES)
+def test_dkdv_on_cta_pairs(cuda_lib, B, H, Nq, Nk, causal):
+    """The CTA-pair dK/dV pass against the oracle, and against fa_bwd_dkdv."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    d = 128
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, dO = _inputs(700 + Nq + 3 * Nk + causal, B, H, Nq, Nk, d)
+    qd, kd, vd, dOd = (t.to(dev) for t in (q, k, v, dO))
+    o, lse = fa.forward(qd, kd, vd, scale=scale, causal=causal)
+    delta = torch.empty(B, H, Nq, device=dev)
+    fa.fa_bwd_preprocess(o, dOd, delta, B, H, Nq, d)
+    dk, dv = torch.full_like(kd, float("nan")), torch.full_like(vd, float("nan"))
+    dk1, dv1 = torch.empty_like(kd), torch.empty_like(vd)
+    fa.fa_bwd_dkdv_pair(qd, kd, vd, lse, delta, dOd, dk, dv, B, H, Nq, Nk, d, scale, causal)
+    fa.fa_bwd_dkdv(qd, kd, vd, lse, delta, dOd, dk1, dv1, B, H, Nq, Nk, d, scale, causal)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_get_last_device_error()
+    assert st == 0, detail
+    _, rk, rv = naive.backward(f64(q), f64(k), f64(v), f64(dO), scale, causal)
+    tag = "pair B%d H%d Nq%d Nk%d c%d" % (B, H, Nq, Nk, causal)
+    dp_max = np.abs(f64(dO) @ np.swapaxes(f64(v), -1, -2)).max()
+    cancel = scale * dp_max * np.abs(f64(q)).max()
+    check_grad(f64(dk.cpu()), rk, "dK " + tag, cancel_scale=cancel)
+    check_grad(f64(dv.cpu()), rv, "dV " + tag)
+    # the same sums as the single-CTA pass, computed on other tensor cores: equal to
+    # within fp32 accumulation order (both are rounded to bf16 at the end)
+    assert (dk.float() - dk1.float()).abs().max() <= 2 ** -7 * dk1.float().abs().max() + 1e-6
+    assert (dv.float() - dv1.float()).abs().max() <= 2 ** -7 * dv1.float().abs().max() + 1e-6
+
+
 @pytest.mark.parametrize("N,d", [(700, 128), (300, 64)])
 def test_backward_gradients_16_byte_aligned(cuda_lib, N, d):
     """dQ, dK, dV written 16 bytes past a 32-byte boundary take the 16-byte
@@ -145,15 +200,31 @@ def test_backward_deterministic(cuda_lib):
     assert all(torch.equal(x, y) for x, y in zip(a, b))
 
 
+def test_fused_backward_matches_two_pass(cuda_lib):
+    """fa_bwd_fused: dK and dV are the same sums over the same query tiles as
+    fa_bwd's, in 64-row instead of 128-row tiles; dQ differs only in the order
+    of its fp32 additions.  All three agree with fa_bwd to within bf16 rounding,
+    and dK, dV repeat bit for bit from run to run."""
+    q, k, v, dO = _inputs(19, 1, 4, 1000, 1000, 128)
+    ref = _run(cuda_lib, q, k, v, dO, 0.088, True)
+    a = _run(cuda_lib, q, k, v, dO, 0.088, True, fused=True)
+    b = _run(cuda_lib, q, k, v, dO, 0.088, True, fused=True)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    for x, y in zip(a, ref):
+        assert (x.float() - y.float()).abs().max() <= 2 ** -7 * y.float().abs().max() + 1e-6
+
+
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("N", [1024, 2048, 4096, 8192])
-def test_backward_full_size_sweep(cuda_lib, N):
-    """B=1, H=32, d=128, causal, N in the 1k-8k sweep: heads 0 and 31 against the oracle."""
+def test_backward_full_size_sweep(cuda_lib, N, fused):
+    """B=1, H=32, d=128, causal, N in the 1k-8k sweep: heads 0 and 31 against the
+    oracle, for fa_bwd and for fa_bwd_fused."""
     cfg = syn.CONFIGS["fwd_bwd_sweep"]
     B, H, d = cfg["B"], cfg["H"], cfg["d"]
     seed = cfg["seed"] + N
     q, k, v, dO = _inputs(seed, B, H, N, N, d)
     scale = syn.default_scale(d)
-    dq, dk, dv = _run(cuda_lib, q, k, v, dO, scale, True)
+    dq, dk, dv = _run(cuda_lib, q, k, v, dO, scale, True, fused)
     for h in (0, H - 1):
         rq, rk, rv = naive.backward(f64(q[0, h]), f64(k[0, h]), f64(v[0, h]), f64(dO[0, h]), scale, True)
         check_grad(f64(dq[0, h]), rq, "dQ N%d h%d" % (N, h))
