@@ -282,6 +282,8 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
     out = {"fwd_bwd_causal_B1_H32_d128": [], "fwd_B2_H32_N4096_d128": [], "decode_B32_H32": [],
            "timing": "median of per-call CUDA-event times on the launching stream; L2 flushed before each "
                      "fwd/bwd call (256 MiB write, outside the events)",
+           "bwd_modes": "bwd: fa_bwd (dK/dV pass + dQ pass, deterministic); bwd_fused: fa_bwd_fused (one pass, "
+                        "dQ by fp32 reduce-adds, dQ bits vary run to run)",
            "_windows": {}}
     # decode shapes (the cache is read once per call; >= 1 GiB, larger than L2)
     t0 = time.time()
@@ -314,14 +316,21 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
         for _ in range(3):
             fwd()
             bwd()
+        wsf = torch.empty(fa.fa_bwd_fused_workspace_bytes(1, H, n, n, D), dtype=torch.uint8, device=dev)
+        bwdf = lambda: fa.fa_bwd_fused(q, k, v, o, lse, dO, dq, dk, dv, 1, H, n, n, D, SCALE, True, wsf,
+                                       wsf.numel(), stream)
+        for _ in range(3):
+            bwdf()
         reps = 20 if n <= 2048 else 10
         f_ms = timed(fwd, reps, True)
         b_ms = timed(bwd, reps, True)
+        bf_ms = timed(bwdf, reps, True)
         fl = 4.0 * H * n * n * D / 2
         out["fwd_bwd_causal_B1_H32_d128"].append(
             {"N": n, "fwd_ms": f_ms, "fwd_tflops": fl / (f_ms * 1e-3) / 1e12,
-             "bwd_ms": b_ms, "bwd_tflops": 2.5 * fl / (b_ms * 1e-3) / 1e12})
-        del q, k, v, dO, o, dq, dk, dv, lse, ws
+             "bwd_ms": b_ms, "bwd_tflops": 2.5 * fl / (b_ms * 1e-3) / 1e12,
+             "bwd_fused_ms": bf_ms, "bwd_fused_tflops": 2.5 * fl / (bf_ms * 1e-3) / 1e12})
+        del q, k, v, dO, o, dq, dk, dv, lse, ws, wsf
     for causal in (False, True):
         q, k, v = (rnd(2, H, 4096, D) for _ in range(3))
         o = torch.empty_like(q)
@@ -382,6 +391,7 @@ def finish_sweep(sw, pk, sampler):
     for e in sw["fwd_bwd_causal_B1_H32_d128"]:
         e["fwd_frac"] = e["fwd_tflops"] / pk["bf16"]
         e["bwd_frac"] = e["bwd_tflops"] / pk["bf16"]
+        e["bwd_fused_frac"] = e["bwd_fused_tflops"] / pk["bf16"]
     for e in sw["fwd_B2_H32_N4096_d128"]:
         e["fwd_frac"] = e["fwd_tflops"] / pk["bf16"]
     lo = sw["fwd_long_causal_B1_H32_N131072_d128"]
@@ -467,6 +477,7 @@ def run_ours(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError("device error during warm-up: %s" % detail)
 
+    K_ALT = max(3, min(args.steps, 20))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     bevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -483,6 +494,25 @@ def run_ours(args, rank, world, local_rank):
     for i in range(args.steps):
         bwd_steps(bevs[i])
     barrier()
+    # the single-pass backward (fa_bwd_fused) and the CTA-pair dK/dV pass, K calls each
+    wsf = torch.empty(fa.fa_bwd_fused_workspace_bytes(B, H, N, N, D), dtype=torch.uint8, device=dev)
+    fev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(3):
+        fa.fa_bwd_fused(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, D, SCALE, True, wsf, wsf.numel(), stream)
+        fa.fa_bwd_dkdv_pair(q, k, v, lse, delta, dO, dk, dv, B, H, N, N, D, SCALE, True, stream)
+    barrier()
+    fev[0].record(stream)
+    for _ in range(K_ALT):
+        fa.fa_bwd_fused(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, D, SCALE, True, wsf, wsf.numel(), stream)
+    fev[1].record(stream)
+    fev[2].record(stream)
+    for _ in range(K_ALT):
+        fa.fa_bwd_dkdv_pair(q, k, v, lse, delta, dO, dk, dv, B, H, N, N, D, SCALE, True, stream)
+    fev[3].record(stream)
+    barrier()
+    bwd_fused_ms = fev[0].elapsed_time(fev[1]) / K_ALT
+    dkdv_pair_ms = fev[2].elapsed_time(fev[3]) / K_ALT
+    del wsf
     w1 = time.time()  # the clock record covers both passes
     st, detail = fa.fa_get_last_device_error(stream)
     if st != 0:
@@ -699,6 +729,13 @@ def run_ours(args, rank, world, local_rank):
             "bwd_pre_ms": pre_ms, "bwd_dkdv_ms": dkdv_ms, "bwd_dq_ms": dq_ms,
             "bwd_kernels_note": "pre/dkdv/dq: the step entry points timed one by one after the timed region "
                                 "(fa_bwd overlaps the dQ pass with the end of the dK/dV pass)",
+            "bwd_fused_ms": bwd_fused_ms, "bwd_fused_tflops": BWD_FLOPS / (bwd_fused_ms * 1e-3) / 1e12,
+            "bwd_fused_note": "fa_bwd_fused: the same backward in one pass over the key tiles (dQ^T = K^T dS^T on "
+                              "the tensor cores, bulk fp32 reduce-adds; dQ bits vary run to run), %d back-to-back "
+                              "calls" % K_ALT,
+            "bwd_dkdv_pair_ms": dkdv_pair_ms,
+            "bwd_dkdv_pair_note": "fa_bwd_dkdv_pair: the dK/dV pass on CTA pairs (cta_group::2), %d back-to-back "
+                                  "calls; compare bwd_dkdv_ms" % K_ALT,
             "fwd_frac_of_peak": FWD_FLOPS / (fwd_ms * 1e-3) / 1e12 / pk["bf16"],
             "bwd_frac_of_peak": BWD_FLOPS / (bwd_ms * 1e-3) / 1e12 / pk["bf16"],
             "peak_source": "%s bf16_tflops (burst)" % pk["source"],
@@ -760,6 +797,79 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+# ------------------------------------------------------------------ one kernel for a profiler
+PROFILE_TARGETS = ("fwd", "dkdv", "dq", "fused", "pair", "decode", "decode64", "paged", "fp8")
+
+
+def run_profile(target, launches):
+    """Runs one kernel of the bench workload ``launches`` times (after one warm-up
+    call) with only its own inputs on the device, for an ncu capture:
+    fwd / dkdv / dq / fused / pair at B=1, H=32, N=8192, d=128 causal; decode at
+    B=32, H=32, Nk=4096 (d=128 or d=64); paged at B=32, Hq=32, Hkv=8, page 16;
+    fp8 the FP8 forward.  Prints one line; no timing."""
+    import torch
+    import exact_tiled_attention_21_gb300 as fa
+    dev = torch.device("cuda", 0)
+    fa.load()
+    s = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev).manual_seed(99)
+    rnd = lambda *sh: torch.randn(*sh, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    if target in ("fwd", "dkdv", "dq", "fused", "pair"):
+        q, k, v, dO = (rnd(B, H, N, D) for _ in range(4))
+        o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+        lse = torch.empty(B, H, N, device=dev)
+        delta = torch.empty(B, H, N, device=dev)
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, N, D, SCALE, True, s)
+        fa.fa_bwd_preprocess(o, dO, delta, B, H, N, D, s)
+        wsf = torch.empty(fa.fa_bwd_fused_workspace_bytes(B, H, N, N, D), dtype=torch.uint8, device=dev)
+        call = {
+            "fwd": lambda: fa.fa_fwd(q, k, v, o, lse, B, H, N, N, D, SCALE, True, s),
+            "dkdv": lambda: fa.fa_bwd_dkdv(q, k, v, lse, delta, dO, dk, dv, B, H, N, N, D, SCALE, True, s),
+            "dq": lambda: fa.fa_bwd_dq(q, k, v, lse, delta, dO, dq, B, H, N, N, D, SCALE, True, s),
+            "fused": lambda: fa.fa_bwd_fused(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, D, SCALE, True, wsf,
+                                             wsf.numel(), s),
+            "pair": lambda: fa.fa_bwd_dkdv_pair(q, k, v, lse, delta, dO, dk, dv, B, H, N, N, D, SCALE, True, s),
+        }[target]
+    elif target in ("decode", "decode64"):
+        d = 128 if target == "decode" else 64
+        qd, kc, vc = rnd(DEC_B, DEC_H, d), rnd(DEC_B, DEC_H, DEC_NK, d), rnd(DEC_B, DEC_H, DEC_NK, d)
+        od = torch.empty_like(qd)
+        lsed = torch.empty(DEC_B, DEC_H, device=dev)
+        ws = torch.empty(fa.fa_decode_workspace_bytes(DEC_B, DEC_H, DEC_NK, d, DEC_SPLITS), dtype=torch.uint8,
+                         device=dev)
+        call = lambda: fa.fa_decode(qd, kc, vc, od, lsed, DEC_B, DEC_H, DEC_NK, d, 1 / math.sqrt(d), DEC_SPLITS, ws,
+                                    ws.numel(), s)
+    elif target == "paged":
+        hkv, page = 8, 16
+        npages = DEC_B * (DEC_NK // page)
+        kp, vp = rnd(npages, hkv, page, D), rnd(npages, hkv, page, D)
+        qd = rnd(DEC_B, DEC_H, D)
+        table = torch.randperm(npages, generator=torch.Generator().manual_seed(5)).to(torch.int32)
+        table = table.reshape(DEC_B, DEC_NK // page).to(dev)
+        lens = torch.full((DEC_B,), DEC_NK, dtype=torch.int32, device=dev)
+        od = torch.empty_like(qd)
+        lsed = torch.empty(DEC_B, DEC_H, device=dev)
+        ws = torch.empty(fa.fa_decode_paged_workspace_bytes(DEC_B, DEC_H, D, 0), dtype=torch.uint8, device=dev)
+        call = lambda: fa.fa_decode_paged(qd, kp, vp, table, lens, od, lsed, DEC_B, DEC_H, hkv, page, DEC_NK // page,
+                                          npages, D, SCALE, 0, ws, ws.numel(), s)
+    else:  # fp8
+        mk = lambda: torch.randint(0, 126, (1, H, N, D), generator=torch.Generator().manual_seed(7),
+                                   dtype=torch.int32).to(torch.uint8).to(dev)
+        q8, k8, v8 = mk(), mk(), mk()
+        sq = torch.full((H, N // 128), 1.0 / 64, device=dev)
+        sv = torch.full((H,), 1.0 / 64, device=dev)
+        o = torch.empty(1, H, N, D, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(1, H, N, device=dev)
+        ws = torch.empty(fa.fa_fwd_fp8_workspace_bytes(1, H, N, D), dtype=torch.uint8, device=dev)
+        call = lambda: fa.fa_fwd_fp8(q8, k8, v8, sq, sq, sv, o, lse, 1, H, N, N, D, SCALE, 1, ws, ws.numel(), s)
+    for _ in range(1 + launches):
+        call()
+    torch.cuda.synchronize(dev)
+    st, detail = fa.fa_get_last_device_error(s)
+    print(json.dumps({"profile": target, "launches": 1 + launches, "device_error": st}), flush=True)
+    return 0 if st == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -769,12 +879,17 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload sweep (not timed in the step)")
+    ap.add_argument("--profile", choices=PROFILE_TARGETS, default=None,
+                    help="run one kernel of the workload a few times with only its own inputs (for ncu); no timing")
+    ap.add_argument("--launches", type=int, default=2, help="with --profile: launches after one warm-up call")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.profile:
+        return run_profile(args.profile, args.launches)
     if args.impl == "reference":
         return run_reference(args, rank)
     return run_ours(args, rank, world, local_rank)
