@@ -22,6 +22,8 @@
 // pv_done[t] barrier tells the softmax when P_t and O_t may be written again.
 // The transposed copy [B*H, 128, Nk rounded up to 16] is made by vt_kernel into
 // the caller's workspace before the forward runs.
+#include <algorithm>
+
 #include "fa_internal.h"
 
 namespace fa {
@@ -82,6 +84,7 @@ struct F8Params {
     const float* q_scale;  // [B*H, ceil(Nq/128)]
     const float* k_scale;  // [B*H, ceil(Nk/128)]
     const float* v_scale;  // [B*H]
+    int hc;  // heads per scheduling chunk
     int BH, Nq, Nk, causal, n_qb, n_kb;
     int n_mtiles, num_work;
     float scale_log2;
@@ -98,9 +101,17 @@ __device__ __forceinline__ int f8_num_kv(const F8Params& p, int row0) {
     return min(kv_total, (int)(lim / 128) + 1);
 }
 
+// Work tile w -> (bh, first row), as the bf16 forward's: heads in chunks of hc
+// (non-causal: whose K and V fit in L2 together; causal: one chunk, heaviest
+// row tiles of every head first).
 __device__ __forceinline__ void f8_decode(const F8Params& p, int w, int& bh, int& row0) {
-    const int mr = w / p.BH;
-    bh = w - mr * p.BH;
+    const int chunk = p.hc * p.n_mtiles;
+    const int c = w / chunk;
+    const int r = w - c * chunk;
+    const int h0 = c * p.hc;
+    const int hn = min(p.hc, p.BH - h0);
+    const int mr = r / hn;
+    bh = h0 + (r - mr * hn);
     const int m = p.causal ? (p.n_mtiles - 1 - mr) : mr;
     row0 = m * kFwdRowsPerCta;
 }
@@ -547,6 +558,10 @@ cudaError_t launch_fwd_fp8(const Fp8FwdLaunch& a, cudaStream_t s) {
     p.n_kb = (a.Nk + 127) / 128;
     p.n_mtiles = (a.Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
     p.num_work = p.n_mtiles * BH;
+    {  // K (e4m3) and V^T (e4m3) of a head: 2 Nk d bytes
+        const long long per_head = 2ll * a.Nk * 128;
+        p.hc = a.causal ? BH : (int)std::max(1ll, std::min((long long)BH, (64ll << 20) / per_head));
+    }
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
     p.timeout_ns = a.timeout_ns;

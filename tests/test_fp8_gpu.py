@@ -74,12 +74,13 @@ def test_fp8_forward_parity(cuda_lib, B, H, Nq, Nk, causal):
 
 
 def test_fp8_forward_full_size_sampled(cuda_lib):
-    """B=1, H=32, N=8192, causal (the bench workload): 2 heads x 128 seeded rows."""
+    """B=1, H=32, N=8192, causal (the bench workload): 8 heads x 256 seeded rows
+    (always including rows 0 and N - 1)."""
     N, H = 8192, 32
-    heads = syn.sample_heads(31, H, 2)
+    heads = syn.sample_heads(31, H, 8)
     q8, k8, v8, sq, sk, sv = _inputs(4242, 1, H, N, N, heads=heads)
     o, lse = _run(cuda_lib, q8, k8, v8, sq, sk, sv, True)
-    rows = syn.sample_rows(31, N, 128)
+    rows = syn.sample_rows(31, N, 256)
     for h in heads:
         sl = slice(h, h + 1)
         o_ref, lse_ref, p_ref, v = _oracle(q8[:, sl], k8[:, sl], v8[:, sl], sq[sl], sk[sl], sv[sl], True,
