@@ -213,19 +213,25 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, __nv_bfloat16* dst
     taddr += c0;
     dst += c0;
     const bool wide = ((uintptr_t)dst & 31) == 0;  // the same for every row: rows are 32-byte multiples
-#pragma unroll 1
-    for (int q4 = 0; q4 < D / 64; ++q4) {
-        uint32_t v[32];
-        if (!zero) {
-            tmem_ld32(taddr + q4 * 32, v);
-        } else {
+    constexpr int NQ = D / 64;  // 32-column chunks of this warpgroup's half
+    uint32_t v[NQ][32];
+    if (!zero) {  // (warp-uniform) every chunk's load in flight before the one wait
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
+        for (int q4 = 0; q4 < NQ; ++q4) tmem_ld32_async(taddr + q4 * 32, v[q4]);
+#pragma unroll
+        for (int q4 = 0; q4 < NQ; ++q4) tmem_wait_ld(v[q4]);
+    } else {
+#pragma unroll
+        for (int q4 = 0; q4 < NQ; ++q4)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[q4][i] = 0u;
+    }
+#pragma unroll
+    for (int q4 = 0; q4 < NQ; ++q4) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+            pk[i] = pack_bf16(__uint_as_float(v[q4][2 * i]) * mul, __uint_as_float(v[q4][2 * i + 1]) * mul);
         if (valid) store_row64(dst + q4 * 32, pk, wide);
     }
 }
@@ -361,16 +367,20 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // S: S^T ready; SF: S^T read out of TMEM (the next S^T may overwrite it); DP: dP^T ready;
     // DS: P^T and dS^T written over dP^T (bf16, TMEM)
     // STE[s]: stage s free, once both issuers' products that read it are done (two arrivals);
-    // TD, TD2: teardown of issuer 1 and 2
+    // TD, TD2: teardown of issuer 1 and 2; ACC: an item's dK and dV complete
+    // KE, VE: an item's K (its last S^T) and V (its last dP^T) no longer read; ACCE: its dK, dV
+    // read out of TMEM
     const uint32_t B_KV = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_DP = bar0 + 48,
-                   B_DS = bar0 + 56, B_ACC = bar0 + 64, B_TD = bar0 + 72, B_SF = bar0 + 80, B_TD2 = bar0 + 88;
+                   B_DS = bar0 + 56, B_ACC = bar0 + 64, B_TD = bar0 + 72, B_SF = bar0 + 80, B_TD2 = bar0 + 88,
+                   B_KE = bar0 + 96, B_ACCE = bar0 + 104, B_VE = bar0 + 112;
     // STF: the producer's 32 lanes (of each CTA of a pair); SF, DS: every compute thread, or in a
-    // pair one elected thread per compute warp of each CTA
+    // pair one elected thread per compute warp of each CTA; ACCE: every compute thread
     constexpr uint32_t N_STF = PAIR ? 64 : 32, N_SD = PAIR ? 16 : 256;
-    const uint32_t counts[12] = {1, N_STF, N_STF, 2, 2, 1, 1, N_SD, 1, 1, N_SD, 1};
+    const uint32_t counts[15] = {1, N_STF, N_STF, 2, 2, 1, 1, N_SD, 1, 1, N_SD, 1, 1, 256, 1};
+    static_assert(15 <= C::NBAR, "barrier space");
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
-    const uint32_t tmem = bwd_setup<D, PAIR>(smem, bar0, ctl, counts, 12);
+    const uint32_t tmem = bwd_setup<D, PAIR>(smem, bar0, ctl, counts, 15);
     const uint32_t rank = PAIR ? cluster_rank() : 0u;
     const bool lead = rank == 0;  // the CTA whose thread issues the products
     // a barrier the issuing thread waits on, as addressed from this CTA
@@ -383,50 +393,95 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int bh, kt;  // key tile 0 (the most query tiles when causal) first, heads in L2-sized chunks
-    if constexpr (PAIR) {
-        int pt;
-        chunked_order(blockIdx.x >> 1, p.n_pt, p.BH, p.hc_kv, bh, pt);
-        kt = 2 * pt + (int)rank;
-    } else {
-        chunked_order(blockIdx.x, p.n_kt, p.BH, p.hc_kv, bh, kt);
-    }
-    int nq, nk;
-    bwd_seqlen(p, bh, nq, nk);
-    const int off = nk - nq;
-    const int kt_lo = kt - (int)rank, kt_hi = PAIR ? kt_lo + 1 : kt;  // the key tiles sharing the loop
-    int i0 = 0;
-    if (p.causal) {
-        const int first_q = kt_lo * 128 - off;  // smallest query that sees key kt_lo*128
-        i0 = first_q <= 0 ? 0 : first_q / 128;
-    }
-    auto tile_end = [&](int t) {  // one past the last query tile that sees key tile t
-        int e = t * 128 < nk ? (nq + 127) / 128 : 0;  // no query tile past the sequence
-        if (p.window > 0) {  // the last query that sees the tile's last key
-            const long long qlast = (long long)t * 128 + 127 - off + p.window - 1;
-            e = qlast < 0 ? 0 : (int)min((long long)e, qlast / 128 + 1);
-        }
-        return e;
+    // Work items: key tiles (in a pair, key-tile pairs) in the chunked order (key tile 0, the most
+    // query tiles when causal, first; heads in L2-sized chunks).  A single CTA is persistent and,
+    // while its compute warps store one item's dK and dV, already loads the next item's K, V and
+    // first query tiles and runs its first score products.  Within each chunk the CTAs take the
+    // items round by round, alternating direction (round r: r*G + c, or r*G + G-1-c), odd chunks
+    // starting reversed, so that the rounds' long and short items even out per CTA; with chunks
+    // smaller than the grid the rounds run over the whole order instead.  A pair takes the one
+    // item of its cluster.
+    const int n_items = PAIR ? p.n_pt * p.BH : p.n_kt * p.BH;
+    const int chunk_items = p.hc_kv * p.n_kt;
+    struct ItemSeq {
+        int ci, rd;  // chunk and round within it
     };
-    const int i_end = max(tile_end(kt_lo), tile_end(kt_hi));
-    const int n = i0 < i_end ? i_end - i0 : 0;
+    auto next_item = [&](ItemSeq& q) -> int {
+        if constexpr (PAIR) {
+            return q.rd++ == 0 ? (int)(blockIdx.x >> 1) : n_items;
+        } else {
+            const int G = gridDim.x, c = blockIdx.x;
+            if (chunk_items < G) return min(n_items, persistent_work(q.rd++, c, G));
+            for (;;) {
+                const int start = q.ci * chunk_items;
+                if (start >= n_items) return n_items;
+                const int wl = q.rd * G + (((q.rd + q.ci) & 1) ? G - 1 - c : c);
+                if (wl < min(chunk_items, n_items - start)) {
+                    ++q.rd;
+                    return start + wl;
+                }
+                ++q.ci;
+                q.rd = 0;
+            }
+        }
+    };
+    struct Item {
+        int bh, kt, nq, nk, off, i0, n;  // n query tiles from i0 (the union of a pair's two key tiles)
+    };
+    auto item_of = [&](int w) {
+        Item it;
+        if constexpr (PAIR) {
+            int pt;
+            chunked_order(w, p.n_pt, p.BH, p.hc_kv, it.bh, pt);
+            it.kt = 2 * pt + (int)rank;
+        } else {
+            chunked_order(w, p.n_kt, p.BH, p.hc_kv, it.bh, it.kt);
+        }
+        bwd_seqlen(p, it.bh, it.nq, it.nk);
+        it.off = it.nk - it.nq;
+        const int kt_lo = it.kt - (int)rank, kt_hi = PAIR ? kt_lo + 1 : it.kt;  // the key tiles sharing the loop
+        it.i0 = 0;
+        if (p.causal) {
+            const int first_q = kt_lo * 128 - it.off;  // smallest query that sees key kt_lo*128
+            it.i0 = first_q <= 0 ? 0 : first_q / 128;
+        }
+        auto tile_end = [&](int t) {  // one past the last query tile that sees key tile t
+            int e = t * 128 < it.nk ? (it.nq + 127) / 128 : 0;  // no query tile past the sequence
+            if (p.window > 0) {  // the last query that sees the tile's last key
+                const long long qlast = (long long)t * 128 + 127 - it.off + p.window - 1;
+                e = qlast < 0 ? 0 : (int)min((long long)e, qlast / 128 + 1);
+            }
+            return e;
+        };
+        const int i_end = max(tile_end(kt_lo), tile_end(kt_hi));
+        it.n = it.i0 < i_end ? i_end - it.i0 : 0;
+        return it;
+    };
     const uint32_t sK = s_base + C::OFF_FIXED, sV = sK + C::TILE;
     auto sQ = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
     auto sDO = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
     float* vec = (float*)(smem + C::OFF_VEC);  // stage s: lse2 at [s*256], delta at [s*256 + 128]
-    const bool kv_issued = warp == C::PRODUCER && lane == 0 && n > 0 && !*abort_flag;
-    if (kv_issued) {  // K and V do not come from the preprocess: they load before the wait for it
+    auto load_kv = [&](const Item& it) {  // one lane
         if (lead) mbar_arrive_expect_tx(B_KV, (PAIR ? 4 : 2) * C::TILE);
         const uint32_t kvb = lead_bar(B_KV);
         for (int c = 0; c < C::KCH; ++c) {
             if constexpr (PAIR) {
-                tma_load_3d_pair(sK + c * C::CHUNK, &map_k, kvb, c * 64, kt * 128, bh, l2_policy_evict_last());
-                tma_load_3d_pair(sV + c * C::CHUNK, &map_v, kvb, c * 64, kt * 128, bh, l2_policy_evict_last());
+                tma_load_3d_pair(sK + c * C::CHUNK, &map_k, kvb, c * 64, it.kt * 128, it.bh, l2_policy_evict_last());
+                tma_load_3d_pair(sV + c * C::CHUNK, &map_v, kvb, c * 64, it.kt * 128, it.bh, l2_policy_evict_last());
             } else {
-                tma_load_3d(sK + c * C::CHUNK, &map_k, kvb, c * 64, kt * 128, bh, l2_policy_evict_last());
-                tma_load_3d(sV + c * C::CHUNK, &map_v, kvb, c * 64, kt * 128, bh, l2_policy_evict_last());
+                tma_load_3d(sK + c * C::CHUNK, &map_k, kvb, c * 64, it.kt * 128, it.bh, l2_policy_evict_last());
+                tma_load_3d(sV + c * C::CHUNK, &map_v, kvb, c * 64, it.kt * 128, it.bh, l2_policy_evict_last());
             }
         }
+    };
+    // the first item's K and V do not come from the preprocess: they load before the wait for it
+    ItemSeq q0{0, 0};
+    const int w_first = next_item(q0);
+    const bool first_active = w_first < n_items && item_of(w_first).n > 0;
+    int kv_fills = 0;  // K/V loads issued (producer lane 0)
+    if (warp == C::PRODUCER && lane == 0 && first_active && !*abort_flag) {
+        load_kv(item_of(w_first));
+        kv_fills = 1;
     }
     // Launched as a programmatic dependent of the preprocess, this grid may start before D is
     // complete: every read of D comes after this wait.  Then the dQ pass launched after this grid
@@ -434,92 +489,128 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    // Every role counts the query tiles (g) and the items with at least one (a) it has taken:
+    // the per-tile barriers complete once per query tile, B_KV, B_ACC, B_KE, B_VE and B_ACCE once
+    // per item with query tiles, so their parities follow these counts.
     if (warp == C::PRODUCER) {
         // ------------------------------------------------------------ producer (whole warp)
-        if (!*abort_flag && n > 0) {
+        uint32_t issued = 0, issued_par = 0;
+        if (!*abort_flag) {
             const uint64_t pol = l2_policy_evict_last();
             if (lane == 0) {
                 tma_prefetch_desc(&map_q);
                 tma_prefetch_desc(&map_do);
             }
-            uint32_t issued = 0, issued_par = 0;
             // per-column LSE*log2(e) and D of query tile i (4 values of each per lane),
             // read from global memory one tile ahead so the load latency is off the
             // path from "stage free" to "TMA issued"
             float nl2[4], ndl[4];
-            auto fetch_vec = [&](int i) {
+            auto fetch_vec = [&](const Item& it, int i) {
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const int q = i * 128 + lane + 32 * t;
                     nl2[t] = INFINITY;
                     ndl[t] = 0.f;
-                    if (q < nq) {
-                        const float L = p.lse[(size_t)bh * p.Nq + q];
+                    if (q < it.nq) {
+                        const float L = p.lse[(size_t)it.bh * p.Nq + q];
                         nl2[t] = (L == -INFINITY) ? INFINITY : L * kLog2e;
-                        ndl[t] = p.delta[(size_t)bh * p.Nq + q];
+                        ndl[t] = p.delta[(size_t)it.bh * p.Nq + q];
                     }
                 }
             };
-            fetch_vec(i0);
-            for (int ii = 0; ii < n; ++ii) {
-                const int st = ii & 1, i = i0 + ii;
-                if (!bwait<PAIR>(B_STE + 8 * st, ((ii >> 1) & 1) ^ 1, ctl, kSiteBwdQEmpty)) break;
-                if (lane == 0) {  // byte count first (no arrival), then the copies
-                    if (lead) mbar_expect_tx(B_STF + 8 * st, (PAIR ? 4 : 2) * C::TILE);
-                    if constexpr (PAIR) {
-                        const uint32_t fb = lead_bar(B_STF + 8 * st);
-                        const int qr = i * 128 + 64 * (int)rank, fc = 64 * (int)rank;
+            bool ok = true;
+            int g = 0, a = 0;
+            for (ItemSeq q{0, 0}; ok;) {
+                const int w = next_item(q);
+                if (w >= n_items) break;
+                const Item it = item_of(w);
+                if (it.n == 0) continue;
+                if (a > 0) {  // K and V of the last item are free once its last S^T and dP^T are done
+                    if (!(ok = bwait<PAIR>(B_KE, (a - 1) & 1, ctl, kSiteBwdQEmpty))) break;
+                    if (!(ok = bwait<PAIR>(B_VE, (a - 1) & 1, ctl, kSiteBwdQEmpty))) break;
+                    if (lane == 0) {
+                        load_kv(it);
+                        ++kv_fills;
+                    }
+                } else if (!first_active && lane == 0) {
+                    load_kv(it);
+                    ++kv_fills;
+                }
+                fetch_vec(it, it.i0);
+                for (int ii = 0; ii < it.n; ++ii) {
+                    const int gi = g + ii, st = gi & 1, i = it.i0 + ii;
+                    if (!(ok = bwait<PAIR>(B_STE + 8 * st, ((gi >> 1) & 1) ^ 1, ctl, kSiteBwdQEmpty))) break;
+                    if (lane == 0) {  // byte count first (no arrival), then the copies
+                        if (lead) mbar_expect_tx(B_STF + 8 * st, (PAIR ? 4 : 2) * C::TILE);
+                        if constexpr (PAIR) {
+                            const uint32_t fb = lead_bar(B_STF + 8 * st);
+                            const int qr = i * 128 + 64 * (int)rank, fc = 64 * (int)rank;
 #pragma unroll
-                        for (int t = 0; t < 2; ++t) {
-                            const CUtensorMap* m = t ? &map_do : &map_q;
-                            const uint32_t dst = t ? sDO(st) : sQ(st);
-                            tma_load_3d_pair(dst, m, fb, 0, qr, bh, pol);                      // X0
-                            tma_load_3d_pair(dst + kQuad, m, fb, 64, qr, bh, pol);             // X1
-                            tma_load_3d_pair(dst + 2 * kQuad, m, fb, fc, i * 128, bh, pol);    // Y0
-                            tma_load_3d_pair(dst + 3 * kQuad, m, fb, fc, i * 128 + 64, bh, pol);  // Y1
-                        }
-                    } else {
-                        for (int c = 0; c < C::KCH; ++c) {
-                            tma_load_3d(sQ(st) + c * C::CHUNK, &map_q, B_STF + 8 * st, c * 64, i * 128, bh, pol);
-                            tma_load_3d(sDO(st) + c * C::CHUNK, &map_do, B_STF + 8 * st, c * 64, i * 128, bh, pol);
+                            for (int t = 0; t < 2; ++t) {
+                                const CUtensorMap* m = t ? &map_do : &map_q;
+                                const uint32_t dst = t ? sDO(st) : sQ(st);
+                                tma_load_3d_pair(dst, m, fb, 0, qr, it.bh, pol);                      // X0
+                                tma_load_3d_pair(dst + kQuad, m, fb, 64, qr, it.bh, pol);             // X1
+                                tma_load_3d_pair(dst + 2 * kQuad, m, fb, fc, i * 128, it.bh, pol);    // Y0
+                                tma_load_3d_pair(dst + 3 * kQuad, m, fb, fc, i * 128 + 64, it.bh, pol);  // Y1
+                            }
+                        } else {
+                            for (int c = 0; c < C::KCH; ++c) {
+                                tma_load_3d(sQ(st) + c * C::CHUNK, &map_q, B_STF + 8 * st, c * 64, i * 128, it.bh, pol);
+                                tma_load_3d(sDO(st) + c * C::CHUNK, &map_do, B_STF + 8 * st, c * 64, i * 128, it.bh, pol);
+                            }
                         }
                     }
-                }
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    vec[st * 256 + lane + 32 * t] = nl2[t];
-                    vec[st * 256 + 128 + lane + 32 * t] = ndl[t];
+                    for (int t = 0; t < 4; ++t) {
+                        vec[st * 256 + lane + 32 * t] = nl2[t];
+                        vec[st * 256 + 128 + lane + 32 * t] = ndl[t];
+                    }
+                    arrive_lead(B_STF + 8 * st);  // all 32 lanes, after their writes
+                    issued |= 1u << st;
+                    issued_par = (issued_par & ~(1u << st)) | ((uint32_t)((gi >> 1) & 1) << st);
+                    if (ii + 1 < it.n) fetch_vec(it, i + 1);
                 }
-                arrive_lead(B_STF + 8 * st);  // all 32 lanes, after their writes
-                issued |= 1u << st;
-                issued_par = (issued_par & ~(1u << st)) | ((uint32_t)((ii >> 1) & 1) << st);
-                if (ii + 1 < n) fetch_vec(i + 1);
+                g += it.n;
+                ++a;
             }
-            // let the loads in flight land before exit (in a pair, the even CTA's barriers
-            // count the odd CTA's loads too)
-            if (*abort_flag && lane == 0 && lead) {
-                if (kv_issued) bdrain<PAIR>(B_KV, 0, ctl, kSiteTeardown);
-                for (int st = 0; st < 2; ++st)
-                    if (issued & (1u << st))
-                        bdrain<PAIR>(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
-            }
+        }
+        // let the loads in flight land before exit (in a pair, the even CTA's barriers
+        // count the odd CTA's loads too)
+        if (*abort_flag && lane == 0 && lead) {
+            if (kv_fills > 0) bdrain<PAIR>(B_KV, (kv_fills - 1) & 1, ctl, kSiteTeardown);
+            for (int st = 0; st < 2; ++st)
+                if (issued & (1u << st))
+                    bdrain<PAIR>(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
         }
     } else if (warp == C::MMA) {
         // ------------------------------------------------------------ MMA issuer 1: S^T
         // S^T(i) once S^T(i-1) has been read out of TMEM and stage i is loaded
-        if (lane == 0 && lead && !*abort_flag && n > 0) {
-            bool ok = bwait<PAIR>(B_KV, 0, ctl, kSiteBwdKvFull);
-            for (int ii = 0; ii < n && ok; ++ii) {
-                const int st = ii & 1;
-                if (ii > 0 && !(ok = bwait<PAIR>(B_SF, (ii - 1) & 1, ctl, kSiteBwdS))) break;
-                if (!(ok = bwait<PAIR>(B_STF + 8 * st, (ii >> 1) & 1, ctl, kSiteBwdQFull))) break;
-                tc_fence_after();
-                if constexpr (PAIR)
-                    issue_ss_pair<D>(tmem + C::COL_A, sK, sQ(st));
-                else
-                    issue_ss<D>(tmem + C::COL_A, sK, sQ(st));
-                bcommit<PAIR>(B_S);
-                bcommit<PAIR>(B_STE + 8 * st);
+        if (lane == 0 && lead && !*abort_flag) {
+            bool ok = true;
+            int g = 0, a = 0;
+            for (ItemSeq q{0, 0}; ok;) {
+                const int w = next_item(q);
+                if (w >= n_items) break;
+                const Item it = item_of(w);
+                if (it.n == 0) continue;
+                if (!(ok = bwait<PAIR>(B_KV, a & 1, ctl, kSiteBwdKvFull))) break;
+                for (int ii = 0; ii < it.n; ++ii) {
+                    const int gi = g + ii, st = gi & 1;
+                    if (gi > 0 && !(ok = bwait<PAIR>(B_SF, (gi - 1) & 1, ctl, kSiteBwdS))) break;
+                    if (!(ok = bwait<PAIR>(B_STF + 8 * st, (gi >> 1) & 1, ctl, kSiteBwdQFull))) break;
+                    tc_fence_after();
+                    if constexpr (PAIR)
+                        issue_ss_pair<D>(tmem + C::COL_A, sK, sQ(st));
+                    else
+                        issue_ss<D>(tmem + C::COL_A, sK, sQ(st));
+                    bcommit<PAIR>(B_S);
+                    bcommit<PAIR>(B_STE + 8 * st);
+                }
+                if (!ok) break;
+                if constexpr (!PAIR) mma_commit(B_KE);  // this item's last product that reads K
+                g += it.n;
+                ++a;
             }
             if (*abort_flag) {
                 bcommit<PAIR>(B_TD);
@@ -529,41 +620,54 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     } else if (warp == C::MMA2) {
         // ------------------------------------------------------------ MMA issuer 2: dP^T, dV, dK
         // dV(i) and dK(i) once P^T(i) and dS^T(i) are in TMEM; dP^T(i+1) over them (this
-        // thread's products run in issue order, so it overwrites them only after both)
-        if (lane == 0 && lead && !*abort_flag && n > 0) {
-            bool ok = bwait<PAIR>(B_KV, 0, ctl, kSiteBwdKvFull);
-            if (ok) ok = bwait<PAIR>(B_STF, 0, ctl, kSiteBwdQFull);
-            if (ok) {
+        // thread's products run in issue order, so it overwrites them only after both).  An
+        // item's first dV and dK overwrite the accumulators once the last item's are stored.
+        if (lane == 0 && lead && !*abort_flag) {
+            bool ok = true;
+            int g = 0, a = 0;
+            for (ItemSeq q{0, 0}; ok;) {
+                const int w = next_item(q);
+                if (w >= n_items) break;
+                const Item it = item_of(w);
+                if (it.n == 0) continue;
+                if (!(ok = bwait<PAIR>(B_KV, a & 1, ctl, kSiteBwdKvFull))) break;
+                if (!(ok = bwait<PAIR>(B_STF + 8 * (g & 1), (g >> 1) & 1, ctl, kSiteBwdQFull))) break;
                 tc_fence_after();
                 if constexpr (PAIR)
-                    issue_ss_pair<D>(tmem + C::COL_B, sV, sDO(0));
+                    issue_ss_pair<D>(tmem + C::COL_B, sV, sDO(g & 1));
                 else
-                    issue_ss<D>(tmem + C::COL_B, sV, sDO(0));
+                    issue_ss<D>(tmem + C::COL_B, sV, sDO(g & 1));
                 bcommit<PAIR>(B_DP);
-            }
-            for (int ii = 0; ii < n && ok; ++ii) {
-                const int st = ii & 1;
-                if (!(ok = bwait<PAIR>(B_DS, ii & 1, ctl, kSiteBwdDS))) break;
-                tc_fence_after();
-                if constexpr (PAIR) {
-                    issue_ts_pair<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sDO(st) + 2 * kQuad, ii > 0);      // dV
-                    issue_ts_pair<D>(tmem + C::COL_ACC1, tmem + C::COL_B + 32, sQ(st) + 2 * kQuad, ii > 0);  // dK
-                } else {
-                    issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sDO(st), ii > 0);      // dV += P^T dO
-                    issue_ts<D>(tmem + C::COL_ACC1, tmem + C::COL_B + 32, sQ(st), ii > 0);  // dK += dS^T Q
-                }
-                bcommit<PAIR>(B_STE + 8 * st);
-                if (ii + 1 < n) {
-                    if (!(ok = bwait<PAIR>(B_STF + 8 * (st ^ 1), ((ii + 1) >> 1) & 1, ctl, kSiteBwdQFull))) break;
+                if (!PAIR && it.n == 1) mma_commit(B_VE);  // the item's last product that reads V
+                for (int ii = 0; ii < it.n; ++ii) {
+                    const int gi = g + ii, st = gi & 1;
+                    if (!(ok = bwait<PAIR>(B_DS, gi & 1, ctl, kSiteBwdDS))) break;
+                    if (ii == 0 && a > 0 && !(ok = bwait<PAIR>(B_ACCE, (a - 1) & 1, ctl, kSiteBwdDone))) break;
                     tc_fence_after();
-                    if constexpr (PAIR)
-                        issue_ss_pair<D>(tmem + C::COL_B, sV, sDO(st ^ 1));
-                    else
-                        issue_ss<D>(tmem + C::COL_B, sV, sDO(st ^ 1));  // dP^T of the next query tile
-                    bcommit<PAIR>(B_DP);
+                    if constexpr (PAIR) {
+                        issue_ts_pair<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sDO(st) + 2 * kQuad, ii > 0);      // dV
+                        issue_ts_pair<D>(tmem + C::COL_ACC1, tmem + C::COL_B + 32, sQ(st) + 2 * kQuad, ii > 0);  // dK
+                    } else {
+                        issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sDO(st), ii > 0);      // dV += P^T dO
+                        issue_ts<D>(tmem + C::COL_ACC1, tmem + C::COL_B + 32, sQ(st), ii > 0);  // dK += dS^T Q
+                    }
+                    bcommit<PAIR>(B_STE + 8 * st);
+                    if (ii + 1 < it.n) {
+                        if (!(ok = bwait<PAIR>(B_STF + 8 * (st ^ 1), ((gi + 1) >> 1) & 1, ctl, kSiteBwdQFull))) break;
+                        tc_fence_after();
+                        if constexpr (PAIR)
+                            issue_ss_pair<D>(tmem + C::COL_B, sV, sDO(st ^ 1));
+                        else
+                            issue_ss<D>(tmem + C::COL_B, sV, sDO(st ^ 1));  // dP^T of the next query tile
+                        bcommit<PAIR>(B_DP);
+                        if (!PAIR && ii + 2 == it.n) mma_commit(B_VE);  // the item's last product that reads V
+                    }
                 }
+                if (!ok) break;
+                bcommit<PAIR>(B_ACC);
+                g += it.n;
+                ++a;
             }
-            if (ok) bcommit<PAIR>(B_ACC);
             if (*abort_flag) {
                 bcommit<PAIR>(B_TD2);
                 bdrain<PAIR>(B_TD2, 0, ctl, kSiteTeardown);
@@ -574,9 +678,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         // Two warpgroups: warpgroup h handles query columns [64h, 64h + 64) of every key row.
         const int h = warp >> 2;
         const int r = ((warp & 3) << 5) + lane;  // key row within the tile = TMEM lane
-        const int kg = kt * 128 + r;
-        const bool row_ok = kg < p.Nk;   // stored (zeros past the sequence)
-        const bool key_ok = kg < nk;     // a key of the sequence
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t colA = C::COL_A + 64 * h, colB = C::COL_B + 64 * h;
         const float sc = p.scale_log2;
@@ -596,98 +697,113 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
         };
         bool ok = true;
-        for (int ii = 0; ii < n; ++ii) {
-            const int st = ii & 1, i = i0 + ii;
-            const float* l2 = vec + st * 256 + 64 * h;
-            const float* dl = l2 + 128;
-            // key kg is visible to query q iff kg <= q + off, i.e. column c >= cmin
-            const int cmin = p.causal ? kg - off - i * 128 - 64 * h : -1;
-            if (!(ok = wait_c(B_S, ii & 1, kSiteBwdS))) break;
-            tc_fence_after();
-            uint32_t pp[32];
-            uint32_t va[32], vb[32];
-            // read this warpgroup's 64 S^T columns, then release them: the next S^T may overwrite
-            tmem_ld32_async(lane_addr + colA, va);
-            tmem_ld32_async(lane_addr + colA + 32, vb);
-            tmem_wait_ld(va);
-            tmem_wait_ld(vb);
-            tc_fence_before();
-            arrive_c(B_SF);
-            // masked entries: rows past Nk (whole row) and, causal, columns c < cmin.
-            // Tiles with none in the warp take the instantiation without the test.
-            const int cmin_eff = key_ok ? cmin : (1 << 30);
-            // sliding window: queries c > cmax_w no longer see key kg
-            const int cmax_w = p.window > 0 ? kg - off + p.window - 1 - i * 128 - 64 * h : (1 << 30);
-            auto p_phase = [&](auto MASK) {
+        int g = 0, a = 0;
+        for (ItemSeq q{0, 0}; ok;) {
+            const int w = next_item(q);
+            if (w >= n_items) break;
+            const Item it = item_of(w);
+            const int kg = it.kt * 128 + r;
+            const bool row_ok = kg < p.Nk;    // stored (zeros past the sequence)
+            const bool key_ok = kg < it.nk;   // a key of the sequence
+            const int off = it.off;
+            for (int ii = 0; ii < it.n; ++ii) {
+                const int gi = g + ii, st = gi & 1, i = it.i0 + ii;
+                const float* l2 = vec + st * 256 + 64 * h;
+                const float* dl = l2 + 128;
+                // key kg is visible to query q iff kg <= q + off, i.e. column c >= cmin
+                const int cmin = p.causal ? kg - off - i * 128 - 64 * h : -1;
+                if (!(ok = wait_c(B_S, gi & 1, kSiteBwdS))) break;
+                tc_fence_after();
+                uint32_t pp[32];
+                uint32_t va[32], vb[32];
+                // read this warpgroup's 64 S^T columns, then release them: the next S^T may overwrite
+                tmem_ld32_async(lane_addr + colA, va);
+                tmem_ld32_async(lane_addr + colA + 32, vb);
+                tmem_wait_ld(va);
+                tmem_wait_ld(vb);
+                tc_fence_before();
+                arrive_c(B_SF);
+                // masked entries: rows past Nk (whole row) and, causal, columns c < cmin.
+                // Tiles with none in the warp take the instantiation without the test.
+                const int cmin_eff = key_ok ? cmin : (1 << 30);
+                // sliding window: queries c > cmax_w no longer see key kg
+                const int cmax_w = p.window > 0 ? kg - off + p.window - 1 - i * 128 - 64 * h : (1 << 30);
+                auto p_phase = [&](auto MASK) {
 #pragma unroll
-            for (int q4 = 0; q4 < 2; ++q4) {
-                uint32_t(&v)[32] = q4 ? vb : va;
-                float lv[32];
+                for (int q4 = 0; q4 < 2; ++q4) {
+                    uint32_t(&v)[32] = q4 ? vb : va;
+                    float lv[32];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float4 t = reinterpret_cast<const float4*>(l2 + q4 * 32)[e];
-                    lv[4 * e] = t.x, lv[4 * e + 1] = t.y, lv[4 * e + 2] = t.z, lv[4 * e + 3] = t.w;
-                }
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int c0 = q4 * 32 + 2 * e;
-                    const float2 x = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
-                                           make_float2(sc, sc), make_float2(-lv[2 * e], -lv[2 * e + 1]));
-                    float a = ex2(x.x), b = ex2(x.y);
-                    if constexpr (decltype(MASK)::value) {
-                        if (c0 < cmin_eff || c0 > cmax_w) a = 0.f;
-                        if (c0 + 1 < cmin_eff || c0 + 1 > cmax_w) b = 0.f;
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 t = reinterpret_cast<const float4*>(l2 + q4 * 32)[e];
+                        lv[4 * e] = t.x, lv[4 * e + 1] = t.y, lv[4 * e + 2] = t.z, lv[4 * e + 3] = t.w;
                     }
-                    pp[q4 * 16 + e] = pack_bf16(a, b);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c0 = q4 * 32 + 2 * e;
+                        const float2 x = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                               make_float2(sc, sc), make_float2(-lv[2 * e], -lv[2 * e + 1]));
+                        float a = ex2(x.x), b = ex2(x.y);
+                        if constexpr (decltype(MASK)::value) {
+                            if (c0 < cmin_eff || c0 > cmax_w) a = 0.f;
+                            if (c0 + 1 < cmin_eff || c0 + 1 > cmax_w) b = 0.f;
+                        }
+                        pp[q4 * 16 + e] = pack_bf16(a, b);
+                    }
                 }
+                };
+                if (__any_sync(0xffffffffu, cmin_eff > 0 || cmax_w < 63))
+                    p_phase(std::true_type{});
+                else
+                    p_phase(std::false_type{});
+                if (!(ok = wait_c(B_DP, gi & 1, kSiteBwdDP))) break;
+                tc_fence_after();
+                // this warpgroup's 64 dP^T columns; once both chunks are in registers, its bf16 P^T
+                // goes over the first 32 of them and dS^T over the last 32
+                tmem_ld32_async(lane_addr + colB, va);
+                tmem_ld32_async(lane_addr + colB + 32, vb);
+                tmem_wait_ld(va);
+                tmem_wait_ld(vb);
+                tmem_st32_async(lane_addr + colB, pp);
+#pragma unroll
+                for (int q4 = 0; q4 < 2; ++q4) {
+                    uint32_t(&v)[32] = q4 ? vb : va;
+                    float dv[32];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 t = reinterpret_cast<const float4*>(dl + q4 * 32)[e];
+                        dv[4 * e] = t.x, dv[4 * e + 1] = t.y, dv[4 * e + 2] = t.z, dv[4 * e + 3] = t.w;
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint32_t pr = pp[q4 * 16 + e];
+                        const float a = bf_lo(pr) * (__uint_as_float(v[2 * e]) - dv[2 * e]);
+                        const float b = bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dv[2 * e + 1]);
+                        pk[e] = pack_bf16(a, b);
+                    }
+                    tmem_st16_async(lane_addr + colB + 32 + q4 * 16, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                arrive_c(B_DS);
             }
-            };
-            if (__any_sync(0xffffffffu, cmin_eff > 0 || cmax_w < 63))
-                p_phase(std::true_type{});
-            else
-                p_phase(std::false_type{});
-            if (!(ok = wait_c(B_DP, ii & 1, kSiteBwdDP))) break;
-            tc_fence_after();
-            // this warpgroup's 64 dP^T columns; once both chunks are in registers, its bf16 P^T
-            // goes over the first 32 of them and dS^T over the last 32
-            tmem_ld32_async(lane_addr + colB, va);
-            tmem_ld32_async(lane_addr + colB + 32, vb);
-            tmem_wait_ld(va);
-            tmem_wait_ld(vb);
-            tmem_st32_async(lane_addr + colB, pp);
-#pragma unroll
-            for (int q4 = 0; q4 < 2; ++q4) {
-                uint32_t(&v)[32] = q4 ? vb : va;
-                float dv[32];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float4 t = reinterpret_cast<const float4*>(dl + q4 * 32)[e];
-                    dv[4 * e] = t.x, dv[4 * e + 1] = t.y, dv[4 * e + 2] = t.z, dv[4 * e + 3] = t.w;
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const uint32_t pr = pp[q4 * 16 + e];
-                    const float a = bf_lo(pr) * (__uint_as_float(v[2 * e]) - dv[2 * e]);
-                    const float b = bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dv[2 * e + 1]);
-                    pk[e] = pack_bf16(a, b);
-                }
-                tmem_st16_async(lane_addr + colB + 32 + q4 * 16, pk);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            arrive_c(B_DS);
-        }
-        if (ok) {
-            bool have = n > 0;
+            if (!ok) break;
+            const bool have = it.n > 0;
             if (have) {
-                ok = wait_c(B_ACC, 0, kSiteBwdDone);
+                if (!(ok = wait_c(B_ACC, a & 1, kSiteBwdDone))) break;
                 tc_fence_after();
             }
-            if (ok) {
-                const size_t base = ((size_t)bh * p.Nk + (row_ok ? kg : 0)) * D;
-                store_acc_row<D>(lane_addr + C::COL_ACC0, p.dv + base, 1.f, row_ok, !have, h * (D / 2));
-                store_acc_row<D>(lane_addr + C::COL_ACC1, p.dk + base, p.scale, row_ok, !have, h * (D / 2));
+            const size_t base = ((size_t)it.bh * p.Nk + (row_ok ? kg : 0)) * D;
+            store_acc_row<D>(lane_addr + C::COL_ACC0, p.dv + base, 1.f, row_ok, !have, h * (D / 2));
+            store_acc_row<D>(lane_addr + C::COL_ACC1, p.dk + base, p.scale, row_ok, !have, h * (D / 2));
+            if (have) {
+                if constexpr (!PAIR) {  // the accumulators are read out: the next item may overwrite them
+                    tc_fence_before();
+                    mbar_arrive(B_ACCE);
+                }
+                g += it.n;
+                ++a;
             }
         }
     }
@@ -1404,7 +1520,9 @@ cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t s, bool after_pre) {
     if (e != cudaSuccess) return e;
     const BwdParams p = make_params(a);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(PAIR ? 2 * p.n_pt * p.BH : p.n_kt * p.BH));
+    // one CTA per SM at most (persistent over key tiles); a pair per key-tile pair
+    const int n_items = p.n_kt * p.BH;
+    cfg.gridDim = dim3((unsigned)(PAIR ? 2 * p.n_pt * p.BH : std::min(n_items, std::max(1, a.num_sms))));
     cfg.blockDim = dim3(C::THREADS_DKDV);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;

@@ -136,7 +136,10 @@ __device__ __forceinline__ void fwd_decode(const FwdParams& p, int w, int& bh, i
 // instantiated only for the blocks that hold a masked column.
 template <bool MASKED>
 __device__ __forceinline__ float row_max_pass(uint32_t taddr, int lim2, int lo2) {
-    float mraw = -INFINITY;
+    // eight running maxima, so that the 64 max instructions form eight short dependency chains
+    float mx[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
     uint32_t va[32], vb[32];
     tmem_ld32_async(taddr, va);
     tmem_wait_ld(va);
@@ -152,11 +155,11 @@ __device__ __forceinline__ float row_max_pass(uint32_t taddr, int lim2, int lo2)
                 if (q4 * 32 + i > lim2 || q4 * 32 + i < lo2) x0 = -INFINITY;
                 if (q4 * 32 + i + 1 > lim2 || q4 * 32 + i + 1 < lo2) x1 = -INFINITY;
             }
-            mraw = fmax3(mraw, x0, x1);
+            mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], x0, x1);
         }
         if (q4 + 1 < 4) tmem_wait_ld(nx);
     }
-    return mraw;
+    return fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
 }
 
 // Pass 2: p = 2^(s c - m) for the 128 columns, their sum, and bf16 P written
@@ -165,7 +168,9 @@ __device__ __forceinline__ float row_max_pass(uint32_t taddr, int lim2, int lo2)
 // of columns >= 32 (q + 1)), or to columns of its own.
 template <bool MASKED>
 __device__ __forceinline__ float exp_pass(uint32_t taddr, uint32_t paddr, int lim2, int lo2, float c, float msub) {
-    float2 rs = make_float2(0.f, 0.f);
+    float2 rs[4];  // four partial sums (short dependency chains), added at the end
+#pragma unroll
+    for (int k = 0; k < 4; ++k) rs[k] = make_float2(0.f, 0.f);
     const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
     uint32_t va[32], vb[32];
     tmem_ld32_async(taddr, va);
@@ -185,14 +190,15 @@ __device__ __forceinline__ float exp_pass(uint32_t taddr, uint32_t paddr, int li
             }
             const float2 x = ffma2(make_float2(s0, s1), c2, nm2);  // s*c - m, two lanes
             const float2 e = make_float2(ex2(x.x), ex2(x.y));
-            rs = fadd2(rs, e);
+            rs[i & 3] = fadd2(rs[i & 3], e);
             pk[i] = pack_bf16(e.x, e.y);
         }
         tmem_st16_async(paddr + q4 * 16, pk);
         if (q4 + 1 < 4) tmem_wait_ld(nx);
     }
     tmem_wait_st();
-    return rs.x + rs.y;
+    const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+    return (r01.x + r23.x) + (r01.y + r23.y);
 }
 
 // WIN: the sliding-window variant; VL: per-sequence lengths (rows past a

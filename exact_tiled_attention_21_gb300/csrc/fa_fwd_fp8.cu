@@ -119,7 +119,10 @@ __device__ __forceinline__ void f8_decode(const F8Params& p, int w, int& bh, int
 // Row maximum of the raw scores of one 128-column S row (thread = row).
 template <bool MASKED>
 __device__ __forceinline__ float f8_row_max(uint32_t taddr, int lim2) {
-    float mraw = -INFINITY;
+    // eight running maxima, so that the 64 max instructions form eight short dependency chains
+    float mx[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
     uint32_t va[32], vb[32];
     tmem_ld32_async(taddr, va);
     tmem_wait_ld(va);
@@ -135,18 +138,20 @@ __device__ __forceinline__ float f8_row_max(uint32_t taddr, int lim2) {
                 if (q4 * 32 + i > lim2) x0 = -INFINITY;
                 if (q4 * 32 + i + 1 > lim2) x1 = -INFINITY;
             }
-            mraw = fmax3(mraw, x0, x1);
+            mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], x0, x1);
         }
         if (q4 + 1 < 4) tmem_wait_ld(nx);
     }
-    return mraw;
+    return fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
 }
 
 // p = 2^(s c - m) for the 128 columns, their sum, and P as e4m3 into the
 // thread's row of the P tile (16-byte granule g at g ^ (r & 7)).
 template <bool MASKED>
 __device__ __forceinline__ float f8_exp_row(uint32_t taddr, int lim2, float c, float msub, uint8_t* prow, int r) {
-    float2 rs = make_float2(0.f, 0.f);
+    float2 rs[4];  // four partial sums (short dependency chains), added at the end
+#pragma unroll
+    for (int k = 0; k < 4; ++k) rs[k] = make_float2(0.f, 0.f);
     const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
     uint32_t va[32], vb[32];
     tmem_ld32_async(taddr, va);
@@ -171,7 +176,7 @@ __device__ __forceinline__ float f8_exp_row(uint32_t taddr, int lim2, float c, f
                 const float2 x = ffma2(make_float2(s0, s1), c2, nm2);
                 e[u] = ex2(x.x);
                 e[u + 1] = ex2(x.y);
-                rs = fadd2(rs, make_float2(e[u], e[u + 1]));
+                rs[(2 * w + u / 2) & 3] = fadd2(rs[(2 * w + u / 2) & 3], make_float2(e[u], e[u + 1]));
             }
             pk[w] = pack_e4m3x4(e[0], e[1], e[2], e[3]);
         }
@@ -183,7 +188,8 @@ __device__ __forceinline__ float f8_exp_row(uint32_t taddr, int lim2, float c, f
         }
         if (q4 + 1 < 4) tmem_wait_ld(nx);
     }
-    return rs.x + rs.y;
+    const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+    return (r01.x + r23.x) + (r01.y + r23.y);
 }
 
 __global__ void __launch_bounds__(F8::THREADS, 1)
