@@ -98,6 +98,31 @@ __device__ __forceinline__ void chunked_order(int idx, int n_t, int BH, int hc, 
     bh = h0 + (r - t * hn);
 }
 
+// Item sequence of a persistent CTA (one per SM at most) over n_items work items
+// in the chunked order (chunks of chunk_items): within each chunk the CTAs take
+// the items round by round, alternating direction (round r: r*G + c, or
+// r*G + G-1-c), odd chunks starting reversed, so that the rounds' long and
+// short items even out per CTA.  With chunks smaller than the grid the rounds
+// run over the whole order instead.  Returns n_items once the CTA has no more.
+struct ItemSeq {
+    int ci = 0, rd = 0;  // chunk, and round within it
+};
+__device__ __forceinline__ int next_chunked_item(ItemSeq& q, int n_items, int chunk_items) {
+    const int G = gridDim.x, c = blockIdx.x;
+    if (chunk_items < G) return min(n_items, persistent_work(q.rd++, c, G));
+    for (;;) {
+        const int start = q.ci * chunk_items;
+        if (start >= n_items) return n_items;
+        const int wl = q.rd * G + (((q.rd + q.ci) & 1) ? G - 1 - c : c);
+        if (wl < min(chunk_items, n_items - start)) {
+            ++q.rd;
+            return start + wl;
+        }
+        ++q.ci;
+        q.rd = 0;
+    }
+}
+
 // Query and key counts of head bh's sequence (per-sequence lengths clamped to
 // [0, Nq] and [0, Nk]; the forward records lengths out of range).  Rows and
 // keys past them are padding: their LSE reads as -inf (P = 0), key columns are
@@ -394,36 +419,17 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Work items: key tiles (in a pair, key-tile pairs) in the chunked order (key tile 0, the most
-    // query tiles when causal, first; heads in L2-sized chunks).  A single CTA is persistent and,
-    // while its compute warps store one item's dK and dV, already loads the next item's K, V and
-    // first query tiles and runs its first score products.  Within each chunk the CTAs take the
-    // items round by round, alternating direction (round r: r*G + c, or r*G + G-1-c), odd chunks
-    // starting reversed, so that the rounds' long and short items even out per CTA; with chunks
-    // smaller than the grid the rounds run over the whole order instead.  A pair takes the one
-    // item of its cluster.
+    // query tiles when causal, first; heads in L2-sized chunks).  A single CTA is persistent
+    // (next_chunked_item) and, while its compute warps store one item's dK and dV, already loads
+    // the next item's K, V and first query tiles and runs its first score products.  A pair
+    // takes the one item of its cluster.
     const int n_items = PAIR ? p.n_pt * p.BH : p.n_kt * p.BH;
     const int chunk_items = p.hc_kv * p.n_kt;
-    struct ItemSeq {
-        int ci, rd;  // chunk and round within it
-    };
     auto next_item = [&](ItemSeq& q) -> int {
-        if constexpr (PAIR) {
+        if constexpr (PAIR)
             return q.rd++ == 0 ? (int)(blockIdx.x >> 1) : n_items;
-        } else {
-            const int G = gridDim.x, c = blockIdx.x;
-            if (chunk_items < G) return min(n_items, persistent_work(q.rd++, c, G));
-            for (;;) {
-                const int start = q.ci * chunk_items;
-                if (start >= n_items) return n_items;
-                const int wl = q.rd * G + (((q.rd + q.ci) & 1) ? G - 1 - c : c);
-                if (wl < min(chunk_items, n_items - start)) {
-                    ++q.rd;
-                    return start + wl;
-                }
-                ++q.ci;
-                q.rd = 0;
-            }
-        }
+        else
+            return next_chunked_item(q, n_items, chunk_items);
     };
     struct Item {
         int bh, kt, nq, nk, off, i0, n;  // n query tiles from i0 (the union of a pair's two key tiles)
@@ -475,7 +481,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
     };
     // the first item's K and V do not come from the preprocess: they load before the wait for it
-    ItemSeq q0{0, 0};
+    ItemSeq q0;
     const int w_first = next_item(q0);
     const bool first_active = w_first < n_items && item_of(w_first).n > 0;
     int kv_fills = 0;  // K/V loads issued (producer lane 0)
@@ -520,7 +526,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             };
             bool ok = true;
             int g = 0, a = 0;
-            for (ItemSeq q{0, 0}; ok;) {
+            for (ItemSeq q; ok;) {
                 const int w = next_item(q);
                 if (w >= n_items) break;
                 const Item it = item_of(w);
@@ -589,7 +595,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         if (lane == 0 && lead && !*abort_flag) {
             bool ok = true;
             int g = 0, a = 0;
-            for (ItemSeq q{0, 0}; ok;) {
+            for (ItemSeq q; ok;) {
                 const int w = next_item(q);
                 if (w >= n_items) break;
                 const Item it = item_of(w);
@@ -625,7 +631,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         if (lane == 0 && lead && !*abort_flag) {
             bool ok = true;
             int g = 0, a = 0;
-            for (ItemSeq q{0, 0}; ok;) {
+            for (ItemSeq q; ok;) {
                 const int w = next_item(q);
                 if (w >= n_items) break;
                 const Item it = item_of(w);
@@ -698,7 +704,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         };
         bool ok = true;
         int g = 0, a = 0;
-        for (ItemSeq q{0, 0}; ok;) {
+        for (ItemSeq q; ok;) {
             const int w = next_item(q);
             if (w >= n_items) break;
             const Item it = item_of(w);
@@ -743,12 +749,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                         const int c0 = q4 * 32 + 2 * e;
                         const float2 x = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
                                                make_float2(sc, sc), make_float2(-lv[2 * e], -lv[2 * e + 1]));
-                        float a = ex2(x.x), b = ex2(x.y);
+                        float pa = ex2(x.x), pb = ex2(x.y);
                         if constexpr (decltype(MASK)::value) {
-                            if (c0 < cmin_eff || c0 > cmax_w) a = 0.f;
-                            if (c0 + 1 < cmin_eff || c0 + 1 > cmax_w) b = 0.f;
+                            if (c0 < cmin_eff || c0 > cmax_w) pa = 0.f;
+                            if (c0 + 1 < cmin_eff || c0 + 1 > cmax_w) pb = 0.f;
                         }
-                        pp[q4 * 16 + e] = pack_bf16(a, b);
+                        pp[q4 * 16 + e] = pack_bf16(pa, pb);
                     }
                 }
                 };
@@ -778,9 +784,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const uint32_t pr = pp[q4 * 16 + e];
-                        const float a = bf_lo(pr) * (__uint_as_float(v[2 * e]) - dv[2 * e]);
-                        const float b = bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dv[2 * e + 1]);
-                        pk[e] = pack_bf16(a, b);
+                        const float da = bf_lo(pr) * (__uint_as_float(v[2 * e]) - dv[2 * e]);
+                        const float db = bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dv[2 * e + 1]);
+                        pk[e] = pack_bf16(da, db);
                     }
                     tmem_st16_async(lane_addr + colB + 32 + q4 * 16, pk);
                 }
@@ -836,45 +842,68 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const uint32_t tmem = bwd_setup<D>(smem, bar0, ctl, counts, 13);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int bh, mr;  // causal: late query tiles (most keys) first, heads in L2-sized chunks
-    chunked_order(blockIdx.x, p.n_qt, p.BH, p.hc_q, bh, mr);
-    const int it = p.causal ? p.n_qt - 1 - mr : mr;  // causal: late query tiles (most keys) first
-    int nq, nk;
-    bwd_seqlen(p, bh, nq, nk);
-    const int off = nk - nq;
-    int n = it * 128 < nq ? (nk + 127) / 128 : 0;  // a tile wholly past the sequence only stores zeros
-    if (p.causal && n > 0) {
-        const int qmax = min(it * 128 + 127, nq - 1);
-        const long long lim = (long long)qmax + off;
-        n = lim < 0 ? 0 : min(n, (int)(lim / 128) + 1);
-    }
-    int jlo = 0;  // sliding window: first key tile the tile's first query sees
-    if (p.window > 0) {
-        const long long lo = (long long)it * 128 + off - p.window + 1;
-        jlo = lo <= 0 ? 0 : (int)min((long long)n, lo / 128);
-    }
-    n -= jlo;
+    // Work items: query tiles in the chunked order (causal: late query tiles, the most keys,
+    // first; heads in L2-sized chunks), taken persistently as the dK/dV pass takes its key tiles.
+    // The K/V ring runs on across items, so the next item's first key tiles load while this one
+    // finishes.
+    const int n_items = p.n_qt * p.BH;
+    const int chunk_items = p.hc_q * p.n_qt;
+    struct Item {
+        int bh, it, nq, nk, off, n, jlo;  // n key tiles from jlo
+    };
+    auto item_of = [&](int w) {
+        Item t;
+        int mr;
+        chunked_order(w, p.n_qt, p.BH, p.hc_q, t.bh, mr);
+        t.it = p.causal ? p.n_qt - 1 - mr : mr;  // causal: late query tiles (most keys) first
+        bwd_seqlen(p, t.bh, t.nq, t.nk);
+        t.off = t.nk - t.nq;
+        int n = t.it * 128 < t.nq ? (t.nk + 127) / 128 : 0;  // a tile wholly past the sequence only stores zeros
+        if (p.causal && n > 0) {
+            const int qmax = min(t.it * 128 + 127, t.nq - 1);
+            const long long lim = (long long)qmax + t.off;
+            n = lim < 0 ? 0 : min(n, (int)(lim / 128) + 1);
+        }
+        int jlo = 0;  // sliding window: first key tile the tile's first query sees
+        if (p.window > 0) {
+            const long long lo = (long long)t.it * 128 + t.off - p.window + 1;
+            jlo = lo <= 0 ? 0 : (int)min((long long)n, lo / 128);
+        }
+        t.jlo = jlo;
+        t.n = n - jlo;
+        return t;
+    };
     static_assert(NST * 2 * C::TILE <= C::OFF_VEC, "K/V stages fit below the vector region");
     auto sK = [&](int st) { return s_base + st * 2 * C::TILE; };
     auto sV = [&](int st) { return s_base + st * 2 * C::TILE + C::TILE; };
 
+    // Every role counts the key tiles (g) and the items with at least one (a) it has taken: the
+    // ring and the per-tile barriers follow g, B_QA and B_ACC follow a.
     if (warp == C::PRODUCER) {
-        if (lane == 0 && !*abort_flag && n > 0) {
+        if (lane == 0 && !*abort_flag) {
             const uint64_t pol = l2_policy_evict_last();
             tma_prefetch_desc(&map_k);
             tma_prefetch_desc(&map_v);
             uint32_t issued = 0, issued_par = 0;
-            for (int jj = 0; jj < n; ++jj) {
-                const int st = jj % NST;
-                const uint32_t ph = (uint32_t)((jj / NST) & 1);
-                if (!mbar_wait(B_STE + 8 * st, ph ^ 1, ctl, kSiteBwdQEmpty)) break;
-                mbar_arrive_expect_tx(B_STF + 8 * st, 2 * C::TILE);
-                for (int c = 0; c < C::KCH; ++c) {
-                    tma_load_3d(sK(st) + c * C::CHUNK, &map_k, B_STF + 8 * st, c * 64, (jlo + jj) * 128, bh, pol);
-                    tma_load_3d(sV(st) + c * C::CHUNK, &map_v, B_STF + 8 * st, c * 64, (jlo + jj) * 128, bh, pol);
+            bool ok = true;
+            int g = 0;
+            for (ItemSeq q; ok;) {
+                const int w = next_chunked_item(q, n_items, chunk_items);
+                if (w >= n_items) break;
+                const Item t = item_of(w);
+                for (int jj = 0; jj < t.n; ++jj) {
+                    const int gj = g + jj, st = gj % NST;
+                    const uint32_t ph = (uint32_t)((gj / NST) & 1);
+                    if (!(ok = mbar_wait(B_STE + 8 * st, ph ^ 1, ctl, kSiteBwdQEmpty))) break;
+                    mbar_arrive_expect_tx(B_STF + 8 * st, 2 * C::TILE);
+                    for (int c = 0; c < C::KCH; ++c) {
+                        tma_load_3d(sK(st) + c * C::CHUNK, &map_k, B_STF + 8 * st, c * 64, (t.jlo + jj) * 128, t.bh, pol);
+                        tma_load_3d(sV(st) + c * C::CHUNK, &map_v, B_STF + 8 * st, c * 64, (t.jlo + jj) * 128, t.bh, pol);
+                    }
+                    issued |= 1u << st;
+                    issued_par = (issued_par & ~(1u << st)) | (ph << st);
                 }
-                issued |= 1u << st;
-                issued_par = (issued_par & ~(1u << st)) | (ph << st);
+                g += t.n;
             }
             if (*abort_flag) {
                 for (int st = 0; st < NST; ++st)
@@ -882,36 +911,47 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             }
         }
     } else if (warp == C::MMA) {
-        if (lane == 0 && !*abort_flag && n > 0) {
-            bool ok = mbar_wait(B_QA, 0, ctl, kSiteBwdQFull);
-            if (ok) ok = mbar_wait(B_STF, 0, ctl, kSiteBwdKvFull);
-            if (ok) {
+        if (lane == 0 && !*abort_flag) {
+            bool ok = true;
+            int g = 0, a = 0;
+            for (ItemSeq q; ok;) {
+                const int w = next_chunked_item(q, n_items, chunk_items);
+                if (w >= n_items) break;
+                const Item t = item_of(w);
+                if (t.n == 0) continue;
+                // Q and dO of this item in TMEM; written after every product of the last item
+                // (which read them, and its dQ) is done and its dQ has been read out
+                if (!(ok = mbar_wait(B_QA, a & 1, ctl, kSiteBwdQFull))) break;
+                if (!(ok = mbar_wait(B_STF + 8 * (g % NST), (g / NST) & 1, ctl, kSiteBwdKvFull))) break;
                 tc_fence_after();
-                issue_ts_k<D>(tmem + C::COL_A, tmem + COL_QA, sK(0));   // S = Q K^T, Q from TMEM
+                issue_ts_k<D>(tmem + C::COL_A, tmem + COL_QA, sK(g % NST));   // S = Q K^T, Q from TMEM
                 mma_commit(B_S);
-                issue_ts_k<D>(tmem + C::COL_B, tmem + COL_DOA, sV(0));  // dP = dO V^T, dO from TMEM
+                issue_ts_k<D>(tmem + C::COL_B, tmem + COL_DOA, sV(g % NST));  // dP = dO V^T, dO from TMEM
                 mma_commit(B_DP);
-            }
-            for (int jj = 0; jj < n && ok; ++jj) {
-                const int st = jj % NST, stn = (jj + 1) % NST;
-                const bool more = jj + 1 < n;
-                if (more) {
-                    if (!(ok = mbar_wait(B_SF, jj & 1, ctl, kSiteBwdP))) break;
-                    if (!(ok = mbar_wait(B_STF + 8 * stn, ((jj + 1) / NST) & 1, ctl, kSiteBwdKvFull))) break;
+                for (int jj = 0; jj < t.n; ++jj) {
+                    const int gj = g + jj, st = gj % NST, stn = (gj + 1) % NST;
+                    const bool more = jj + 1 < t.n;
+                    if (more) {
+                        if (!(ok = mbar_wait(B_SF, gj & 1, ctl, kSiteBwdP))) break;
+                        if (!(ok = mbar_wait(B_STF + 8 * stn, ((gj + 1) / NST) & 1, ctl, kSiteBwdKvFull))) break;
+                        tc_fence_after();
+                        issue_ts_k<D>(tmem + C::COL_A, tmem + COL_QA, sK(stn));
+                        mma_commit(B_S);
+                    }
+                    if (!(ok = mbar_wait(B_DS, gj & 1, ctl, kSiteBwdDS))) break;
                     tc_fence_after();
-                    issue_ts_k<D>(tmem + C::COL_A, tmem + COL_QA, sK(stn));
-                    mma_commit(B_S);
+                    issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sK(st), jj > 0);  // dQ += dS K
+                    mma_commit(B_STE + 8 * st);
+                    if (more) {
+                        issue_ts_k<D>(tmem + C::COL_B, tmem + COL_DOA, sV(stn));
+                        mma_commit(B_DP);
+                    }
                 }
-                if (!(ok = mbar_wait(B_DS, jj & 1, ctl, kSiteBwdDS))) break;
-                tc_fence_after();
-                issue_ts<D>(tmem + C::COL_ACC0, tmem + C::COL_B, sK(st), jj > 0);  // dQ += dS K
-                mma_commit(B_STE + 8 * st);
-                if (more) {
-                    issue_ts_k<D>(tmem + C::COL_B, tmem + COL_DOA, sV(stn));
-                    mma_commit(B_DP);
-                }
+                if (!ok) break;
+                mma_commit(B_ACC);
+                g += t.n;
+                ++a;
             }
-            if (ok) mma_commit(B_ACC);
             if (*abort_flag) {
                 mma_commit(B_TD);
                 mbar_drain(B_TD, 0, ctl, kSiteTeardown);
@@ -921,112 +961,136 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         // Two warpgroups: warpgroup h handles key columns [64h, 64h + 64) of every query row.
         const int h = warp >> 2;
         const int r = ((warp & 3) << 5) + lane;  // query row within the tile = TMEM lane
-        const int qg = it * 128 + r;
-        const bool row_ok = qg < p.Nq;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t colA = C::COL_A + 64 * h, colB = C::COL_B + 64 * h;
-        float l2 = INFINITY, dl = 0.f;
-        if (qg < nq) {  // a row past the sequence keeps P = 0
-            const float L = p.lse[(size_t)bh * p.Nq + qg];
-            l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
-            dl = p.delta[(size_t)bh * p.Nq + qg];
-        }
         const float sc = p.scale_log2;
-        const int lim_row = p.causal ? min(qg + off, nk - 1) : nk - 1;  // last key this row sees
-        // Q_i and dO_i into TMEM as the A operands of the score products: row = lane,
-        // bf16 pairs in column order; warpgroup h writes d-columns [h D/2, (h+1) D/2)
-        if (n > 0) {
-            constexpr int W = D / 4;  // 32-bit words per half row
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const __nv_bfloat16* src = (t ? p.dO : p.q) + ((size_t)bh * p.Nq + (row_ok ? qg : 0)) * D + h * (D / 2);
-                uint32_t w[W];
-#pragma unroll
-                for (int e = 0; e < W / 4; ++e) {
-                    const uint4 x = row_ok ? __ldg(reinterpret_cast<const uint4*>(src) + e) : make_uint4(0, 0, 0, 0);
-                    w[4 * e] = x.x, w[4 * e + 1] = x.y, w[4 * e + 2] = x.z, w[4 * e + 3] = x.w;
-                }
-                const uint32_t col = (t ? COL_DOA : COL_QA) + h * (D / 4);
-                if constexpr (W == 32) {
-                    tmem_st32(lane_addr + col, w);
-                } else {
-                    tmem_st16(lane_addr + col, w);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(B_QA);
-        }
         bool ok = true;
-        for (int jj = 0; jj < n; ++jj) {
-            const int kb = (jlo + jj) * 128 + 64 * h;           // key of this warpgroup's column 0
-            const int cmax = lim_row - kb;                       // columns > cmax are masked
-            const int cmin_w = p.window > 0 ? qg + off - p.window + 1 - kb : -(1 << 30);  // and < cmin_w
-            if (!(ok = mbar_wait(B_S, jj & 1, ctl, kSiteBwdS))) break;
-            tc_fence_after();
-            uint32_t pp[32];
-            uint32_t va[32], vb[32];
-            // read this warpgroup's 64 S columns, then release them: the next S may overwrite
-            tmem_ld32_async(lane_addr + colA, va);
-            tmem_ld32_async(lane_addr + colA + 32, vb);
-            tmem_wait_ld(va);
-            tmem_wait_ld(vb);
-            tc_fence_before();
-            mbar_arrive(B_SF);
-            // masked entries: columns c > cmax (keys past Nk or, causal, past the
-            // row's limit); tiles with none in the warp skip the test.
-            auto p_phase = [&](auto MASK) {
+        int g = 0, a = 0;
+        for (ItemSeq q; ok;) {
+            const int w = next_chunked_item(q, n_items, chunk_items);
+            if (w >= n_items) break;
+            const Item t = item_of(w);
+            const int n = t.n, jlo = t.jlo, off = t.off, bh = t.bh;
+            const int qg = t.it * 128 + r;
+            const bool row_ok = qg < p.Nq;
+            float l2 = INFINITY, dl = 0.f;
+            if (qg < t.nq) {  // a row past the sequence keeps P = 0
+                const float L = p.lse[(size_t)bh * p.Nq + qg];
+                l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
+                dl = p.delta[(size_t)bh * p.Nq + qg];
+            }
+            const int lim_row = p.causal ? min(qg + off, t.nk - 1) : t.nk - 1;  // last key this row sees
+            // Q_i and dO_i into TMEM as the A operands of the score products: row = lane,
+            // bf16 pairs in column order; warpgroup h writes d-columns [h D/2, (h+1) D/2)
+            if (n > 0) {
+                constexpr int W = D / 4;  // 32-bit words per half row
 #pragma unroll
-            for (int q4 = 0; q4 < 2; ++q4) {
-                uint32_t(&v)[32] = q4 ? vb : va;
+                for (int u = 0; u < 2; ++u) {
+                    const __nv_bfloat16* src = (u ? p.dO : p.q) + ((size_t)bh * p.Nq + (row_ok ? qg : 0)) * D + h * (D / 2);
+                    uint32_t wd[W];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int c0 = q4 * 32 + 2 * e;
-                    const float2 x = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
-                                           make_float2(sc, sc), make_float2(-l2, -l2));
-                    float a = ex2(x.x), b = ex2(x.y);
-                    if constexpr (decltype(MASK)::value) {
-                        if (c0 > cmax || c0 < cmin_w) a = 0.f;
-                        if (c0 + 1 > cmax || c0 + 1 < cmin_w) b = 0.f;
+                    for (int e = 0; e < W / 4; ++e) {
+                        const uint4 x = row_ok ? __ldg(reinterpret_cast<const uint4*>(src) + e) : make_uint4(0, 0, 0, 0);
+                        wd[4 * e] = x.x, wd[4 * e + 1] = x.y, wd[4 * e + 2] = x.z, wd[4 * e + 3] = x.w;
                     }
-                    pp[q4 * 16 + e] = pack_bf16(a, b);
+                    const uint32_t col = (u ? COL_DOA : COL_QA) + h * (D / 4);
+                    if constexpr (W == 32) {
+                        tmem_st32(lane_addr + col, wd);
+                    } else {
+                        tmem_st16(lane_addr + col, wd);
+                    }
                 }
+                tc_fence_before();
+                mbar_arrive(B_QA);
             }
-            };
-            if (__any_sync(0xffffffffu, cmax < 63 || cmin_w > 0))
-                p_phase(std::true_type{});
-            else
-                p_phase(std::false_type{});
-            if (!(ok = mbar_wait(B_DP, jj & 1, ctl, kSiteBwdDP))) break;
-            tc_fence_after();
-            tmem_ld32_async(lane_addr + colB, va);
-            tmem_wait_ld(va);
-            tmem_ld32_async(lane_addr + colB + 32, vb);
-#pragma unroll
-            for (int q4 = 0; q4 < 2; ++q4) {
-                uint32_t(&v)[32] = q4 ? vb : va;
-                if (q4) tmem_wait_ld(vb);
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const uint32_t pr = pp[q4 * 16 + e];
-                    pk[e] = pack_bf16(bf_lo(pr) * (__uint_as_float(v[2 * e]) - dl),
-                                      bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dl));
+            for (int jj = 0; jj < n; ++jj) {
+                const int gj = g + jj;
+                const int kb = (jlo + jj) * 128 + 64 * h;           // key of this warpgroup's column 0
+                const int cmax = lim_row - kb;                       // columns > cmax are masked
+                const int cmin_w = p.window > 0 ? qg + off - p.window + 1 - kb : -(1 << 30);  // and < cmin_w
+                if (jj + 1 == n) {  // the next item's Q and dO rows towards L2 while this one finishes
+                    ItemSeq qn = q;
+                    const int wn = next_chunked_item(qn, n_items, chunk_items);
+                    if (wn < n_items) {
+                        int bhn, mrn;
+                        chunked_order(wn, p.n_qt, p.BH, p.hc_q, bhn, mrn);
+                        const int qn_row = (p.causal ? p.n_qt - 1 - mrn : mrn) * 128 + r;
+                        if (qn_row < p.Nq) {
+                            const size_t o = ((size_t)bhn * p.Nq + qn_row) * D + h * (D / 2);
+                            asm volatile("prefetch.L2 [%0];" ::"l"(p.q + o));
+                            asm volatile("prefetch.L2 [%0];" ::"l"(p.dO + o));
+                        }
+                    }
                 }
-                tmem_st16_async(lane_addr + colB + q4 * 16, pk);
+                if (!(ok = mbar_wait(B_S, gj & 1, ctl, kSiteBwdS))) break;
+                tc_fence_after();
+                uint32_t pp[32];
+                uint32_t va[32], vb[32];
+                // read this warpgroup's 64 S columns, then release them: the next S may overwrite
+                tmem_ld32_async(lane_addr + colA, va);
+                tmem_ld32_async(lane_addr + colA + 32, vb);
+                tmem_wait_ld(va);
+                tmem_wait_ld(vb);
+                tc_fence_before();
+                mbar_arrive(B_SF);
+                // masked entries: columns c > cmax (keys past Nk or, causal, past the
+                // row's limit); tiles with none in the warp skip the test.
+                auto p_phase = [&](auto MASK) {
+#pragma unroll
+                for (int q4 = 0; q4 < 2; ++q4) {
+                    uint32_t(&v)[32] = q4 ? vb : va;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c0 = q4 * 32 + 2 * e;
+                        const float2 x = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                               make_float2(sc, sc), make_float2(-l2, -l2));
+                        float pa = ex2(x.x), pb = ex2(x.y);
+                        if constexpr (decltype(MASK)::value) {
+                            if (c0 > cmax || c0 < cmin_w) pa = 0.f;
+                            if (c0 + 1 > cmax || c0 + 1 < cmin_w) pb = 0.f;
+                        }
+                        pp[q4 * 16 + e] = pack_bf16(pa, pb);
+                    }
+                }
+                };
+                if (__any_sync(0xffffffffu, cmax < 63 || cmin_w > 0))
+                    p_phase(std::true_type{});
+                else
+                    p_phase(std::false_type{});
+                if (!(ok = mbar_wait(B_DP, gj & 1, ctl, kSiteBwdDP))) break;
+                tc_fence_after();
+                tmem_ld32_async(lane_addr + colB, va);
+                tmem_wait_ld(va);
+                tmem_ld32_async(lane_addr + colB + 32, vb);
+#pragma unroll
+                for (int q4 = 0; q4 < 2; ++q4) {
+                    uint32_t(&v)[32] = q4 ? vb : va;
+                    if (q4) tmem_wait_ld(vb);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint32_t pr = pp[q4 * 16 + e];
+                        pk[e] = pack_bf16(bf_lo(pr) * (__uint_as_float(v[2 * e]) - dl),
+                                          bf_hi(pr) * (__uint_as_float(v[2 * e + 1]) - dl));
+                    }
+                    tmem_st16_async(lane_addr + colB + q4 * 16, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(B_DS);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(B_DS);
-        }
-        if (ok) {
+            if (!ok) break;
             const bool have = n > 0;
             if (have) {
-                ok = mbar_wait(B_ACC, 0, ctl, kSiteBwdDone);
+                if (!(ok = mbar_wait(B_ACC, a & 1, ctl, kSiteBwdDone))) break;
                 tc_fence_after();
             }
-            if (ok)
-                store_acc_row<D>(lane_addr + C::COL_ACC0, p.dq + ((size_t)bh * p.Nq + (row_ok ? qg : 0)) * D,
-                                 p.scale, row_ok, !have, h * (D / 2));
+            store_acc_row<D>(lane_addr + C::COL_ACC0, p.dq + ((size_t)bh * p.Nq + (row_ok ? qg : 0)) * D,
+                             p.scale, row_ok, !have, h * (D / 2));
+            if (have) {
+                g += n;
+                ++a;
+            }
         }
     }
     bwd_teardown<D>(tmem);
@@ -1559,7 +1623,7 @@ cudaError_t launch_dq_d(const BwdLaunch& a, cudaStream_t s, bool after_dkdv) {
     if (e != cudaSuccess) return e;
     const BwdParams p = make_params(a);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.n_qt * p.BH));
+    cfg.gridDim = dim3((unsigned)std::min(p.n_qt * p.BH, std::max(1, a.num_sms)));  // persistent over query tiles
     cfg.blockDim = dim3(C::THREADS_DQ);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
