@@ -98,31 +98,6 @@ __device__ __forceinline__ void chunked_order(int idx, int n_t, int BH, int hc, 
     bh = h0 + (r - t * hn);
 }
 
-// Item sequence of a persistent CTA (one per SM at most) over n_items work items
-// in the chunked order (chunks of chunk_items): within each chunk the CTAs take
-// the items round by round, alternating direction (round r: r*G + c, or
-// r*G + G-1-c), odd chunks starting reversed, so that the rounds' long and
-// short items even out per CTA.  With chunks smaller than the grid the rounds
-// run over the whole order instead.  Returns n_items once the CTA has no more.
-struct ItemSeq {
-    int ci = 0, rd = 0;  // chunk, and round within it
-};
-__device__ __forceinline__ int next_chunked_item(ItemSeq& q, int n_items, int chunk_items) {
-    const int G = gridDim.x, c = blockIdx.x;
-    if (chunk_items < G) return min(n_items, persistent_work(q.rd++, c, G));
-    for (;;) {
-        const int start = q.ci * chunk_items;
-        if (start >= n_items) return n_items;
-        const int wl = q.rd * G + (((q.rd + q.ci) & 1) ? G - 1 - c : c);
-        if (wl < min(chunk_items, n_items - start)) {
-            ++q.rd;
-            return start + wl;
-        }
-        ++q.ci;
-        q.rd = 0;
-    }
-}
-
 // Query and key counts of head bh's sequence (per-sequence lengths clamped to
 // [0, Nq] and [0, Nk]; the forward records lengths out of range).  Rows and
 // keys past them are padding: their LSE reads as -inf (P = 0), key columns are
@@ -429,7 +404,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         if constexpr (PAIR)
             return q.rd++ == 0 ? (int)(blockIdx.x >> 1) : n_items;
         else
-            return next_chunked_item(q, n_items, chunk_items);
+            return next_chunked_item(q, n_items, chunk_items, gridDim.x, blockIdx.x, p.causal != 0);
     };
     struct Item {
         int bh, kt, nq, nk, off, i0, n;  // n query tiles from i0 (the union of a pair's two key tiles)
@@ -888,7 +863,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             bool ok = true;
             int g = 0;
             for (ItemSeq q; ok;) {
-                const int w = next_chunked_item(q, n_items, chunk_items);
+                const int w = next_chunked_item(q, n_items, chunk_items, gridDim.x, blockIdx.x, p.causal != 0);
                 if (w >= n_items) break;
                 const Item t = item_of(w);
                 for (int jj = 0; jj < t.n; ++jj) {
@@ -915,7 +890,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             bool ok = true;
             int g = 0, a = 0;
             for (ItemSeq q; ok;) {
-                const int w = next_chunked_item(q, n_items, chunk_items);
+                const int w = next_chunked_item(q, n_items, chunk_items, gridDim.x, blockIdx.x, p.causal != 0);
                 if (w >= n_items) break;
                 const Item t = item_of(w);
                 if (t.n == 0) continue;
@@ -967,7 +942,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         bool ok = true;
         int g = 0, a = 0;
         for (ItemSeq q; ok;) {
-            const int w = next_chunked_item(q, n_items, chunk_items);
+            const int w = next_chunked_item(q, n_items, chunk_items, gridDim.x, blockIdx.x, p.causal != 0);
             if (w >= n_items) break;
             const Item t = item_of(w);
             const int n = t.n, jlo = t.jlo, off = t.off, bh = t.bh;
@@ -1010,7 +985,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                 const int cmin_w = p.window > 0 ? qg + off - p.window + 1 - kb : -(1 << 30);  // and < cmin_w
                 if (jj + 1 == n) {  // the next item's Q and dO rows towards L2 while this one finishes
                     ItemSeq qn = q;
-                    const int wn = next_chunked_item(qn, n_items, chunk_items);
+                    const int wn = next_chunked_item(qn, n_items, chunk_items, gridDim.x, blockIdx.x, p.causal != 0);
                     if (wn < n_items) {
                         int bhn, mrn;
                         chunked_order(wn, p.n_qt, p.BH, p.hc_q, bhn, mrn);

@@ -26,6 +26,7 @@
 //               max), write P as bf16 over the S columns, and run the
 //               epilogue O / l -> bf16, LSE = (m + log2 l) ln 2.
 #include <algorithm>
+#include <mutex>
 
 #include "fa_internal.h"
 
@@ -73,6 +74,7 @@ struct FwdParams {
     int rows;  // query rows per work tile: 256 (two 128-row tiles) or 128 (split-KV)
     int n_mtiles, num_work;
     int hc;    // heads per scheduling chunk: their K and V fit in 64 MiB of L2 together
+    int per_chunk;  // the CTAs take the chunks in per-chunk rounds (next_chunked_item)
     float scale_log2;
     DevError* err;
     uint64_t timeout_ns;
@@ -117,7 +119,8 @@ __device__ __forceinline__ int fwd_kv_first(const FwdParams& p, int row0, int nq
 // Work tile w -> (bh, first row).  Heads come in chunks of hc whose K and V
 // fit in L2 together, so the CTAs in flight share them there; within a chunk
 // every head's row tile of one level comes before the next level (causal:
-// heaviest first).  With hc = BH this is one chunk over all heads.
+// heaviest first).  The persistent CTAs take each chunk in rounds of
+// alternating direction (next_chunked_item).
 __device__ __forceinline__ void fwd_decode(const FwdParams& p, int w, int& bh, int& row0) {
     const int chunk = p.hc * p.n_mtiles;
     const int c = w / chunk;
@@ -235,6 +238,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // this CTA's work tiles (every role walks the same sequence)
+    auto next_work = [&](ItemSeq& q) {
+        return next_chunked_item(q, p.num_work, p.hc * p.n_mtiles, gridDim.x, blockIdx.x, p.per_chunk != 0);
+    };
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -286,12 +293,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             uint32_t phase = 0, q_iter = 0;
             uint32_t issued = 0, issued_par = 0;  // per slot: filled at least once / its last parity
             bool ok = true;
-            SeqLen sl_next = fwd_seqlen<VL>(p, persistent_work(0, blockIdx.x, gridDim.x));
-            for (int rd = 0; rd * (int)gridDim.x < p.num_work && ok; ++rd) {
-                const int w = persistent_work(rd, blockIdx.x, gridDim.x);
+            ItemSeq seq;
+            int w_next = next_work(seq);
+            SeqLen sl_next = fwd_seqlen<VL>(p, w_next);
+            for (int w = w_next; w < p.num_work && ok; w = w_next) {
+                w_next = next_work(seq);
                 const SeqLen sl = sl_next;  // loaded one tile ahead
-                sl_next = fwd_seqlen<VL>(p, persistent_work(rd + 1, blockIdx.x, gridDim.x));
-                if (w >= p.num_work) continue;
+                sl_next = fwd_seqlen<VL>(p, w_next);
                 int bh, row0;
                 fwd_decode(p, w, bh, row0);
                 const int jlo = fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk);
@@ -375,12 +383,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             };
             bool ok = true;
             uint32_t fill = 0, pit0 = 0, pit1 = 0;  // split-KV: ring fills consumed, P handoffs per warpgroup
-            SeqLen sl_next = fwd_seqlen<VL>(p, persistent_work(0, blockIdx.x, gridDim.x));
-            for (int rd = 0; rd * (int)gridDim.x < p.num_work && ok; ++rd) {
-                const int w = persistent_work(rd, blockIdx.x, gridDim.x);
+            ItemSeq seq;
+            int w_next = next_work(seq);
+            SeqLen sl_next = fwd_seqlen<VL>(p, w_next);
+            for (int w = w_next; w < p.num_work && ok; w = w_next) {
+                w_next = next_work(seq);
                 const SeqLen sl = sl_next;  // loaded one tile ahead
-                sl_next = fwd_seqlen<VL>(p, persistent_work(rd + 1, blockIdx.x, gridDim.x));
-                if (w >= p.num_work) continue;
+                sl_next = fwd_seqlen<VL>(p, w_next);
                 int bh, row0;
                 fwd_decode(p, w, bh, row0);
                 const int n = max(0, fwd_num_kv(p, row0, sl.nq, sl.nk) - fwd_kv_first<WIN>(p, row0, sl.nq, sl.nk));
@@ -533,12 +542,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         uint32_t o1_iter = 0, merge_iter = 0;  // split-KV: warpgroup 1's O handoffs, merges
         bool md_pending = false;               // split-KV (warpgroup 1): merge of the last tile not yet confirmed
         float2* stage = (float2*)(smem + C::OFF_STAGE);  // split-KV: warpgroup 1's (m, l) per row
-        SeqLen sl_next = fwd_seqlen<VL>(p, persistent_work(0, blockIdx.x, gridDim.x));
-        for (int rd = 0; rd * (int)gridDim.x < p.num_work; ++rd) {
-            const int w = persistent_work(rd, blockIdx.x, gridDim.x);
+        ItemSeq seq;
+        int w_next = next_work(seq);
+        SeqLen sl_next = fwd_seqlen<VL>(p, w_next);
+        for (int w = w_next; w < p.num_work; w = w_next) {
+            w_next = next_work(seq);
             const SeqLen sl = sl_next;
-            sl_next = fwd_seqlen<VL>(p, persistent_work(rd + 1, blockIdx.x, gridDim.x));
-            if (w >= p.num_work) continue;
+            sl_next = fwd_seqlen<VL>(p, w_next);
             if (VL && sl.bad && tid == 0 && atomicCAS(&p.err->code, 0, kErrInvalid) == 0) {
                 p.err->site = kSiteSeqLen;
                 p.err->block = blockIdx.x;
@@ -689,6 +699,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     }
 }
 
+// Heads per scheduling chunk: their K and V fit in 64 MiB of L2 together.
+// Causal and non-causal alike: causal grids take the chunks in per-chunk
+// rounds (next_chunked_item), so their tiles' weights still even out per CTA.
+int fwd_head_chunk(int BH, int Nk, int d) {
+    const long long per_head = 4ll * Nk * d;
+    return (int)std::max(1ll, std::min((long long)BH, (64ll << 20) / per_head));
+}
+
 template <int D, bool WIN, bool VL, bool SPLIT>
 cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
     using C = Fwd<D>;
@@ -709,14 +727,12 @@ cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
     p.H = a.H;
     p.rows = SPLIT ? 128 : kFwdRowsPerCta;
     p.n_mtiles = (a.Nq + p.rows - 1) / p.rows;
-    {  // Non-causal: chunks of heads whose K and V fit in 64 MiB of L2 together (all tiles weigh
-       // the same, so chunks keep the balance; B=4 H=32 N=8192: 3.03 -> 2.87 ms).  Causal: one
-       // chunk, so the heaviest tiles of every head start first (chunks cut the DRAM traffic of
-       // B=1 H=32 N=8192 from 579 to 317 MB but ran 10% slower: the tail of each chunk is light);
-       // split-KV grids are small: one chunk.
-        const long long per_head = 4ll * a.Nk * a.d;
-        p.hc = (SPLIT || a.causal) ? p.BH
-                                   : (int)std::max(1ll, std::min((long long)p.BH, (64ll << 20) / per_head));
+    // chunks of heads whose K and V fit in 64 MiB of L2 together (split-KV grids are small: one chunk)
+    if (SPLIT) {
+        p.hc = p.BH;
+        p.per_chunk = 0;
+    } else {
+        fwd_work_order(p.BH, a.Nq, a.Nk, a.causal, fwd_head_chunk(p.BH, a.Nk, a.d), a.num_sms, &p.hc, &p.per_chunk);
     }
     p.num_work = p.n_mtiles * p.BH;
     p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -728,31 +744,36 @@ cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
 }
 
 // Tile mode for the plain forward.  The grid is persistent with a static
-// schedule (round rd of CTA c takes work tile persistent_work(rd, c, G)), so
-// the host can add up every CTA's share for both tile sizes and take the one
-// whose busiest CTA finishes first.  Costs, in units of one 128-key block of
+// schedule (next_chunked_item), so the host can add up every CTA's share for
+// both tile sizes and take the one whose busiest CTA finishes first.  Costs, in units of one 128-key block of
 // a 256-row tile, fitted to GB300 timings: a key block of a split-KV tile
 // costs 0.55 (half the rows, but the two softmax warpgroups alternate on one
 // tile's blocks, at ~85% of the two-tile rate), and a tile costs 1.5 (256
 // rows) or 2 (split-KV: the merge) for its prologue and epilogue.  Only small
 // grids are evaluated; past four tiles per SM the 256-row tiles always win.
-int fwd_makespan(int BH, int Nq, int Nk, int causal, int rows, int block_cost, int tile_cost, int num_sms) {
+int fwd_makespan(int BH, int Nq, int Nk, int causal, int rows, int hc, bool per_chunk, int block_cost, int tile_cost,
+                 int num_sms) {
     const int n_m = (Nq + rows - 1) / rows;
     const int work = n_m * BH, G = work < num_sms ? work : num_sms;
     const int kv_total = (Nk + 127) / 128;
-    long long tot[1024] = {};
-    for (int w = 0; w < work; ++w) {
-        const int rd = w / G, pos = w - rd * G, cta = (rd & 1) ? G - 1 - pos : pos;
-        const int mr = w / BH, m = causal ? n_m - 1 - mr : mr;
-        int n = kv_total;
-        if (causal) {
-            const long long lim = (long long)(m * rows + rows - 1 < Nq - 1 ? m * rows + rows - 1 : Nq - 1) + Nk - Nq;
-            n = lim < 0 ? 0 : (int)(lim / 128 + 1 < kv_total ? lim / 128 + 1 : kv_total);
-        }
-        tot[cta] += (long long)n * block_cost + tile_cost;
-    }
     long long mx = 0;
-    for (int c = 0; c < G; ++c) mx = tot[c] > mx ? tot[c] : mx;
+    for (int c = 0; c < G; ++c) {
+        long long tot = 0;
+        ItemSeq q;
+        for (int w = next_chunked_item(q, work, hc * n_m, G, c, per_chunk); w < work;
+             w = next_chunked_item(q, work, hc * n_m, G, c, per_chunk)) {
+            const int chunk = w / (hc * n_m), r = w - chunk * hc * n_m;
+            const int hn = hc < BH - chunk * hc ? hc : BH - chunk * hc;
+            const int mr = r / hn, m = causal ? n_m - 1 - mr : mr;
+            int n = kv_total;
+            if (causal) {
+                const long long lim = (long long)(m * rows + rows - 1 < Nq - 1 ? m * rows + rows - 1 : Nq - 1) + Nk - Nq;
+                n = lim < 0 ? 0 : (int)(lim / 128 + 1 < kv_total ? lim / 128 + 1 : kv_total);
+            }
+            tot += (long long)n * block_cost + tile_cost;
+        }
+        mx = tot > mx ? tot : mx;
+    }
     return (int)(mx < (1LL << 30) ? mx : (1LL << 30));
 }
 
@@ -769,8 +790,33 @@ bool fwd_use_split(const FwdLaunch& a) {
     const long long work256 = (long long)((a.Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta) * a.B * a.H;
     if (work256 > 4LL * a.num_sms || a.num_sms > 1024 || a.num_sms <= 0) return false;
     const int BH = a.B * a.H;
-    return fwd_makespan(BH, a.Nq, a.Nk, a.causal, 128, 55, 200, a.num_sms) <
-           fwd_makespan(BH, a.Nq, a.Nk, a.causal, kFwdRowsPerCta, 100, 150, a.num_sms);
+    int hc, per_chunk;
+    fwd_work_order(BH, a.Nq, a.Nk, a.causal, fwd_head_chunk(BH, a.Nk, a.d), a.num_sms, &hc, &per_chunk);
+    return fwd_makespan(BH, a.Nq, a.Nk, a.causal, 128, BH, false, 55, 200, a.num_sms) <
+           fwd_makespan(BH, a.Nq, a.Nk, a.causal, kFwdRowsPerCta, hc, per_chunk != 0, 100, 150, a.num_sms);
+}
+
+void fwd_work_order(int BH, int Nq, int Nk, int causal, int hc_l2, int num_sms, int* hc, int* per_chunk) {
+    *hc = hc_l2;
+    *per_chunk = causal ? 1 : 0;
+    if (!causal || hc_l2 >= BH || num_sms <= 0) return;
+    // The one-chunk order's rounds pair heavy and light tiles exactly; per-chunk rounds leave each
+    // chunk's remainder (up to ~2% at N >= 16384) and are kept when within 0.5% of it.  The replay
+    // walks every tile once per schedule, so the last shape's answer is kept.
+    static std::mutex mu;
+    static long long last_key[6] = {-1, -1, -1, -1, -1, -1};
+    static int last_hc = 0;
+    const long long key[6] = {BH, Nq, Nk, hc_l2, num_sms, 1};
+    std::lock_guard<std::mutex> lock(mu);
+    if (std::equal(key, key + 6, last_key)) {
+        *hc = last_hc;
+        return;
+    }
+    const long long chunked = fwd_makespan(BH, Nq, Nk, 1, kFwdRowsPerCta, hc_l2, true, 100, 150, num_sms);
+    const long long one = fwd_makespan(BH, Nq, Nk, 1, kFwdRowsPerCta, BH, true, 100, 150, num_sms);
+    if (chunked * 1000 > one * 1005) *hc = BH;
+    std::copy(key, key + 6, last_key);
+    last_hc = *hc;
 }
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s) {

@@ -85,6 +85,7 @@ struct F8Params {
     const float* k_scale;  // [B*H, ceil(Nk/128)]
     const float* v_scale;  // [B*H]
     int hc;  // heads per scheduling chunk
+    int per_chunk;  // the CTAs take the chunks in per-chunk rounds (next_chunked_item)
     int BH, Nq, Nk, causal, n_qb, n_kb;
     int n_mtiles, num_work;
     float scale_log2;
@@ -102,8 +103,8 @@ __device__ __forceinline__ int f8_num_kv(const F8Params& p, int row0) {
 }
 
 // Work tile w -> (bh, first row), as the bf16 forward's: heads in chunks of hc
-// (non-causal: whose K and V fit in L2 together; causal: one chunk, heaviest
-// row tiles of every head first).
+// whose K and V fit in L2 together, every head's row tile of one level before
+// the next level within a chunk (causal: heaviest first).
 __device__ __forceinline__ void f8_decode(const F8Params& p, int w, int& bh, int& row0) {
     const int chunk = p.hc * p.n_mtiles;
     const int c = w / chunk;
@@ -213,6 +214,10 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // this CTA's work tiles (every role walks the same sequence; next_chunked_item)
+    auto next_work = [&](ItemSeq& q) {
+        return next_chunked_item(q, p.num_work, p.hc * p.n_mtiles, gridDim.x, blockIdx.x, p.per_chunk != 0);
+    };
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -255,9 +260,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             int slot = 0;
             uint32_t phase = 0, q_iter = 0, issued = 0, issued_par = 0;
             bool ok = true;
-            for (int rd = 0; rd * (int)gridDim.x < p.num_work && ok; ++rd) {
-                const int w = persistent_work(rd, blockIdx.x, gridDim.x);
-                if (w >= p.num_work) continue;
+            ItemSeq seq;
+            for (int w = next_work(seq); w < p.num_work && ok; w = next_work(seq)) {
                 int bh, row0;
                 f8_decode(p, w, bh, row0);
                 const int n = f8_num_kv(p, row0);
@@ -323,9 +327,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                 }
             };
             bool ok = true;
-            for (int rd = 0; rd * (int)gridDim.x < p.num_work && ok; ++rd) {
-                const int w = persistent_work(rd, blockIdx.x, gridDim.x);
-                if (w >= p.num_work) continue;
+            ItemSeq seq;
+            for (int w = next_work(seq); w < p.num_work && ok; w = next_work(seq)) {
                 int bh, row0;
                 f8_decode(p, w, bh, row0);
                 const int n = f8_num_kv(p, row0);
@@ -399,9 +402,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         uint8_t* prow = smem + C::OFF_P + t * C::TILE + r * 128;
         const int off = p.Nk - p.Nq;
         uint32_t s_iter = 0, o_iter = 0, pv_iter = 0;
-        for (int rd = 0; rd * (int)gridDim.x < p.num_work; ++rd) {
-            const int w = persistent_work(rd, blockIdx.x, gridDim.x);
-            if (w >= p.num_work) continue;
+        ItemSeq seq;
+        for (int w = next_work(seq); w < p.num_work; w = next_work(seq)) {
             int bh, row0;
             f8_decode(p, w, bh, row0);
             const int n = f8_num_kv(p, row0);
@@ -564,9 +566,10 @@ cudaError_t launch_fwd_fp8(const Fp8FwdLaunch& a, cudaStream_t s) {
     p.n_kb = (a.Nk + 127) / 128;
     p.n_mtiles = (a.Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
     p.num_work = p.n_mtiles * BH;
-    {  // K (e4m3) and V^T (e4m3) of a head: 2 Nk d bytes
+    {  // heads whose K (e4m3) and V^T (e4m3), 2 Nk d bytes each, fit in 64 MiB of L2 together
         const long long per_head = 2ll * a.Nk * 128;
-        p.hc = a.causal ? BH : (int)std::max(1ll, std::min((long long)BH, (64ll << 20) / per_head));
+        const int hc_l2 = (int)std::max(1ll, std::min((long long)BH, (64ll << 20) / per_head));
+        fwd_work_order(BH, a.Nq, a.Nk, a.causal, hc_l2, a.num_sms, &p.hc, &p.per_chunk);
     }
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;

@@ -20,6 +20,40 @@ __device__ __forceinline__ int persistent_work(int rd, int cta, int G) {
     return rd * G + ((rd & 1) ? G - 1 - cta : cta);
 }
 
+// Item sequence of persistent CTA c (of G) over n_items work items listed in
+// chunks of chunk_items (heads whose streamed operands fit in L2 together).
+// per_chunk (items of unequal weight, heaviest first within each chunk): the
+// CTAs take each chunk round by round, alternating direction (round r:
+// r*G + c, or r*G + G-1-c), and odd chunks start reversed, so that the
+// rounds' long and short items even out per CTA while the CTAs in flight stay
+// within one chunk.  Otherwise (equal weights), and with chunks smaller than
+// the grid, the rounds run over the whole list (persistent_work), which keeps
+// every CTA's count within one item.  Returns n_items once the CTA has no
+// more.  Host and device (the host replays the schedule to size grids).
+struct ItemSeq {
+    int ci = 0, rd = 0;  // chunk, and round within it
+};
+__host__ __device__ inline int next_chunked_item(ItemSeq& q, int n_items, int chunk_items, int G, int c,
+                                                 bool per_chunk) {
+    if (!per_chunk || chunk_items < G) {
+        const int rd = q.rd++;
+        const int w = rd * G + ((rd & 1) ? G - 1 - c : c);
+        return w < n_items ? w : n_items;
+    }
+    for (;;) {
+        const int start = q.ci * chunk_items;
+        if (start >= n_items) return n_items;
+        const int size = chunk_items < n_items - start ? chunk_items : n_items - start;
+        const int wl = q.rd * G + (((q.rd + q.ci) & 1) ? G - 1 - c : c);
+        if (wl < size) {
+            ++q.rd;
+            return start + wl;
+        }
+        ++q.ci;
+        q.rd = 0;
+    }
+}
+
 struct FwdLaunch {
     CUtensorMap map_q, map_k, map_v;  // 3-D maps (d, N, B*H), box (64, 128, 1), 128B swizzle
     void* o;
@@ -157,6 +191,14 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
 // Whether the plain forward (no window, no per-sequence lengths) takes
 // 128-row split-KV tiles for a.B, a.H, a.Nq, a.Nk, a.causal on a.num_sms SMs.
 bool fwd_use_split(const FwdLaunch& a);
+// Work order of the forward's 256-row tiles (bf16 and FP8): the heads per
+// scheduling chunk (*hc) and whether the CTAs take the chunks in per-chunk
+// rounds (*per_chunk, next_chunked_item).  hc_l2 heads fill the L2 budget.
+// Causal grids take hc_l2-head chunks in per-chunk rounds unless the host's
+// replay of both schedules finds the one-chunk, heaviest-first order's
+// busiest CTA clearly less loaded; non-causal grids take hc_l2-head chunks in
+// rounds over the whole order.
+void fwd_work_order(int BH, int Nq, int Nk, int causal, int hc_l2, int num_sms, int* hc, int* per_chunk);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t s);   // D = rowsum(dO o O)
 cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s, bool after_pre = false);  // dK, dV; after_pre:
                                                                                         // overlaps the preprocess's end
