@@ -14,7 +14,7 @@ from tests.parity import check_out_fp8
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(seed, B, H, Nq, Nk, heads=None):
+def _inputs(seed, B, H, Nq, Nk, heads=None, k_ramp=None):
     heads = range(H) if heads is None else heads
 
     def gen(tag, n):
@@ -24,7 +24,10 @@ def _inputs(seed, B, H, Nq, Nk, heads=None):
                 x[b, h] = syn.head_f32(seed, tag, b, h, n, 128)
         return x
     q8, sq = syn.to_e4m3(gen(syn.TAG_Q, Nq), rows=128)
-    k8, sk = syn.to_e4m3(gen(syn.TAG_K, Nk), rows=128)
+    k = gen(syn.TAG_K, Nk)
+    if k_ramp is not None:  # key row t scaled by k_ramp[t] before quantisation
+        k = k * k_ramp[None, None, :, None]
+    k8, sk = syn.to_e4m3(k, rows=128)
     v8, sv = syn.to_e4m3(gen(syn.TAG_V, Nk))
     return q8, k8, v8, sq, sk, sv
 
@@ -71,6 +74,21 @@ def test_fp8_forward_parity(cuda_lib, B, H, Nq, Nk, causal):
     o_ref, lse_ref, p_ref, v = _oracle(q8, k8, v8, sq, sk, sv, causal)
     check_out_fp8(o.double().numpy(), lse.double().numpy(), o_ref, lse_ref, p_ref, v,
                   "fp8 Nq%d Nk%d causal%d" % (Nq, Nk, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_growing_scores(cuda_lib, causal):
+    """Key rows scaled by a ramp (0.5 at the first key to 12.5 at the last, the
+    per-block scales following it): the row max grows by more than 2^8 in the
+    log2 domain every block or two, so blocks whose exponentials ran against
+    the running max are redone after the accumulator is rescaled."""
+    Nq = Nk = 1024
+    ramp = 0.5 + 12.0 * torch.arange(Nk, dtype=torch.float32) / Nk
+    q8, k8, v8, sq, sk, sv = _inputs(2500, 1, 2, Nq, Nk, k_ramp=ramp)
+    o, lse = _run(cuda_lib, q8, k8, v8, sq, sk, sv, causal)
+    o_ref, lse_ref, p_ref, v = _oracle(q8, k8, v8, sq, sk, sv, causal)
+    check_out_fp8(o.double().numpy(), lse.double().numpy(), o_ref, lse_ref, p_ref, v,
+                  "fp8 growing scores causal%d" % causal)
 
 
 def test_fp8_forward_full_size_sampled(cuda_lib):

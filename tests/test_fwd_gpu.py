@@ -148,6 +148,23 @@ def test_forward_scale_argument(cuda_lib):
                   max_abs=derived_o_bound(f64(v)))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_growing_scores(cuda_lib, causal):
+    """Key rows scaled by a ramp (0.5 at the first key to 12.5 at the last): the
+    row max keeps growing from key block to key block, by more than 2^8 in the
+    log2 domain every block or two, so the accumulator is rescaled over and
+    over (the lazy-rescale path).  Off the workloads' scores, so the max-abs
+    bound is the one derived from the bf16 roundings."""
+    B, H, N, d = 1, 2, 1024, 128
+    q, k, v = _inputs(61, B, H, N, N, d)
+    ramp = 0.5 + 12.0 * torch.arange(N, dtype=torch.float32) / N
+    k = (k.float() * ramp[None, None, :, None]).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(cuda_lib, q, k, v, scale, causal)
+    o_ref, lse_ref = naive.forward(f64(q), f64(k), f64(v), scale, causal)
+    check_out(f64(o), f64(lse), o_ref, lse_ref, "growing scores causal%d" % causal, max_abs=derived_o_bound(f64(v)))
+
+
 def test_forward_repeatable(cuda_lib):
     """The forward has no atomics: two runs are bitwise identical."""
     q, k, v = _inputs(8, 1, 4, 640, 640, 128)
