@@ -9,16 +9,18 @@
 //
 // Three launches on one stream:
 //   bwd_pre   D_i = rowsum(dO o O) in fp32 (one warp per row).
-//   bwd_dkdv  one CTA per 128-key tile (KV-tile parallel): K_j, V_j stay in
-//             shared memory, Q_i / dO_i stream through a 2-stage ring;
+//   bwd_dkdv  work item = one 128-key tile (KV-tile parallel), taken by
+//             persistent CTAs (one per SM): K_j, V_j stay in shared memory
+//             for the item, Q_i / dO_i stream through a 2-stage ring;
 //             tcgen05: S^T = K Q^T and dP^T = V dO^T into TMEM; S^T is read
 //             out at once (so S^T of the next query tile can be issued while
 //             P waits in registers); once dP^T is read, P^T and dS^T are
 //             written over it as bf16 for dV += P^T dO and dK += dS^T Q, both
 //             with A from TMEM; dK, dV accumulate in TMEM over all query
 //             tiles.
-//   bwd_dq    one CTA per 128-query tile (Q-tile parallel): Q_i, dO_i are
-//             written into TMEM by the compute threads and stay; K_j / V_j
+//   bwd_dq    work item = one 128-query tile (Q-tile parallel), taken by
+//             persistent CTAs: Q_i, dO_i are written into TMEM by the compute
+//             threads and stay for the item; K_j / V_j
 //             stream; S = Q K^T and dP = dO V^T take Q, dO from TMEM; dQ +=
 //             dS K with dS from TMEM.  dQ is accumulated in fp32 TMEM and
 //             written once, so the backward needs no atomics and is

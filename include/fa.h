@@ -193,10 +193,11 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
  * may start on SMs that the last dK/dV CTAs leave free.  Every read of D still
  * follows the preprocess, and the dQ grid completes only after the dK/dV grid.
  *  fa_bwd_preprocess: delta [B,H,Nq] fp32 = rowsum(dO o O).
- *  fa_bwd_dkdv: dk, dv [B,H,Nk,d] from q, k, v, lse, delta, dO; one CTA per
- *    128-key tile, P and dS rebuilt on chip for every query tile it sees.
- *  fa_bwd_dq: dq [B,H,Nq,d] from q, k, v, lse, delta, dO; one CTA per
- *    128-query tile.  dkdv and dq only read delta, so they may run in any
+ *  fa_bwd_dkdv: dk, dv [B,H,Nk,d] from q, k, v, lse, delta, dO; each
+ *    128-key tile is one work item of a persistent grid (at most one CTA per
+ *    SM), P and dS rebuilt on chip for every query tile it sees.
+ *  fa_bwd_dq: dq [B,H,Nq,d] from q, k, v, lse, delta, dO; each 128-query
+ *    tile is one work item.  dkdv and dq only read delta, so they may run in any
  *    order (or concurrently) after the preprocess.
  * Same conventions and errors as fa_bwd. */
 int fa_bwd_preprocess(const void *o, const void *dO, float *delta, int B, int H, int Nq, int d,
