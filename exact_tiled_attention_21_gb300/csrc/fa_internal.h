@@ -12,14 +12,6 @@
 
 namespace fa {
 
-// Work tile of persistent CTA `cta` (of G) in round `rd`: the rounds alternate
-// direction, so when the work list is ordered heaviest first every CTA's total
-// comes out nearly equal (CTA 0 takes the heaviest tile of one round and the
-// lightest of the next).
-__device__ __forceinline__ int persistent_work(int rd, int cta, int G) {
-    return rd * G + ((rd & 1) ? G - 1 - cta : cta);
-}
-
 // Item sequence of persistent CTA c (of G) over n_items work items listed in
 // chunks of chunk_items (heads whose streamed operands fit in L2 together).
 // per_chunk (items of unequal weight, heaviest first within each chunk): the
@@ -27,9 +19,11 @@ __device__ __forceinline__ int persistent_work(int rd, int cta, int G) {
 // r*G + c, or r*G + G-1-c), and odd chunks start reversed, so that the
 // rounds' long and short items even out per CTA while the CTAs in flight stay
 // within one chunk.  Otherwise (equal weights), and with chunks smaller than
-// the grid, the rounds run over the whole list (persistent_work), which keeps
-// every CTA's count within one item.  Returns n_items once the CTA has no
-// more.  Host and device (the host replays the schedule to size grids).
+// the grid, the rounds run over the whole list, which keeps every CTA's count
+// within one item (and with the list heaviest first, CTA 0 takes the heaviest
+// item of one round and the lightest of the next).  Returns n_items once the
+// CTA has no more.  Host and device (the host replays the schedule to size
+// grids).
 struct ItemSeq {
     int ci = 0, rd = 0;  // chunk, and round within it
 };
