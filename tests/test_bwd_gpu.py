@@ -96,6 +96,27 @@ def test_backward_parity_many_heads(cuda_lib, Nq, Nk, d, causal):
     check_grad(f64(dv), rv, "dV " + tag)
 
 
+def test_backward_schedule_with_chunks_smaller_than_the_grid(cuda_lib):
+    """B=1, H=32, Nq=16384, Nk=512, causal: the dK/dV pass's L2 chunks (8 heads
+    of 4 key tiles) are smaller than its grid, so the persistent CTAs take the
+    items in rounds over the whole list instead of per chunk; the dQ pass keeps
+    per-chunk rounds.  Heads 0 and 31 against the oracle (queries before
+    16384 - 512 see no key: zero dQ rows)."""
+    B, H, Nq, Nk, d = 1, 32, 16384, 512, 128
+    q, k, v, dO = _inputs(77, B, H, Nq, Nk, d)
+    scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = _run(cuda_lib, q, k, v, dO, scale, True)
+    for h in (0, H - 1):
+        sl = slice(h, h + 1)
+        rq, rk, rv = naive.backward(f64(q[:, sl]), f64(k[:, sl]), f64(v[:, sl]), f64(dO[:, sl]), scale, True)
+        tag = "Nq%d Nk%d head %d" % (Nq, Nk, h)
+        dp_max = np.abs(f64(dO[:, sl]) @ np.swapaxes(f64(v[:, sl]), -1, -2)).max()
+        cancel = scale * dp_max * max(np.abs(f64(k[:, sl])).max(), np.abs(f64(q[:, sl])).max())
+        check_grad(f64(dq[:, sl]), rq, "dQ " + tag, cancel_scale=cancel)
+        check_grad(f64(dk[:, sl]), rk, "dK " + tag, cancel_scale=cancel)
+        check_grad(f64(dv[:, sl]), rv, "dV " + tag)
+
+
 @pytest.mark.parametrize("B,H,N", [(1, 1, 128), (1, 2, 700), (1, 32, 2048)])
 def test_backward_matches_step_entry_points(cuda_lib, B, H, N):
     """fa_bwd launches the dQ pass to overlap the end of the dK/dV pass: the
