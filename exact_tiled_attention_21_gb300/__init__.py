@@ -95,6 +95,8 @@ def load():
     lib.fa_version.restype = i
     lib.fa_fwd_tile_rows.argtypes = [i] * 6
     lib.fa_fwd_tile_rows.restype = i
+    lib.fa_work_schedule.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+    lib.fa_work_schedule.restype = i
     _lib = lib
     return lib
 
@@ -289,6 +291,14 @@ def fa_decode_workspace_bytes(B, H, Nk, d, num_splits=0):
 def fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream=None):
     _raise(load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
                          float(scale), int(bool(causal)), _stream(stream)), "fa_fwd")
+
+
+def fa_work_schedule(n_items, chunk_items, grid, per_chunk):
+    """The CTA that takes each work item in the persistent grids' static
+    schedule (a list of n_items ints)."""
+    owner = (ctypes.c_int * max(1, n_items))()
+    _raise(load().fa_work_schedule(n_items, chunk_items, grid, int(bool(per_chunk)), owner), "fa_work_schedule")
+    return list(owner)[:n_items]
 
 
 def fa_fwd_tile_rows(B, H, Nq, Nk, d, causal):

@@ -241,6 +241,20 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 0, nullptr, nullptr, stream);
 }
 
+int fa_work_schedule(int n_items, int chunk_items, int grid, int per_chunk, int* owner) {
+    if (n_items < 0 || chunk_items < 1 || grid < 1 || (n_items > 0 && !owner)) return FA_ERR_INVALID_ARG;
+    for (int i = 0; i < n_items; ++i) owner[i] = -1;
+    for (int c = 0; c < grid; ++c) {
+        ItemSeq q;
+        for (int w = next_chunked_item(q, n_items, chunk_items, grid, c, per_chunk != 0); w < n_items;
+             w = next_chunked_item(q, n_items, chunk_items, grid, c, per_chunk != 0)) {
+            if (w < 0 || owner[w] != -1) return FA_ERR_INVALID_ARG;
+            owner[w] = c;
+        }
+    }
+    return FA_OK;
+}
+
 int fa_fwd_tile_rows(int B, int H, int Nq, int Nk, int d, int causal) {
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     int st = check_shape(B, H, Nq, Nk, d);

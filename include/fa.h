@@ -81,6 +81,19 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  * nothing. */
 int fa_fwd_tile_rows(int B, int H, int Nq, int Nk, int d, int causal);
 
+/* The static schedule of the persistent grids (the forward's work tiles, the
+ * backward's key and query tiles): n_items work items listed in chunks of
+ * chunk_items (heads whose streamed operands fit in L2 together), taken by
+ * `grid` CTAs.  per_chunk != 0 (causal lists, heaviest item first in each
+ * chunk): each chunk in its own rounds of alternating direction, odd chunks
+ * starting reversed; otherwise, or when a chunk is smaller than the grid,
+ * rounds of alternating direction over the whole list.  Writes owner[i] = the
+ * CTA that takes item i (owner: n_items ints, host memory).  Returns FA_OK,
+ * FA_ERR_INVALID_ARG for bad sizes or a null owner, or FA_ERR_INVALID_ARG if
+ * an item would be taken twice (never: the schedule is a partition).
+ * Host-only; launches nothing. */
+int fa_work_schedule(int n_items, int chunk_items, int grid, int per_chunk, int *owner);
+
 /* Causal sliding-window forward: like fa_fwd with causal = 1, except that
  * query i sees only the `window` (>= 1) keys ending at its diagonal, keys j
  * with i + Nk - Nq - window < j <= i + Nk - Nq (the fixed-window local

@@ -100,3 +100,47 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fa, "_lib", None)
     with pytest.raises(fa.FAError):
         fa.load()
+
+
+@pytest.mark.parametrize("per_chunk", [False, True])
+def test_work_schedule_is_a_partition(lib, per_chunk):
+    """Every work item of the persistent grids is taken by exactly one CTA, for
+    chunks larger and smaller than the grid, ragged last chunks and rounds;
+    without per-chunk rounds every CTA's count is within one item."""
+    for n_items, chunk, grid in [(1, 1, 1), (5, 2, 3), (512, 512, 152), (2048, 1024, 152), (2048, 32, 152),
+                                 (4096, 512, 152), (4097, 333, 152), (256, 8, 152), (100, 100, 152),
+                                 (16384, 512, 152), (3, 64, 2)]:
+        g = min(grid, n_items)
+        owner = fa.fa_work_schedule(n_items, chunk, g, per_chunk)
+        assert len(owner) == n_items and all(0 <= c < g for c in owner), (n_items, chunk, g)
+        counts = [0] * g
+        for c in owner:
+            counts[c] += 1
+        assert sum(counts) == n_items
+        if not per_chunk or chunk < g:
+            assert max(counts) - min(counts) <= 1, (n_items, chunk, g, max(counts), min(counts))
+
+
+def test_work_schedule_balances_causal_chunks(lib):
+    """Causal lists (each chunk heaviest first: 16 heads of 64 key tiles whose
+    weights fall from 64 to 1): per-chunk rounds keep the busiest CTA within 2%
+    of the mean, where rounds over the whole list would give it ~10% more."""
+    heads, tiles, g = 16, 64, 152
+    weights = [tiles - (i // heads) for i in range(heads * tiles)] * 2  # two chunks
+    for per_chunk, bound in ((True, 1.02), (False, None)):
+        owner = fa.fa_work_schedule(len(weights), heads * tiles, g, per_chunk)
+        load = [0] * g
+        for w, c in zip(weights, owner):
+            load[c] += w
+        ratio = max(load) / (sum(load) / g)
+        if bound:
+            assert ratio <= bound, ratio
+        else:
+            assert ratio > 1.05, ratio  # the reason for per-chunk rounds
+
+
+def test_work_schedule_rejects_bad_sizes(lib):
+    with pytest.raises(fa.FAError):
+        fa.fa_work_schedule(10, 0, 4, True)
+    with pytest.raises(fa.FAError):
+        fa.fa_work_schedule(10, 4, 0, False)
