@@ -800,6 +800,9 @@ void fwd_work_order(int BH, int Nq, int Nk, int causal, int hc_l2, int num_sms, 
     *hc = hc_l2;
     *per_chunk = causal ? 1 : 0;
     if (!causal || hc_l2 >= BH || num_sms <= 0) return;
+    // past ~1M work tiles the replay would cost milliseconds of host time per new shape; the
+    // chunks' remainders are a smaller share there, so the chunked order stays
+    if ((long long)((Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta) * BH > (1ll << 20)) return;
     // The one-chunk order's rounds pair heavy and light tiles exactly; per-chunk rounds leave each
     // chunk's remainder (up to ~2% at N >= 16384) and are kept when within 0.5% of it.  The replay
     // walks every tile once per schedule, so the last shape's answer is kept.
