@@ -285,24 +285,27 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
            "bwd_modes": "bwd: fa_bwd (dK/dV pass + dQ pass, deterministic); bwd_fused: fa_bwd_fused (one pass, "
                         "dQ by fp32 reduce-adds, dQ bits vary run to run)",
            "_windows": {}}
-    # decode shapes (the cache is read once per call; >= 1 GiB, larger than L2)
+    # decode shapes (the cache is read once per call; >= 1 GiB, larger than L2), each with the
+    # headline's 16 splits and with the library's automatic count
     t0 = time.time()
     for nk, d in ((4096, 128), (4000, 128), (4096, 64)):
         q = rnd(DEC_B, DEC_H, d)
         kc, vc = rnd(DEC_B, DEC_H, nk, d), rnd(DEC_B, DEC_H, nk, d)
         o = torch.empty_like(q)
         lse = torch.empty(DEC_B, DEC_H, device=dev, dtype=torch.float32)
-        ws = torch.empty(fa.fa_decode_workspace_bytes(DEC_B, DEC_H, nk, d, DEC_SPLITS), dtype=torch.uint8,
-                         device=dev)
-        call = lambda: fa.fa_decode(q, kc, vc, o, lse, DEC_B, DEC_H, nk, d, 1.0 / math.sqrt(d), DEC_SPLITS, ws,
-                                    ws.numel(), stream)
-        for _ in range(3):
-            call()
-        ms = timed(call, 20, False)
-        byt = 2.0 * DEC_B * DEC_H * nk * d * 2
-        out["decode_B32_H32"].append({"Nk": nk, "d": d, "splits": DEC_SPLITS, "ms": ms,
-                                      "gbs": byt / (ms * 1e-3) / 1e9})
-        del q, kc, vc, o, lse, ws
+        for sp in (DEC_SPLITS, 0):
+            ws = torch.empty(fa.fa_decode_workspace_bytes(DEC_B, DEC_H, nk, d, sp), dtype=torch.uint8,
+                             device=dev)
+            call = lambda: fa.fa_decode(q, kc, vc, o, lse, DEC_B, DEC_H, nk, d, 1.0 / math.sqrt(d), sp, ws,
+                                        ws.numel(), stream)
+            for _ in range(3):
+                call()
+            ms = timed(call, 20, False)
+            byt = 2.0 * DEC_B * DEC_H * nk * d * 2
+            out["decode_B32_H32"].append({"Nk": nk, "d": d, "splits": sp if sp > 0 else "auto", "ms": ms,
+                                          "gbs": byt / (ms * 1e-3) / 1e9})
+            del ws
+        del q, kc, vc, o, lse
     out["_windows"]["decode"] = (t0, time.time())
     t0 = time.time()
     for n in SWEEP_N:

@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -121,6 +122,50 @@ int decode_auto_splits(int Nk) {
     // chunks of at least 256 keys, at most 16 chunks
     int s = (Nk + 255) / 256;
     return s < 1 ? 1 : (s > 16 ? 16 : s);
+}
+
+int g_dec_blocks[kMaxDevices][2] = {};  // resident split-kernel CTAs per SM, by device and d (64, 128)
+
+// Automatic split count of the contiguous decode on CUDA cores.  One CTA per (b, h, split) keeps a
+// fixed number of loads in flight, so a launch costs about waves * (per-CTA time): waves =
+// ceil(B*H*splits / resident CTAs), per-CTA time = the split's key pieces plus a fixed cost of
+// about one piece (q load, reductions, the partial write), in keys.  Among 1 .. decode_auto_splits(Nk)
+// splits it takes the cheapest, the fewest on a tie (fewer partials to merge).  A split count
+// that spills a few CTAs into a second wave costs a whole wave: at B=8, H=32, Nk=4000, d=128 (7
+// CTAs per SM, 1064 resident) 4 splits read 0.83 of HBM and 6 splits 0.68.
+int decode_wave_splits(int B, int H, int Nk, int d, int* splits) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    int num_sms = 0;
+    int st = device_state(nullptr, &num_sms);
+    if (st != FA_OK) return st;
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        int& c = g_dec_blocks[dev][d == 128 ? 1 : 0];
+        if (!c) {
+            int b = 0;
+            if (decode_split_blocks_per_sm(d, &b) != cudaSuccess || b < 1) return FA_ERR_CUDA;
+            c = b;
+        }
+        per_sm = c;
+    }
+    const long long resident = (long long)num_sms * per_sm, bh = (long long)B * H;
+    const long long piece = d == 64 ? 256 : 128;  // keys per online-softmax step of the kernel
+    const int cap = decode_auto_splits(Nk);
+    int best = cap;
+    long long best_cost = LLONG_MAX;
+    for (int sp = 1; sp <= cap; ++sp) {
+        const long long chunk = (Nk + sp - 1) / sp;
+        const long long waves = (bh * sp + resident - 1) / resident;
+        const long long cost = waves * ((chunk + piece - 1) / piece * piece + 128);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = sp;
+        }
+    }
+    *splits = best;
+    return FA_OK;
 }
 
 // Paged decode, automatic splits.  The lengths live on the device, so the host
@@ -536,7 +581,14 @@ int fa_decode(const void* q, const void* kcache, const void* vcache, void* o, fl
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
         (lse && !aligned16(lse)))
         return FA_ERR_ALIGNMENT;
-    const int splits = num_splits <= 0 ? decode_auto_splits(Nk) : num_splits;
+    // automatic: the tensor-core path reads best with the most splits its length allows; the
+    // CUDA-core kernel takes the wave rule above.  Both stay within decode_auto_splits(Nk), the
+    // count fa_decode_workspace_bytes sizes for.
+    int splits = num_splits <= 0 ? decode_auto_splits(Nk) : num_splits;
+    if (num_splits <= 0 && !contiguous_on_mma(B, Nk, d)) {
+        st = decode_wave_splits(B, H, Nk, d, &splits);
+        if (st != FA_OK) return st;
+    }
     if (!workspace || workspace_bytes < decode_ws_bytes(B, H, d, splits)) return FA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
     if (contiguous_on_mma(B, Nk, d))
@@ -719,7 +771,11 @@ extern "C" int fa_decode_noalloc(const void* q, const void* kcache, const void* 
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
         (lse && !aligned16(lse)))
         return FA_ERR_ALIGNMENT;
-    const int splits = num_splits <= 0 ? decode_auto_splits(Nk) : num_splits;
+    int splits = num_splits <= 0 ? decode_auto_splits(Nk) : num_splits;  // the rule of fa_decode
+    if (num_splits <= 0 && !contiguous_on_mma(B, Nk, d)) {
+        st = decode_wave_splits(B, H, Nk, d, &splits);
+        if (st != FA_OK) return st;
+    }
     if (decode_ws_bytes(B, H, d, splits) > FA_DECODE_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;

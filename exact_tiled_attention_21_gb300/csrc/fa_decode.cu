@@ -469,6 +469,11 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
     return a.d == 128 ? launch_decode_d<128>(a, s) : launch_decode_d<64>(a, s);
 }
 
+cudaError_t decode_split_blocks_per_sm(int d, int* blocks) {
+    return d == 128 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_split_kernel<128>, kDecThreads, 0)
+                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_split_kernel<64>, kDecThreads, 0);
+}
+
 cudaError_t launch_decode_paged(const PagedDecodeLaunch& a, cudaStream_t s) {
     if (a.mma) return launch_decode_paged_mma(a, s);
     return a.d == 128 ? launch_paged_d<128>(a, s) : launch_paged_d<64>(a, s);

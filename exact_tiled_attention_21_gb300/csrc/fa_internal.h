@@ -201,6 +201,7 @@ cudaError_t launch_bwd_fused(const BwdLaunch& a, cudaStream_t s);  // dK, dV, dQ
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s, bool after_dkdv = false);  // dQ; after_dkdv:
                                                                                      // overlaps the dK/dV grid's end
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);
+cudaError_t decode_split_blocks_per_sm(int d, int* blocks);  // resident CTAs of the split kernel on one SM
 cudaError_t launch_decode_paged(const PagedDecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_paged_mma(const PagedDecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_fwd_fp8(const Fp8FwdLaunch& a, cudaStream_t s);  // V^T copy, then the forward

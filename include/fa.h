@@ -237,8 +237,8 @@ int fa_bwd_dkdv_pair(const void *q, const void *k, const void *v, const float *l
                      int causal, void *stream);
 
 /* Bytes of fp32 workspace fa_decode needs for num_splits partials (<= 0:
- * the number the library would choose for this Nk).  Returns 0 for invalid
- * sizes. */
+ * for min(16, ceil(Nk / 256)) splits, the most the automatic count takes).
+ * Host only, no device call.  Returns 0 for invalid sizes. */
 size_t fa_decode_workspace_bytes(int B, int H, int Nk, int d, int num_splits);
 
 /* Split-KV decode: one query token per (b, h) against a KV cache.  The key
@@ -255,8 +255,11 @@ size_t fa_decode_workspace_bytes(int B, int H, int Nk, int d, int num_splits);
  * other shape takes a kernel of 16-byte loads.  The result is the same up to
  * rounding either way.  q [B,H,d], kcache/vcache [B,H,Nk,d] bf16 in;
  * o [B,H,d] bf16 out; lse [B,H] fp32 out, may be NULL.  num_splits <= 0 lets
- * the library choose; otherwise 1 <= num_splits <= 256.  workspace: at least
- * fa_decode_workspace_bytes(B,H,Nk,d,num_splits) bytes. */
+ * the library choose: min(16, ceil(Nk / 256)) on the tensor-core kernel; on
+ * the other kernel the count in 1 .. min(16, ceil(Nk / 256)) whose
+ * (b, h, split) grid costs the fewest waves of resident CTAs times keys per
+ * split (ties: fewer splits).  Otherwise 1 <= num_splits <= 256.  workspace:
+ * at least fa_decode_workspace_bytes(B,H,Nk,d,num_splits) bytes. */
 int fa_decode(const void *q, const void *kcache, const void *vcache, void *o, float *lse,
               int B, int H, int Nk, int d, float scale, int num_splits,
               void *workspace, size_t workspace_bytes, void *stream);

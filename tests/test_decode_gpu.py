@@ -29,7 +29,9 @@ def _run(fa, q, kc, vc, scale, splits):
 # empty trailing splits (Nk < splits), a single key, automatic split count.
 # d = 128 with Nk a multiple of 128 runs on the tensor-core kernel (whole
 # 128-key stages per split, so trailing splits can be empty there too); every
-# other shape on the 16-byte-load kernel.
+# other shape on the 16-byte-load kernel.  The last two let the automatic
+# count of that kernel fall below its length cap (several hundred heads: it
+# keeps the (b, h, split) grid within whole waves of resident CTAs).
 CASES = [
     (1, 2, 128, 128, 1),
     (2, 3, 256, 128, 16),
@@ -53,6 +55,8 @@ CASES = [
     (1, 2, 8, 128, 1),
     (1, 2, 100, 128, 4),
     (2, 3, 70000, 64, 0),
+    (8, 32, 4000, 128, 0),
+    (16, 32, 2048, 64, 0),
 ]
 
 
