@@ -143,6 +143,34 @@ def test_backward_matches_step_entry_points(cuda_lib, B, H, N):
     assert torch.equal(dk_seen, dk2) and torch.equal(dv_seen, dv2)
 
 
+def test_backward_back_to_back_on_one_workspace(cuda_lib):
+    """Three fa_bwd calls queued back to back on one workspace (filled with 0xFF
+    bytes first): each call's preprocess overwrites D only after the dQ pass of
+    the call before it, which still reads D, is done, so every call gives the
+    bits of the three step entry points.  B=2, H=32, N=1536: 768 key tiles and
+    768 query tiles, five or six per CTA."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    B, H, N, d = 2, 32, 1536, 128
+    q, k, v, dO = (t.to(dev) for t in _inputs(5, B, H, N, N, d))
+    o, lse = fa.forward(q, k, v, causal=True)
+    ws = torch.full((fa.fa_bwd_workspace_bytes(B, H, N, N, d),), 255, dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(3):
+        g = [torch.full_like(q, float("nan")) for _ in range(3)]
+        fa.fa_bwd(q, k, v, o, lse, dO, g[0], g[1], g[2], B, H, N, N, d, d ** -0.5, True, ws, ws.numel())
+        outs.append(g)
+    delta = torch.empty(B, H, N, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa.fa_bwd_preprocess(o, dO, delta, B, H, N, d)
+    fa.fa_bwd_dkdv(q, k, v, lse, delta, dO, dk, dv, B, H, N, N, d, d ** -0.5, True)
+    fa.fa_bwd_dq(q, k, v, lse, delta, dO, dq, B, H, N, N, d, d ** -0.5, True)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error()[0] == 0
+    for g in outs:
+        assert torch.equal(g[0], dq) and torch.equal(g[1], dk) and torch.equal(g[2], dv)
+
+
 # fa_bwd_dkdv_pair takes key tiles two at a time: one key tile (the odd CTA's
 # tile lies wholly past Nk), odd and even tile counts, ragged and Nq != Nk.
 PAIR_CASES = [
