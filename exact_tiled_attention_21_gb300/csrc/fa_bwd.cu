@@ -374,15 +374,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // read out of TMEM
     const uint32_t B_KV = bar0, B_STF = bar0 + 8, B_STE = bar0 + 24, B_S = bar0 + 40, B_DP = bar0 + 48,
                    B_DS = bar0 + 56, B_ACC = bar0 + 64, B_TD = bar0 + 72, B_SF = bar0 + 80, B_TD2 = bar0 + 88,
-                   B_KE = bar0 + 96, B_ACCE = bar0 + 104, B_VE = bar0 + 112;
+                   B_KE = bar0 + 96, B_ACCE = bar0 + 104, B_VE = bar0 + 112, B_VF = bar0 + 120;
     // STF: the producer's 32 lanes (of each CTA of a pair); SF, DS: every compute thread, or in a
     // pair one elected thread per compute warp of each CTA; ACCE: every compute thread
     constexpr uint32_t N_STF = PAIR ? 64 : 32, N_SD = PAIR ? 16 : 256;
-    const uint32_t counts[15] = {1, N_STF, N_STF, 2, 2, 1, 1, N_SD, 1, 1, N_SD, 1, 1, 256, 1};
-    static_assert(15 <= C::NBAR, "barrier space");
+    const uint32_t counts[16] = {1, N_STF, N_STF, 2, 2, 1, 1, N_SD, 1, 1, N_SD, 1, 1, 256, 1, 1};
+    static_assert(16 <= C::NBAR, "barrier space");
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
-    const uint32_t tmem = bwd_setup<D, PAIR>(smem, bar0, ctl, counts, 15);
+    const uint32_t tmem = bwd_setup<D, PAIR>(smem, bar0, ctl, counts, 16);
     const uint32_t rank = PAIR ? cluster_rank() : 0u;
     const bool lead = rank == 0;  // the CTA whose thread issues the products
     // a barrier the issuing thread waits on, as addressed from this CTA
@@ -444,27 +444,33 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     auto sQ = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE; };
     auto sDO = [&](int st) { return s_base + C::OFF_STAGE + st * 2 * C::TILE + C::TILE; };
     float* vec = (float*)(smem + C::OFF_VEC);  // stage s: lse2 at [s*256], delta at [s*256 + 128]
-    auto load_kv = [&](const Item& it) {  // one lane
-        if (lead) mbar_arrive_expect_tx(B_KV, (PAIR ? 4 : 2) * C::TILE);
-        const uint32_t kvb = lead_bar(B_KV);
+    // K (completing B_KV) and V (B_VF) load separately: an item's K is free after its last S^T,
+    // its V only after its last dP^T, and the next item's first S^T needs only K
+    auto load_t = [&](const Item& it, bool is_v) {  // one lane
+        const uint32_t bar = is_v ? B_VF : B_KV;
+        if (lead) mbar_arrive_expect_tx(bar, (PAIR ? 2 : 1) * C::TILE);
+        const uint32_t fb = lead_bar(bar);
+        const uint32_t dst = is_v ? sV : sK;
+        const CUtensorMap* m = is_v ? &map_v : &map_k;
         for (int c = 0; c < C::KCH; ++c) {
-            if constexpr (PAIR) {
-                tma_load_3d_pair(sK + c * C::CHUNK, &map_k, kvb, c * 64, it.kt * 128, it.bh, l2_policy_evict_last());
-                tma_load_3d_pair(sV + c * C::CHUNK, &map_v, kvb, c * 64, it.kt * 128, it.bh, l2_policy_evict_last());
-            } else {
-                tma_load_3d(sK + c * C::CHUNK, &map_k, kvb, c * 64, it.kt * 128, it.bh, l2_policy_evict_last());
-                tma_load_3d(sV + c * C::CHUNK, &map_v, kvb, c * 64, it.kt * 128, it.bh, l2_policy_evict_last());
-            }
+            if constexpr (PAIR)
+                tma_load_3d_pair(dst + c * C::CHUNK, m, fb, c * 64, it.kt * 128, it.bh, l2_policy_evict_last());
+            else
+                tma_load_3d(dst + c * C::CHUNK, m, fb, c * 64, it.kt * 128, it.bh, l2_policy_evict_last());
         }
+    };
+    auto load_kv = [&](const Item& it) {
+        load_t(it, false);
+        load_t(it, true);
     };
     // the first item's K and V do not come from the preprocess: they load before the wait for it
     ItemSeq q0;
     const int w_first = next_item(q0);
     const bool first_active = w_first < n_items && item_of(w_first).n > 0;
-    int kv_fills = 0;  // K/V loads issued (producer lane 0)
+    int k_fills = 0, v_fills = 0;  // K and V loads issued (producer lane 0)
     if (warp == C::PRODUCER && lane == 0 && first_active && !*abort_flag) {
         load_kv(item_of(w_first));
-        kv_fills = 1;
+        k_fills = v_fills = 1;
     }
     // Launched as a programmatic dependent of the preprocess, this grid may start before D is
     // complete: every read of D comes after this wait.  Then the dQ pass launched after this grid
@@ -473,7 +479,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // Every role counts the query tiles (g) and the items with at least one (a) it has taken:
-    // the per-tile barriers complete once per query tile, B_KV, B_ACC, B_KE, B_VE and B_ACCE once
+    // the per-tile barriers complete once per query tile, B_KV, B_VF, B_ACC, B_KE, B_VE and B_ACCE once
     // per item with query tiles, so their parities follow these counts.
     if (warp == C::PRODUCER) {
         // ------------------------------------------------------------ producer (whole warp)
@@ -510,14 +516,19 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 if (it.n == 0) continue;
                 if (a > 0) {  // K and V of the last item are free once its last S^T and dP^T are done
                     if (!(ok = bwait<PAIR>(B_KE, (a - 1) & 1, ctl, kSiteBwdQEmpty))) break;
+                    if (lane == 0) {
+                        load_t(it, false);
+                        ++k_fills;
+                    }
                     if (!(ok = bwait<PAIR>(B_VE, (a - 1) & 1, ctl, kSiteBwdQEmpty))) break;
                     if (lane == 0) {
-                        load_kv(it);
-                        ++kv_fills;
+                        load_t(it, true);
+                        ++v_fills;
                     }
                 } else if (!first_active && lane == 0) {
                     load_kv(it);
-                    ++kv_fills;
+                    ++k_fills;
+                    ++v_fills;
                 }
                 fetch_vec(it, it.i0);
                 for (int ii = 0; ii < it.n; ++ii) {
@@ -561,7 +572,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         // let the loads in flight land before exit (in a pair, the even CTA's barriers
         // count the odd CTA's loads too)
         if (*abort_flag && lane == 0 && lead) {
-            if (kv_fills > 0) bdrain<PAIR>(B_KV, (kv_fills - 1) & 1, ctl, kSiteTeardown);
+            if (k_fills > 0) bdrain<PAIR>(B_KV, (k_fills - 1) & 1, ctl, kSiteTeardown);
+            if (v_fills > 0) bdrain<PAIR>(B_VF, (v_fills - 1) & 1, ctl, kSiteTeardown);
             for (int st = 0; st < 2; ++st)
                 if (issued & (1u << st))
                     bdrain<PAIR>(B_STF + 8 * st, (issued_par >> st) & 1, ctl, kSiteTeardown);
@@ -613,7 +625,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 if (w >= n_items) break;
                 const Item it = item_of(w);
                 if (it.n == 0) continue;
-                if (!(ok = bwait<PAIR>(B_KV, a & 1, ctl, kSiteBwdKvFull))) break;
+                if (!(ok = bwait<PAIR>(B_VF, a & 1, ctl, kSiteBwdKvFull))) break;
                 if (!(ok = bwait<PAIR>(B_STF + 8 * (g & 1), (g >> 1) & 1, ctl, kSiteBwdQFull))) break;
                 tc_fence_after();
                 if constexpr (PAIR)
