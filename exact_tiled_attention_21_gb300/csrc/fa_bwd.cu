@@ -972,23 +972,28 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             // Q_i and dO_i into TMEM as the A operands of the score products: row = lane,
             // bf16 pairs in column order; warpgroup h writes d-columns [h D/2, (h+1) D/2)
             if (n > 0) {
-                constexpr int W = D / 4;  // 32-bit words per half row
+                // both half rows' loads in flight before the first TMEM store (32-byte loads
+                // where the rows allow: a warp instruction touches each row's line once per 32 bytes)
+                constexpr int NC = D / 64;  // 64-byte pieces per half row (D / 2 bf16)
+                const size_t ro = ((size_t)bh * p.Nq + (row_ok ? qg : 0)) * D + h * (D / 2);
+                const bool wide = (((uintptr_t)(p.q + ro) | (uintptr_t)(p.dO + ro)) & 31) == 0;
+                uint32_t wq[NC][16], wo[NC][16];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const __nv_bfloat16* src = (u ? p.dO : p.q) + ((size_t)bh * p.Nq + (row_ok ? qg : 0)) * D + h * (D / 2);
-                    uint32_t wd[W];
-#pragma unroll
-                    for (int e = 0; e < W / 4; ++e) {
-                        const uint4 x = row_ok ? __ldg(reinterpret_cast<const uint4*>(src) + e) : make_uint4(0, 0, 0, 0);
-                        wd[4 * e] = x.x, wd[4 * e + 1] = x.y, wd[4 * e + 2] = x.z, wd[4 * e + 3] = x.w;
-                    }
-                    const uint32_t col = (u ? COL_DOA : COL_QA) + h * (D / 4);
-                    if constexpr (W == 32) {
-                        tmem_st32(lane_addr + col, wd);
+                for (int c = 0; c < NC; ++c) {
+                    if (row_ok) {
+                        load_row64_nc(p.q + ro + 32 * c, wq[c], wide);
+                        load_row64_nc(p.dO + ro + 32 * c, wo[c], wide);
                     } else {
-                        tmem_st16(lane_addr + col, wd);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) wq[c][i] = wo[c][i] = 0u;
                     }
                 }
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    tmem_st16_async(lane_addr + COL_QA + h * (D / 4) + 16 * c, wq[c]);
+                    tmem_st16_async(lane_addr + COL_DOA + h * (D / 4) + 16 * c, wo[c]);
+                }
+                tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(B_QA);
             }

@@ -375,6 +375,26 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // aligned (`wide`), else as four 16-byte stores.  A thread writes a piece of its
 // own row, so a warp's store touches 32 rows at once; the wider store halves the
 // number of store instructions and of the cache lines they touch per byte.
+// 64 bytes from global memory (read-only path): two 32-byte loads when `wide`
+// (src 32-byte aligned), else four 16-byte loads.
+__device__ __forceinline__ void load_row64_nc(const void* src, uint32_t (&w)[16], bool wide) {
+    if (wide) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                         : "=r"(w[8 * h]), "=r"(w[8 * h + 1]), "=r"(w[8 * h + 2]), "=r"(w[8 * h + 3]),
+                           "=r"(w[8 * h + 4]), "=r"(w[8 * h + 5]), "=r"(w[8 * h + 6]), "=r"(w[8 * h + 7])
+                         : "l"((const char*)src + 32 * h));
+    } else {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 x = __ldg(s4 + i);
+            w[4 * i] = x.x, w[4 * i + 1] = x.y, w[4 * i + 2] = x.z, w[4 * i + 3] = x.w;
+        }
+    }
+}
+
 __device__ __forceinline__ void store_row64(void* dst, const uint32_t (&w)[16], bool wide) {
     if (wide) {
 #pragma unroll
