@@ -801,15 +801,16 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------------------ one kernel for a profiler
-PROFILE_TARGETS = ("fwd", "dkdv", "dq", "fused", "pair", "decode", "decode64", "paged", "fp8")
+PROFILE_TARGETS = ("fwd", "dkdv", "dq", "fused", "pair", "decode", "decode64", "paged", "paged48", "fp8")
 
 
 def run_profile(target, launches):
     """Runs one kernel of the bench workload ``launches`` times (after one warm-up
     call) with only its own inputs on the device, for an ncu capture:
     fwd / dkdv / dq / fused / pair at B=1, H=32, N=8192, d=128 causal; decode at
-    B=32, H=32, Nk=4096 (d=128 or d=64); paged at B=32, Hq=32, Hkv=8, page 16;
-    fp8 the FP8 forward.  Prints one line; no timing."""
+    B=32, H=32, Nk=4096 (d=128 or d=64); paged at B=32, Hq=32, Hkv=8, page 16 (the
+    tensor-core kernel) and paged48 with 48-token pages, 85 per sequence (4080
+    tokens: the general kernel); fp8 the FP8 forward.  Prints one line; no timing."""
     import torch
     import exact_tiled_attention_21_gb300 as fa
     dev = torch.device("cuda", 0)
@@ -842,14 +843,14 @@ def run_profile(target, launches):
                          device=dev)
         call = lambda: fa.fa_decode(qd, kc, vc, od, lsed, DEC_B, DEC_H, DEC_NK, d, 1 / math.sqrt(d), DEC_SPLITS, ws,
                                     ws.numel(), s)
-    elif target == "paged":
-        hkv, page = 8, 16
+    elif target in ("paged", "paged48"):
+        hkv, page = (8, 16) if target == "paged" else (8, 48)
         npages = DEC_B * (DEC_NK // page)
         kp, vp = rnd(npages, hkv, page, D), rnd(npages, hkv, page, D)
         qd = rnd(DEC_B, DEC_H, D)
         table = torch.randperm(npages, generator=torch.Generator().manual_seed(5)).to(torch.int32)
         table = table.reshape(DEC_B, DEC_NK // page).to(dev)
-        lens = torch.full((DEC_B,), DEC_NK, dtype=torch.int32, device=dev)
+        lens = torch.full((DEC_B,), (DEC_NK // page) * page, dtype=torch.int32, device=dev)
         od = torch.empty_like(qd)
         lsed = torch.empty(DEC_B, DEC_H, device=dev)
         ws = torch.empty(fa.fa_decode_paged_workspace_bytes(DEC_B, DEC_H, D, 0), dtype=torch.uint8, device=dev)

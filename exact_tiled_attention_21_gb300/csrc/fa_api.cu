@@ -92,8 +92,8 @@ int make_map_nd(CUtensorMap* m, const void* base, int rank, const cuuint64_t* di
 
 // Page sizes the tensor-core paged decode takes: whole 8-row swizzle atoms
 // per page, and pages that tile a 128-key stage (or stages that tile a page).
-bool paged_mma_ok(int B, int d, int page) {
-    if (B > 2048 || (d != 64 && d != 128) || page % 8 != 0) return false;  // lengths of up to 2048 sequences staged on chip
+bool paged_mma_ok(int d, int page) {
+    if ((d != 64 && d != 128) || page % 8 != 0) return false;
     return page <= 128 ? (128 % page == 0) : (page % 128 == 0);
 }
 
@@ -535,7 +535,7 @@ int paged_mma_maps(PagedDecodeLaunch& a) {
 // stage, which d = 128 hides behind 64 KB of cache per stage, shows at d = 64 (4.0 against 5.8 TB/s
 // at Nk = 4096) and on a ragged last stage (6.0 against 6.2 TB/s at Nk = 4000).  Returns false when
 // the shape takes the 16-byte-load kernel.
-bool contiguous_on_mma(int B, int Nk, int d) { return d == 128 && Nk % 128 == 0 && paged_mma_ok(B, d, Nk); }
+bool contiguous_on_mma(int Nk, int d) { return d == 128 && Nk % 128 == 0 && paged_mma_ok(d, Nk); }
 
 int launch_contiguous_on_mma(const void* q, const void* kcache, const void* vcache, void* o, float* lse, int B,
                              int H, int Nk, int d, float scale, int splits, float* part_o, void* stream) {
@@ -585,13 +585,13 @@ int fa_decode(const void* q, const void* kcache, const void* vcache, void* o, fl
     // CUDA-core kernel takes the wave rule above.  Both stay within decode_auto_splits(Nk), the
     // count fa_decode_workspace_bytes sizes for.
     int splits = num_splits <= 0 ? decode_auto_splits(Nk) : num_splits;
-    if (num_splits <= 0 && !contiguous_on_mma(B, Nk, d)) {
+    if (num_splits <= 0 && !contiguous_on_mma(Nk, d)) {
         st = decode_wave_splits(B, H, Nk, d, &splits);
         if (st != FA_OK) return st;
     }
     if (!workspace || workspace_bytes < decode_ws_bytes(B, H, d, splits)) return FA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
-    if (contiguous_on_mma(B, Nk, d))
+    if (contiguous_on_mma(Nk, d))
         return launch_contiguous_on_mma(q, kcache, vcache, o, lse, B, H, Nk, d, scale, splits,
                                         static_cast<float*>(workspace), stream);
     st = device_state(nullptr, nullptr);
@@ -635,7 +635,7 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, con
     PagedDecodeLaunch a;
     int st = device_state(&a.err, &a.num_sms);
     if (st != FA_OK) return st;
-    a.mma = paged_mma_ok(B, d, page_size);
+    a.mma = paged_mma_ok(d, page_size);
     if (num_splits <= 0)
         num_splits = paged_auto_splits(B, Hq, Hkv, max_pages * page_size, a.num_sms, a.mma);
     if (!workspace || workspace_bytes < decode_ws_bytes(B, Hq, d, num_splits)) return FA_ERR_WORKSPACE;
@@ -772,7 +772,7 @@ extern "C" int fa_decode_noalloc(const void* q, const void* kcache, const void* 
         (lse && !aligned16(lse)))
         return FA_ERR_ALIGNMENT;
     int splits = num_splits <= 0 ? decode_auto_splits(Nk) : num_splits;  // the rule of fa_decode
-    if (num_splits <= 0 && !contiguous_on_mma(B, Nk, d)) {
+    if (num_splits <= 0 && !contiguous_on_mma(Nk, d)) {
         st = decode_wave_splits(B, H, Nk, d, &splits);
         if (st != FA_OK) return st;
     }
@@ -789,7 +789,7 @@ extern "C" int fa_decode_noalloc(const void* q, const void* kcache, const void* 
         }
         scratch = g_scratch_addr[dev];
     }
-    if (contiguous_on_mma(B, Nk, d))
+    if (contiguous_on_mma(Nk, d))
         return launch_contiguous_on_mma(q, kcache, vcache, o, lse, B, H, Nk, d, scale, splits,
                                         static_cast<float*>(scratch), stream);
     DecodeLaunch a;

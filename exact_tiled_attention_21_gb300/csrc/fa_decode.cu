@@ -232,8 +232,9 @@ cudaError_t launch_decode_d(const DecodeLaunch& a, cudaStream_t s) {
 
 
 // ------------------------------------------------------------------ paged, grouped-query decode
-// The general path (d = 64, page sizes the tensor-core kernel of
-// fa_decode_mma.cu does not take, more than 2048 sequences).  One CTA per (b,
+// The general path (page sizes the tensor-core kernel of fa_decode_mma.cu
+// does not take: not a multiple of 8, or neither dividing 128 nor a multiple
+// of 128).  One CTA per (b,
 // kv head, split, group of G <= 4 query heads).  The split's keys are the
 // logical tokens [split * chunk, min(len, (split + 1) * chunk)) of the
 // sequence, chunk = ceil(len / splits); each 128-key piece's page rows are
@@ -243,8 +244,15 @@ cudaError_t launch_decode_d(const DecodeLaunch& a, cudaStream_t s) {
 // contiguous decode.  A page index outside [0, num_pages) or
 // a length outside [1, max_pages * page] is recorded as FA_ERR_INVALID_ARG in
 // the error word and read as zeros, never dereferenced.
+// Resident CTAs per SM the general paged kernel is compiled for.  With four query heads per CTA the
+// compiler would otherwise take 168 registers at d = 128 (three CTAs per SM, 0.48 of HBM at
+// Hq/Hkv = 4 and 48-token pages); 127 leave four (0.53); five would spill.  The others keep the
+// occupancy their register use gives anyway.
 template <int D, int G>
-__global__ void __launch_bounds__(kDecThreads)
+constexpr int kPagedMinCtas = G == 4 ? 4 : (D == 128 ? (G == 2 ? 6 : 7) : (G == 2 ? 7 : 10));
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecThreads, kPagedMinCtas<D, G>)
 decode_paged_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kp,
                           const __nv_bfloat16* __restrict__ vp, const int* __restrict__ table,
                           const int* __restrict__ lens, float* __restrict__ part_o,

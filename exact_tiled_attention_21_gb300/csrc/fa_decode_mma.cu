@@ -62,7 +62,7 @@ struct Dm {
     static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;  // fp32 max [2][4][16], sums [4][16]
     static constexpr int OFF_X = OFF_RED + (2 * 4 * 16 + 4 * 16) * 4;  // d = 64: the second O^T half, [64][16] fp32
     static constexpr int OFF_LENS = OFF_X + (D == 64 ? 64 * 16 * 4 : 0);  // int32 [MAX_B]
-    static constexpr int MAX_B = 2048;
+    static constexpr int MAX_B = 2048;  // lengths staged in shared memory (later ones read from global)
     static constexpr int OFF_BAR = OFF_LENS + MAX_B * 4;
     // k_full, k_empty, v_full, v_empty [NSLOT each], q_full[2], q_empty[2], s_full[2], p_ready[2], pv_done[2],
     // o_final, teardown
@@ -127,10 +127,18 @@ __device__ __forceinline__ int clamp_len(const MmaParams& p, int len) {
     return len < 1 ? 0 : min(len, cap);
 }
 
-template <int NH>
+// Length of sequence b: staged in shared memory for the first MAX_B sequences, read (and clamped)
+// from global memory past them.
+template <int D>
+__device__ __forceinline__ int seq_len(const MmaParams& p, int b, const int* s_lens) {
+    if (b < Dm<D>::MAX_B) return s_lens[b];
+    return clamp_len(p, p.lens ? __ldg(p.lens + b) : p.max_pages * p.page);
+}
+
+template <int D, int NH>
 __device__ __forceinline__ Item item_of(const MmaParams& p, int w, const int* s_lens) {
     const int b = (int)((unsigned)w / ((unsigned)p.splits * p.ngrp * p.Hkv));
-    return item_at<NH>(p, w, s_lens[b]);
+    return item_at<NH>(p, w, seq_len<D>(p, b, s_lens));
 }
 
 // Butterfly over the 32 lanes of a warp for NH values per lane (NH = 4, 8,
@@ -211,7 +219,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
     for (int b = tid; b < p.B; b += Dm::THREADS) {
         const int raw = p.lens ? __ldg(p.lens + b) : p.max_pages * p.page;
         const int len = clamp_len(p, raw);
-        s_lens[b] = len;
+        if (b < Dm::MAX_B) s_lens[b] = len;
         if (len != raw && blockIdx.x == 0 && atomicCAS(&p.err->code, 0, kErrInvalid) == 0) {
             p.err->site = kSitePagedTable;
             p.err->block = b;
@@ -248,14 +256,14 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
         // two items ahead, so their latency hides behind two items of copies.
         auto first_entries = [&](int w2) {
             if (w2 >= p.nitems) return 0;
-            const Item n = item_of<NH>(p, w2, s_lens);
+            const Item n = item_of<D, NH>(p, w2, s_lens);
             const int pi = n.k0 / p.page + lane;
             if (!(n.k0 < n.k1 && pi < p.max_pages)) return 0;
             return p.table ? __ldg(p.table + (size_t)n.b * p.max_pages + pi) : n.b * p.max_pages + pi;
         };
         int tb0 = first_entries(first), tb1 = first_entries(first + grid);
         for (int w = first; w < p.nitems && ok; w += grid) {
-            const Item it = item_of<NH>(p, w, s_lens);
+            const Item it = item_of<D, NH>(p, w, s_lens);
             int tbl = tb0;
             tb0 = tb1;
             tb1 = first_entries(w + 2 * grid);
@@ -346,7 +354,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             };
             auto seek = [&](Cur& c, int w) {  // first item with keys at or after w
                 for (; w < p.nitems; w += grid) {
-                    const Item it = item_of<NH>(p, w, s_lens);
+                    const Item it = item_of<D, NH>(p, w, s_lens);
                     if (it.k0 < it.k1) {
                         c.w = w;
                         c.j = 0;
@@ -445,13 +453,13 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
         const int R = min(p.page, 128);
         bool failed = false;
         for (int w = first; w < p.nitems && !failed; w += grid) {
-            const Item it = item_of<NH>(p, w, s_lens);
+            const Item it = item_of<D, NH>(p, w, s_lens);
             const size_t head0 = (size_t)it.b * p.Hq + it.h0;
             if (it.k0 >= it.k1) {  // empty split: weight 0 in the combine
                 if (r < D)
                     for (int h = 0; h < it.gcount; ++h)
-                        p.part_o[((head0 + h) * p.splits + it.split) * Dm::D + r] = 0.f;
-                if (r < it.gcount) p.part_lse[(head0 + r) * p.splits + it.split] = -INFINITY;
+                        p.part_o[((size_t)(head0 + h) * p.splits + it.split) * Dm::D + r] = 0.f;
+                if (r < it.gcount) p.part_lse[(size_t)(head0 + r) * p.splits + it.split] = -INFINITY;
                 continue;
             }
             const int nst = (it.k1 - it.k0 + Dm::BK - 1) / Dm::BK;
@@ -571,7 +579,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             ++items;
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
-            float* po = p.part_o + (head0 * p.splits + it.split) * Dm::D + r;
+            float* po = p.part_o + ((size_t)head0 * p.splits + it.split) * Dm::D + r;
             if constexpr (D == 128) {
                 uint32_t ov[16];
                 if (ok) {
@@ -610,7 +618,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                                 (__uint_as_float(ov[h]) + xo[r * 16 + ((h + r) & 15)]) * inv_l[h];
                 }
             }
-            if (r < it.gcount) p.part_lse[(head0 + r) * p.splits + it.split] = lse;
+            if (r < it.gcount) p.part_lse[(size_t)(head0 + r) * p.splits + it.split] = lse;
         }
     }
 
@@ -646,7 +654,7 @@ cudaError_t launch_d(const PagedDecodeLaunch& a, const MmaParams& p, cudaStream_
 }  // namespace
 
 cudaError_t launch_decode_paged_mma(const PagedDecodeLaunch& a, cudaStream_t s) {
-    if (a.B > Dm<128>::MAX_B || (a.d != 64 && a.d != 128)) return cudaErrorInvalidValue;
+    if (a.d != 64 && a.d != 128) return cudaErrorInvalidValue;
     MmaParams p;
     p.B = a.B;
     p.table = a.table;

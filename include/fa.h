@@ -248,8 +248,8 @@ size_t fa_decode_workspace_bytes(int B, int H, int Nk, int d, int num_splits);
  * ceil(Nk / num_splits) keys; each chunk yields a partial output and partial
  * LSE, and the partials are merged with the max-shifted rescaling of the
  * online-softmax recurrence (wiki.ai-engineering.at "Flash Attention",
- * "Lösung: Online Softmax").  With d = 128, Nk a multiple of 128 and
- * B <= 2048 the chunks are read by the tensor-core kernel of
+ * "Lösung: Online Softmax").  With d = 128 and Nk a multiple of 128 the
+ * chunks are read by the tensor-core kernel of
  * fa_decode_paged (the cache as one page per sequence), whose chunks are
  * rounded up to whole 128-key stages, so trailing chunks may be empty; every
  * other shape takes a kernel of 16-byte loads.  The result is the same up to
@@ -284,8 +284,8 @@ size_t fa_decode_paged_workspace_bytes(int B, int Hq, int d, int num_splits);
  * possible sequence max_pages * page_size and the SM count; at most 16).
  * Each sequence is cut into num_splits (1..256) contiguous chunks of
  * ceil(seq_lens[b] / num_splits) tokens (rounded up to whole 128-token stages
- * on the tensor-core path: d = 128, B <= 2048, page_size a multiple of 8 that
- * divides 128 or is a multiple of 128), merged as in fa_decode.  Every K/V
+ * on the tensor-core path: page_size a multiple of 8 that divides 128 or is
+ * a multiple of 128), merged as in fa_decode.  Every K/V
  * row is read once per group of up to 16 query heads on that path (4 on the
  * general one).  Tokens past seq_lens[b] in a page are never used, whatever
  * they hold.  Host checks: Hq % Hkv

@@ -29,9 +29,10 @@ def _run(fa, q, kc, vc, scale, splits):
 # empty trailing splits (Nk < splits), a single key, automatic split count.
 # d = 128 with Nk a multiple of 128 runs on the tensor-core kernel (whole
 # 128-key stages per split, so trailing splits can be empty there too); every
-# other shape on the 16-byte-load kernel.  The last two let the automatic
-# count of that kernel fall below its length cap (several hundred heads: it
-# keeps the (b, h, split) grid within whole waves of resident CTAs).
+# other shape on the 16-byte-load kernel.  B=8 H=32 and B=16 H=32 let the
+# automatic count of that kernel fall below its length cap (several hundred
+# heads: it keeps the (b, h, split) grid within whole waves of resident CTAs);
+# B=2100 has more sequences than the tensor-core kernel stages lengths for.
 CASES = [
     (1, 2, 128, 128, 1),
     (2, 3, 256, 128, 16),
@@ -57,6 +58,7 @@ CASES = [
     (2, 3, 70000, 64, 0),
     (8, 32, 4000, 128, 0),
     (16, 32, 2048, 64, 0),
+    (2100, 2, 256, 128, 0),
 ]
 
 

@@ -145,3 +145,36 @@ def test_paged_decode_growing_scores(cuda_lib, d):
     # late keys dominate (|O| ~ |v|): the rounding bound per element applies
     vmax = float(np.abs(f64(vp)).max())
     check_out_elementwise(f64(o), f64(lse), o_ref, lse_ref, vmax, "growing scores")
+
+
+@pytest.mark.parametrize("d,splits", [(128, 0), (64, 3)])
+def test_paged_decode_more_sequences_than_staged_lengths(cuda_lib, d, splits):
+    """B=2100 sequences on the tensor-core path: the kernel stages the first
+    2048 lengths in shared memory and reads the others per work item.  Every
+    sequence against the oracle (lengths 1..200, 16-token pages, groups of 4)."""
+    rng = np.random.default_rng(2100 + d)
+    lens = list(rng.integers(1, 201, size=2100))
+    lens[2047], lens[2048], lens[2099] = 200, 1, 129  # either side of the staged range
+    q, kp, vp, table, L = _case(61 + d, 2100, 8, 2, 16, lens, d)
+    o, lse = _run(cuda_lib, q, kp, vp, table, L, splits)
+    o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(d))
+    check_out(f64(o), f64(lse), o_ref, lse_ref, "B2100 d%d" % d)
+
+
+def test_paged_decode_length_out_of_range_past_the_staged_lengths(cuda_lib):
+    """A length above max_pages * page for a sequence past the first 2048 is
+    clamped to the table, never read past it, and recorded as
+    FA_ERR_INVALID_ARG; the other sequences are unaffected."""
+    lens = [40] * 2060
+    q, kp, vp, table, L = _case(8, 2060, 4, 2, 16, lens, 128)
+    L[2050] = 10 ** 6
+    dev = torch.device("cuda", 0)
+    o, lse = cuda_lib.decode_paged(q.to(dev), kp.to(dev), vp.to(dev), torch.from_numpy(table).to(dev),
+                                   torch.from_numpy(L).to(dev), num_splits=2)
+    st, detail = cuda_lib.fa_get_last_device_error()
+    assert st == fa_mod.FA_ERR_INVALID_ARG, detail
+    assert detail[2] == 2050 and detail[3] == 10 ** 6
+    L_ok = L.copy()
+    L_ok[2050] = table.shape[1] * 16  # the clamped length: the whole table row
+    o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L_ok, 1 / math.sqrt(128))
+    check_out(f64(o.cpu()), f64(lse.cpu()), o_ref, lse_ref, "clamped length")
