@@ -253,8 +253,12 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
     """Every workload of the 1k-8k protocol and the other configurations, each
     timed on its own: the forward and the backward of B=1, H=32, d=128 causal at
     N = 1024 ... 8192; the forward at B=2, H=32, N=4096 causal and non-causal;
+    the forward and backward under a causal 256-key sliding window (B=1, H=32,
+    N=8192) and with per-sequence lengths 8192 / 5000 / 2500 / 700 (B=4, H=32,
+    padded to 8192, causal), their FLOPs counted over the pairs the mask keeps;
     the long causal forward at N=131072 with its peak device memory; decode at
-    B=32, H=32 for d=128 with Nk=4096 and Nk=4000 and for d=64.  Each entry is
+    B=32, H=32 for d=128 with Nk=4096 and Nk=4000 and for d=64, with 16 splits
+    and with the automatic count.  Each entry is
     the median over calls bracketed by CUDA events on the launching stream.  L2
     is flushed (a 256 MiB write) before every call whose inputs would otherwise
     stay in it; decode caches (>= 1 GiB) are larger than L2.  Decode runs first
@@ -346,6 +350,43 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
         out["fwd_B2_H32_N4096_d128"].append({"causal": causal, "fwd_ms": f_ms,
                                              "fwd_tflops": fl / (f_ms * 1e-3) / 1e12})
         del q, k, v, o, lse
+    # the mask variants: a causal sliding window of 256 keys, and per-sequence lengths in a padded
+    # batch; their FLOPs count only the (query, key) pairs the mask keeps
+    nw, win = 8192, 256
+    q, k, v, dO = (rnd(1, H, nw, D) for _ in range(4))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    lse = torch.empty(1, H, nw, device=dev, dtype=torch.float32)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(1, H, nw, nw, D), dtype=torch.uint8, device=dev)
+    fwd = lambda: fa.fa_fwd_window(q, k, v, o, lse, 1, H, nw, nw, D, SCALE, win, stream)
+    bwd = lambda: fa.fa_bwd_window(q, k, v, o, lse, dO, dq, dk, dv, 1, H, nw, nw, D, SCALE, win, ws, ws.numel(),
+                                   stream)
+    for _ in range(3):
+        fwd()
+        bwd()
+    f_ms, b_ms = timed(fwd, 10, True), timed(bwd, 10, True)
+    fl = 4.0 * H * (win * nw - win * (win - 1) / 2) * D  # query i sees min(i + 1, 256) keys
+    out["window_B1_H32_N8192_d128_W256"] = {"fwd_ms": f_ms, "fwd_tflops": fl / (f_ms * 1e-3) / 1e12,
+                                            "bwd_ms": b_ms, "bwd_tflops": 2.5 * fl / (b_ms * 1e-3) / 1e12}
+    del q, k, v, dO, o, dq, dk, dv, lse, ws
+    lens = [8192, 5000, 2500, 700]
+    nb = len(lens)
+    q, k, v, dO = (rnd(nb, H, nw, D) for _ in range(4))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    lse = torch.empty(nb, H, nw, device=dev, dtype=torch.float32)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(nb, H, nw, nw, D), dtype=torch.uint8, device=dev)
+    sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+    fwd = lambda: fa.fa_fwd_varlen(q, k, v, o, lse, sl, sl, nb, H, nw, nw, D, SCALE, True, stream)
+    bwd = lambda: fa.fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, sl, sl, nb, H, nw, nw, D, SCALE, True, ws,
+                                   ws.numel(), stream)
+    for _ in range(3):
+        fwd()
+        bwd()
+    f_ms, b_ms = timed(fwd, 10, True), timed(bwd, 10, True)
+    fl = 4.0 * H * sum(n * (n + 1) / 2 for n in lens) * D
+    out["varlen_causal_B4_H32_N8192_d128"] = {"lens": lens, "fwd_ms": f_ms,
+                                              "fwd_tflops": fl / (f_ms * 1e-3) / 1e12, "bwd_ms": b_ms,
+                                              "bwd_tflops": 2.5 * fl / (b_ms * 1e-3) / 1e12}
+    del q, k, v, dO, o, dq, dk, dv, lse, ws, sl
     out["_windows"]["short"] = (t0, time.time())
 
     # long causal forward (last: its seconds of full load can bring the power cap in).  Its
@@ -397,6 +438,10 @@ def finish_sweep(sw, pk, sampler):
         e["bwd_fused_frac"] = e["bwd_fused_tflops"] / pk["bf16"]
     for e in sw["fwd_B2_H32_N4096_d128"]:
         e["fwd_frac"] = e["fwd_tflops"] / pk["bf16"]
+    for key in ("window_B1_H32_N8192_d128_W256", "varlen_causal_B4_H32_N8192_d128"):
+        e = sw[key]
+        e["fwd_frac"] = e["fwd_tflops"] / pk["bf16"]
+        e["bwd_frac"] = e["bwd_tflops"] / pk["bf16"]
     lo = sw["fwd_long_causal_B1_H32_N131072_d128"]
     lo["fwd_frac"] = lo["fwd_tflops"] / pk["bf16"]
     for e in sw["decode_B32_H32"]:
