@@ -846,13 +846,14 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------------------ one kernel for a profiler
-PROFILE_TARGETS = ("fwd", "dkdv", "dq", "fused", "pair", "decode", "decode64", "paged", "paged48", "fp8")
+PROFILE_TARGETS = ("fwd", "dkdv", "dq", "fused", "pair", "window", "decode", "decode64", "paged", "paged48", "fp8")
 
 
 def run_profile(target, launches):
     """Runs one kernel of the bench workload ``launches`` times (after one warm-up
     call) with only its own inputs on the device, for an ncu capture:
-    fwd / dkdv / dq / fused / pair at B=1, H=32, N=8192, d=128 causal; decode at
+    fwd / dkdv / dq / fused / pair at B=1, H=32, N=8192, d=128 causal; window the
+    forward under a causal 256-key window at the same size; decode at
     B=32, H=32, Nk=4096 (d=128 or d=64); paged at B=32, Hq=32, Hkv=8, page 16 (the
     tensor-core kernel) and paged48 with 48-token pages, 85 per sequence (4080
     tokens: the general kernel); fp8 the FP8 forward.  Prints one line; no timing."""
@@ -863,7 +864,7 @@ def run_profile(target, launches):
     s = torch.cuda.current_stream(dev)
     g = torch.Generator(device=dev).manual_seed(99)
     rnd = lambda *sh: torch.randn(*sh, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
-    if target in ("fwd", "dkdv", "dq", "fused", "pair"):
+    if target in ("fwd", "dkdv", "dq", "fused", "pair", "window"):
         q, k, v, dO = (rnd(B, H, N, D) for _ in range(4))
         o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
         lse = torch.empty(B, H, N, device=dev)
@@ -873,6 +874,7 @@ def run_profile(target, launches):
         wsf = torch.empty(fa.fa_bwd_fused_workspace_bytes(B, H, N, N, D), dtype=torch.uint8, device=dev)
         call = {
             "fwd": lambda: fa.fa_fwd(q, k, v, o, lse, B, H, N, N, D, SCALE, True, s),
+            "window": lambda: fa.fa_fwd_window(q, k, v, o, lse, B, H, N, N, D, SCALE, 256, s),
             "dkdv": lambda: fa.fa_bwd_dkdv(q, k, v, lse, delta, dO, dk, dv, B, H, N, N, D, SCALE, True, s),
             "dq": lambda: fa.fa_bwd_dq(q, k, v, lse, delta, dO, dq, B, H, N, N, D, SCALE, True, s),
             "fused": lambda: fa.fa_bwd_fused(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, D, SCALE, True, wsf,
