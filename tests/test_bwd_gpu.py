@@ -9,7 +9,7 @@ import torch
 
 from exact_tiled_attention_21_gb300 import synthetic as syn
 from oracle import naive
-from tests.parity import check_grad, f64
+from tests.parity import check_grad, check_out, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -318,3 +318,30 @@ def test_forward_backward_in_cuda_graph(cuda_lib):
     assert fa.fa_get_last_device_error()[0] == 0
     for a, b in zip(ref, (o, lse, dq, dk, dv)):
         assert torch.equal(a, b)
+
+
+def test_forward_backward_past_32_bit_offsets(cuda_lib):
+    """B=1, H=4096, N=4096, d=128, causal: each of Q, K, V, O, dO and the three
+    gradients holds 2^31 elements, so element offsets need more than 31 bits.
+    Inputs are drawn on the device; heads 0 and 4095 (the last rows of every
+    tensor) against the oracle, forward and backward."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    B, H, N, d = 1, 4096, 4096, 128
+    g = torch.Generator(device=dev).manual_seed(4096)
+    q, k, v, dO = (torch.empty(B, H, N, d, dtype=torch.bfloat16, device=dev).normal_(generator=g) for _ in range(4))
+    o, lse = fa.forward(q, k, v, causal=True)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, N, d), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, d ** -0.5, True, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error()[0] == 0
+    for h in (0, H - 1):
+        sl = slice(h, h + 1)
+        qh, kh, vh, dOh = (f64(t[:, sl].cpu()) for t in (q, k, v, dO))
+        o_ref, lse_ref = naive.forward(qh, kh, vh, d ** -0.5, True)
+        check_out(f64(o[:, sl].cpu()), f64(lse[:, sl].cpu()), o_ref, lse_ref, "O, LSE head %d" % h)
+        rq, rk, rv = naive.backward(qh, kh, vh, dOh, d ** -0.5, True)
+        check_grad(f64(dq[:, sl].cpu()), rq, "dQ head %d" % h)
+        check_grad(f64(dk[:, sl].cpu()), rk, "dK head %d" % h)
+        check_grad(f64(dv[:, sl].cpu()), rv, "dV head %d" % h)

@@ -88,3 +88,26 @@ def test_decode_without_lse(cuda_lib):
     o = cuda_lib.decode(q.to(dev), kc.to(dev), vc.to(dev), num_splits=4, want_lse=False)
     o_ref, _ = naive.decode(f64(q), f64(kc), f64(vc), 1 / math.sqrt(128))
     check_out(f64(o.cpu()), None, o_ref, None, "no lse")
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_decode_caches_past_32_bit_offsets(cuda_lib, d):
+    """H=64, Nk=128 and B=4096 (d=128, the tensor-core kernel) or B=8192 (d=64, the
+    16-byte-load kernel): each cache holds 2^32 elements, so element offsets need
+    64 bits.  The caches are drawn on the device; 64 (b, h) rows spread over the
+    whole range, the last one included, against the oracle."""
+    dev = torch.device("cuda", 0)
+    B, H, Nk = (4096 if d == 128 else 8192), 64, 128
+    g = torch.Generator(device=dev).manual_seed(2 ** 31 + d)
+    q = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+    kc = torch.empty(B, H, Nk, d, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+    vc = torch.empty(B, H, Nk, d, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+    o, lse = cuda_lib.decode(q, kc, vc, num_splits=0)
+    torch.cuda.synchronize()
+    idx = torch.linspace(0, B * H - 1, 64).round().long()
+    b, h = idx // H, idx % H
+    o_s, lse_s = o[b, h].cpu()[None], lse[b, h].cpu()[None]
+    q_s, k_s, v_s = q[b, h].cpu()[None], kc[b, h].cpu()[None], vc[b, h].cpu()[None]
+    del kc, vc
+    o_ref, lse_ref = naive.decode(f64(q_s), f64(k_s), f64(v_s), 1 / math.sqrt(d))
+    check_out(f64(o_s), f64(lse_s), o_ref, lse_ref, "2^32-element caches d%d" % d)
