@@ -178,3 +178,35 @@ def test_paged_decode_length_out_of_range_past_the_staged_lengths(cuda_lib):
     L_ok[2050] = table.shape[1] * 16  # the clamped length: the whole table row
     o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L_ok, 1 / math.sqrt(128))
     check_out(f64(o.cpu()), f64(lse.cpu()), o_ref, lse_ref, "clamped length")
+
+
+@pytest.mark.parametrize("P", [16, 48])
+def test_paged_decode_cache_past_32_bit_offsets(cuda_lib, P):
+    """B=64 sequences, Hq=32, Hkv=8, d=128, pages scattered in a random order over a
+    pool of 2^31 elements per cache, so page offsets need 64 bits (16-token pages
+    on the tensor-core kernel, 48-token pages on the general one).  Three sequences,
+    one of them short, against the oracle on their own pages."""
+    dev = torch.device("cuda", 0)
+    B, Hq, Hkv, d = 64, 32, 8, 128
+    max_pages = (1 << 31) // (Hkv * P * d * B) + 1
+    num_pages = B * max_pages
+    g = torch.Generator(device=dev).manual_seed(P)
+    q = torch.empty(B, Hq, d, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+    kp = torch.empty(num_pages, Hkv, P, d, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+    vp = torch.empty(num_pages, Hkv, P, d, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+    table = torch.randperm(num_pages, generator=torch.Generator().manual_seed(P)).to(torch.int32)
+    table = table.reshape(B, max_pages)
+    lens = torch.full((B,), max_pages * P, dtype=torch.int32)
+    lens[1] = 5
+    o, lse = cuda_lib.decode_paged(q, kp, vp, table.to(dev), lens.to(dev), num_splits=0)
+    torch.cuda.synchronize()
+    st, detail = cuda_lib.fa_get_last_device_error()
+    assert st == 0, detail
+    for b in (0, 1, B - 1):
+        n = int(lens[b])
+        pages = table[b, :-(-n // P)].long()
+        kb, vb = kp[pages.to(dev)].cpu(), vp[pages.to(dev)].cpu()
+        tb = np.arange(pages.numel(), dtype=np.int32)[None]
+        o_ref, lse_ref = naive.decode_paged(f64(q[b:b + 1].cpu()), f64(kb), f64(vb), tb,
+                                            np.array([n], dtype=np.int32), 1 / math.sqrt(d))
+        check_out(f64(o[b:b + 1].cpu()), f64(lse[b:b + 1].cpu()), o_ref, lse_ref, "P%d sequence %d" % (P, b))
