@@ -1134,7 +1134,7 @@ struct Fu {
     static constexpr int OFF_DQS = OFF_DS + 2 * DS_BYTES;  // dQ staging [64 queries][128 features] fp32
     static constexpr int OFF_VEC = OFF_DQS + BQ * D * 4;   // stage s: 64 lse2 at [128 s], 64 delta after
     static constexpr int OFF_BAR = OFF_VEC + NST * 2 * BQ * 4;
-    static constexpr int NBAR = 21;
+    static constexpr int NBAR = 22;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16;
     static constexpr int THREADS = 352;
@@ -1159,11 +1159,14 @@ bwd_fused_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const uint32_t B_KV = bar0, B_STF = bar0 + 8, B_STE = bar0 + 32, B_S = bar0 + 56, B_SF = bar0 + 64,
                    B_DP = bar0 + 72, B_DS = bar0 + 88, B_DSF = bar0 + 96, B_DQ = bar0 + 112, B_QF = bar0 + 120,
                    B_ACC = bar0 + 128, B_TD = bar0 + 136, B_TD2 = bar0 + 144, B_QSF = bar0 + 152,
-                   B_QSW = bar0 + 160;
-    // KV, STF[3] (producer lanes), STE[3] (both issuers), S, SF (compute threads), DP[2], DS
-    // (compute), DSF[2], DQ, QF (compute), ACC, TD, TD2, QSF (dQ staging free: thread 0),
-    // QSW (dQ staging written: compute threads)
-    const uint32_t counts[C::NBAR] = {1, 32, 32, 32, 2, 2, 2, 1, 256, 1, 1, 256, 1, 1, 1, 256, 1, 1, 1, 1, 256};
+                   B_QSW = bar0 + 160, B_DS1 = bar0 + 168;
+    // KV, STF[3] (producer lanes), STE[3] (both issuers), S, SF (compute threads), DP[2], DS[2]
+    // (compute: DS for even tiles, DS1 for odd ones), DSF[2], DQ, QF (compute), ACC, TD, TD2, QSF
+    // (dQ staging free: thread 0), QSW (dQ staging written: compute threads).  DS alternates:
+    // dP^T(i+1) is issued before dS(i) is waited for, so a warp can form dS(i+1) while another still
+    // forms dS(i), and one barrier would count both tiles' arrivals in one phase; tile i+2 needs
+    // dQ^T(i), hence every arrival for tile i, so two barriers never mix.
+    const uint32_t counts[C::NBAR] = {1, 32, 32, 32, 2, 2, 2, 1, 256, 1, 1, 256, 1, 1, 1, 256, 1, 1, 1, 1, 256, 256};
     uint32_t* tmem_slot = (uint32_t*)(smem + C::OFF_MISC);
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
     const WaitCtl ctl{p.err, p.timeout_ns, abort_flag};
@@ -1313,7 +1316,7 @@ bwd_fused_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             for (int ii = 0; ii < n && ok; ++ii) {
                 const int st = ii % C::NST, b = ii & 1;
                 if (ii + 1 < n && !(ok = issue_dp(ii + 1))) break;
-                if (!(ok = mbar_wait(B_DS, ii & 1, ctl, kSiteBwdDS))) break;
+                if (!(ok = mbar_wait((ii & 1) ? B_DS1 : B_DS, (ii >> 1) & 1, ctl, kSiteBwdDS))) break;
                 tc_fence_after();
                 const bool acc = ii > 0;
                 {   // dV += P^T dO: A = P^T (TMEM; k-step k = queries 16k.., warpgroup k / 2's
@@ -1473,7 +1476,7 @@ bwd_fused_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(B_DS);
+            mbar_arrive((ii & 1) ? B_DS1 : B_DS);
             if (ii > 0 && !(ok = read_dq(ii - 1))) break;
         }
         ok = __all_sync(0xffffffffu, ok);
