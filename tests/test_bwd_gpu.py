@@ -345,3 +345,43 @@ def test_forward_backward_past_32_bit_offsets(cuda_lib):
         check_grad(f64(dq[:, sl].cpu()), rq, "dQ head %d" % h)
         check_grad(f64(dk[:, sl].cpu()), rk, "dK head %d" % h)
         check_grad(f64(dv[:, sl].cpu()), rv, "dV head %d" % h)
+
+
+def _bits(t):
+    return t.view(torch.int16 if t.element_size() == 2 else torch.int32)
+
+
+@pytest.mark.parametrize("N", [1024, 2048])
+def test_repeated_runs_repeat_bits(cuda_lib, N):
+    """Many back-to-back calls at B=1, H=32, d=128, causal, each compared bit for bit
+    with the first: the forward (O, LSE), fa_bwd (dQ, dK, dV), fa_bwd_fused (dK, dV;
+    its dQ adds in a run-dependent order) and fa_bwd_dkdv_pair (dK, dV).  Every result
+    is a fixed sum in a fixed order, so a hand-off between warps that let a product
+    read a tile before all of it was written shows up as changed bits."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    B, H, d, reps = 1, 32, 128, 25
+    scale = syn.default_scale(d)
+    q, k, v, dO = (t.to(dev) for t in _inputs(31 + N, B, H, N, N, d))
+    o0, lse0 = fa.forward(q, k, v, scale=scale, causal=True)
+    ref_bwd = fa.backward(q, k, v, o0, lse0, dO, scale=scale, causal=True)
+    ref_fused = fa.backward(q, k, v, o0, lse0, dO, scale=scale, causal=True, fused=True)[1:]
+    delta = torch.empty(B, H, N, device=dev)
+    fa.fa_bwd_preprocess(o0, dO, delta, B, H, N, d)
+    ref_pair = (torch.empty_like(k), torch.empty_like(v))
+    fa.fa_bwd_dkdv_pair(q, k, v, lse0, delta, dO, *ref_pair, B, H, N, N, d, scale, True)
+    same = torch.ones((), dtype=torch.bool, device=dev)
+    for _ in range(reps):
+        o, lse = fa.forward(q, k, v, scale=scale, causal=True)
+        g = fa.backward(q, k, v, o0, lse0, dO, scale=scale, causal=True)
+        gf = fa.backward(q, k, v, o0, lse0, dO, scale=scale, causal=True, fused=True)[1:]
+        gp = (torch.empty_like(k), torch.empty_like(v))
+        fa.fa_bwd_dkdv_pair(q, k, v, lse0, delta, dO, *gp, B, H, N, N, d, scale, True)
+        for x, y in zip((o, lse) + tuple(g) + tuple(gf) + gp, (o0, lse0) + tuple(ref_bwd) + tuple(ref_fused) + ref_pair):
+            same &= (_bits(x) == _bits(y)).all()  # on the device: the calls stay back to back
+    torch.cuda.synchronize()
+    st, detail = fa.fa_get_last_device_error()
+    assert st == 0, detail
+    assert bool(same)
+    for x in (o0,) + tuple(ref_bwd):
+        assert torch.isfinite(x.float()).all()

@@ -111,3 +111,21 @@ def test_decode_caches_past_32_bit_offsets(cuda_lib, d):
     del kc, vc
     o_ref, lse_ref = naive.decode(f64(q_s), f64(k_s), f64(v_s), 1 / math.sqrt(d))
     check_out(f64(o_s), f64(lse_s), o_ref, lse_ref, "2^32-element caches d%d" % d)
+
+
+@pytest.mark.parametrize("Nk,d,splits", [(4096, 128, 16), (4000, 128, 0), (4096, 64, 0)])
+def test_decode_repeats_bits(cuda_lib, Nk, d, splits):
+    """B=32, H=32: 50 back-to-back calls give the first call's O and LSE bit for
+    bit (the splits' partials are combined in a fixed order; no atomics)."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    q, kc, vc = (t.to(dev) for t in _inputs(40 + Nk + d, 32, 32, Nk, d))
+    o0, lse0 = fa.decode(q, kc, vc, num_splits=splits)
+    same = torch.ones((), dtype=torch.bool, device=dev)
+    for _ in range(50):
+        o, lse = fa.decode(q, kc, vc, num_splits=splits)
+        same &= (o.view(torch.int16) == o0.view(torch.int16)).all()
+        same &= (lse.view(torch.int32) == lse0.view(torch.int32)).all()
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error()[0] == 0
+    assert bool(same)

@@ -210,3 +210,25 @@ def test_paged_decode_cache_past_32_bit_offsets(cuda_lib, P):
         o_ref, lse_ref = naive.decode_paged(f64(q[b:b + 1].cpu()), f64(kb), f64(vb), tb,
                                             np.array([n], dtype=np.int32), 1 / math.sqrt(d))
         check_out(f64(o[b:b + 1].cpu()), f64(lse[b:b + 1].cpu()), o_ref, lse_ref, "P%d sequence %d" % (P, b))
+
+
+@pytest.mark.parametrize("P,d", [(16, 128), (48, 128), (16, 64)])
+def test_paged_decode_repeats_bits(cuda_lib, P, d):
+    """B=32, Hq=32, Hkv=8, ragged lengths: 50 back-to-back calls give the first
+    call's O and LSE bit for bit."""
+    fa = cuda_lib
+    dev = torch.device("cuda", 0)
+    rng = np.random.default_rng(91 + P)
+    lens = [4080, 1] + list(rng.integers(1, 4081, size=30))
+    q, kp, vp, table, L = _case(92 + P + d, 32, 32, 8, P, lens, d)
+    q, kp, vp = q.to(dev), kp.to(dev), vp.to(dev)
+    table, L = torch.from_numpy(table).to(dev), torch.from_numpy(L).to(dev)
+    o0, lse0 = fa.decode_paged(q, kp, vp, table, L)
+    same = torch.ones((), dtype=torch.bool, device=dev)
+    for _ in range(50):
+        o, lse = fa.decode_paged(q, kp, vp, table, L)
+        same &= (o.view(torch.int16) == o0.view(torch.int16)).all()
+        same &= (lse.view(torch.int32) == lse0.view(torch.int32)).all()
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error()[0] == 0
+    assert bool(same)
