@@ -430,20 +430,50 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
     return out
 
 
+def attention_bytes(rows, d, backward):
+    """Algorithmic HBM bytes of one call over ``rows`` (b, h, position) rows with
+    Nq = Nk: the forward reads Q, K, V and writes O (bf16) and the LSE (fp32); the
+    backward reads Q, K, V, O, dO, writes dQ, dK, dV and reads the LSE and writes
+    and reads D (fp32)."""
+    return rows * (d * 2 * (8 if backward else 4) + 4 * (3 if backward else 1))
+
+
+def roofline_of(tflops, ms, nbytes, pk):
+    """(bound, fraction): the measured time against the larger of the tensor-peak
+    time of the call's FLOPs and the HBM time of its algorithmic bytes."""
+    t_tensor = tflops * ms / pk["bf16"]
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9) * 1e3
+    return ("tensor" if t_tensor >= t_hbm else "hbm"), max(t_tensor, t_hbm) / ms
+
+
+def add_roofline(e, rows, d, pk, keys=("fwd", "bwd", "bwd_fused")):
+    for k in keys:
+        if k + "_ms" in e:
+            e[k + "_bound"], e[k + "_roofline_frac"] = roofline_of(
+                e[k + "_tflops"], e[k + "_ms"], attention_bytes(rows, d, k != "fwd"), pk)
+
+
 def finish_sweep(sw, pk, sampler):
-    """Fractions of the measured peaks and the SM clocks sampled in each window."""
+    """Fractions of the measured peaks and the SM clocks sampled in each window.
+    ``*_frac`` divides by the tensor peak; ``*_roofline_frac`` divides by the
+    roofline of the call (tensor or HBM, whichever takes longer, named in ``*_bound``)."""
     for e in sw["fwd_bwd_causal_B1_H32_d128"]:
         e["fwd_frac"] = e["fwd_tflops"] / pk["bf16"]
         e["bwd_frac"] = e["bwd_tflops"] / pk["bf16"]
         e["bwd_fused_frac"] = e["bwd_fused_tflops"] / pk["bf16"]
+        add_roofline(e, H * e["N"], D, pk)
     for e in sw["fwd_B2_H32_N4096_d128"]:
         e["fwd_frac"] = e["fwd_tflops"] / pk["bf16"]
-    for key in ("window_B1_H32_N8192_d128_W256", "varlen_causal_B4_H32_N8192_d128"):
+        add_roofline(e, 2 * H * 4096, D, pk)
+    for key, rows in (("window_B1_H32_N8192_d128_W256", H * 8192),
+                      ("varlen_causal_B4_H32_N8192_d128", H * sum(sw["varlen_causal_B4_H32_N8192_d128"]["lens"]))):
         e = sw[key]
         e["fwd_frac"] = e["fwd_tflops"] / pk["bf16"]
         e["bwd_frac"] = e["bwd_tflops"] / pk["bf16"]
+        add_roofline(e, rows, D, pk)
     lo = sw["fwd_long_causal_B1_H32_N131072_d128"]
     lo["fwd_frac"] = lo["fwd_tflops"] / pk["bf16"]
+    add_roofline(lo, H * 131072, D, pk)
     for e in sw["decode_B32_H32"]:
         e["frac_of_hbm"] = e["gbs"] / pk["hbm_gbs"]
     win = sw.pop("_windows")

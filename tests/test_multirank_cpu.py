@@ -59,3 +59,22 @@ def test_reference_arm_prints_one_json_line():
     assert rec["impl"] == "reference" and rec["unit"] == "TFLOP/s" and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_roofline_bound_of_sweep_entries():
+    """The roofline side of a call: causal N=8192 forward is tensor-bound, a
+    256-key window and causal N=1024 are HBM-bound (B=1, H=32, d=128)."""
+    import bench
+    pk = {"bf16": 1927.9, "hbm_gbs": 6784.5}
+    rows = 32 * 8192
+    assert bench.attention_bytes(rows, 128, False) == rows * (4 * 256 + 4)
+    assert bench.attention_bytes(rows, 128, True) == rows * (8 * 256 + 12)
+    full = 4.0 * 32 * 8192 * 8192 * 128 / 2
+    bound, frac = bench.roofline_of(full / 0.4e-3 / 1e12, 0.4, bench.attention_bytes(rows, 128, False), pk)
+    assert bound == "tensor" and abs(frac - full / 1927.9e12 / 0.4e-3) < 1e-9
+    win = 4.0 * 32 * (256 * 8192 - 256 * 255 / 2) * 128
+    nbytes = bench.attention_bytes(rows, 128, False)
+    bound, frac = bench.roofline_of(win / 0.12e-3 / 1e12, 0.12, nbytes, pk)
+    assert bound == "hbm" and abs(frac - nbytes / 6784.5e9 / 0.12e-3) < 1e-9
+    small = 4.0 * 32 * 1024 * 1024 * 128 / 2
+    assert bench.roofline_of(small / 0.023e-3 / 1e12, 0.023, bench.attention_bytes(32 * 1024, 128, False), pk)[0] == "hbm"
