@@ -878,7 +878,8 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------------------ one kernel for a profiler
-PROFILE_TARGETS = ("fwd", "dkdv", "dq", "fused", "pair", "window", "decode", "decode64", "paged", "paged48", "fp8")
+PROFILE_TARGETS = ("fwd", "dkdv", "dq", "fused", "pair", "window", "decode", "decode64", "paged", "paged48",
+                   "paged20", "fp8")
 
 
 def run_profile(target, launches):
@@ -887,8 +888,10 @@ def run_profile(target, launches):
     fwd / dkdv / dq / fused / pair at B=1, H=32, N=8192, d=128 causal; window the
     forward under a causal 256-key window at the same size; decode at
     B=32, H=32, Nk=4096 (d=128 or d=64); paged at B=32, Hq=32, Hkv=8, page 16 (the
-    tensor-core kernel) and paged48 with 48-token pages, 85 per sequence (4080
-    tokens: the general kernel); fp8 the FP8 forward.  Prints one line; no timing."""
+    tensor-core kernel), paged48 with 48-token pages, 85 per sequence (4080 tokens:
+    the tensor-core kernel in 16-row boxes) and paged20 with 20-token pages, 204 per
+    sequence (4080 tokens: the general kernel); fp8 the FP8 forward.  Prints one
+    line; no timing."""
     import torch
     import exact_tiled_attention_21_gb300 as fa
     dev = torch.device("cuda", 0)
@@ -922,8 +925,8 @@ def run_profile(target, launches):
                          device=dev)
         call = lambda: fa.fa_decode(qd, kc, vc, od, lsed, DEC_B, DEC_H, DEC_NK, d, 1 / math.sqrt(d), DEC_SPLITS, ws,
                                     ws.numel(), s)
-    elif target in ("paged", "paged48"):
-        hkv, page = (8, 16) if target == "paged" else (8, 48)
+    elif target in ("paged", "paged48", "paged20"):
+        hkv, page = 8, {"paged": 16, "paged48": 48, "paged20": 20}[target]
         npages = DEC_B * (DEC_NK // page)
         kp, vp = rnd(npages, hkv, page, D), rnd(npages, hkv, page, D)
         qd = rnd(DEC_B, DEC_H, D)

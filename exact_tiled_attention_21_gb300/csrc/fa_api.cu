@@ -90,12 +90,13 @@ int make_map_nd(CUtensorMap* m, const void* base, int rank, const cuuint64_t* di
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// Page sizes the tensor-core paged decode takes: whole 8-row swizzle atoms
-// per page, and pages that tile a 128-key stage (or stages that tile a page).
-bool paged_mma_ok(int d, int page) {
-    if ((d != 64 && d != 128) || page % 8 != 0) return false;
-    return page <= 128 ? (128 % page == 0) : (page % 128 == 0);
-}
+// Page sizes the tensor-core paged decode takes: whole 8-row swizzle atoms per page.  It loads
+// a page in boxes of gcd(page, 128) rows (at least 8), which tile both the page and a 128-key
+// stage.
+bool paged_mma_ok(int d, int page) { return (d == 64 || d == 128) && page % 8 == 0; }
+
+// Rows of one TMA box of a page: gcd(page, 128) for a multiple of 8.
+int page_box_rows(int page) { return std::min(page & -page, 128); }
 
 // Shared shape checks.  Sizes must keep every element index below 2^31 per
 // tensor row block and the total within 64-bit byte offsets.
@@ -513,12 +514,12 @@ int paged_mma_maps(PagedDecodeLaunch& a) {
     const cuuint64_t kd[4] = {(cuuint64_t)d, (cuuint64_t)page_size, (cuuint64_t)a.Hkv, (cuuint64_t)a.num_pages};
     const cuuint64_t ks[3] = {(cuuint64_t)d * 2, (cuuint64_t)page_size * d * 2,
                               (cuuint64_t)a.Hkv * page_size * d * 2};
-    const cuuint32_t kb[4] = {64, (cuuint32_t)std::min(page_size, 128), 1, 1};
+    const cuuint32_t kb[4] = {64, (cuuint32_t)page_box_rows(page_size), 1, 1};
     // V: the feature dimension as (64, half) so one box holds a page's rows of both halves
     const cuuint64_t vd[5] = {64, (cuuint64_t)page_size, 2, (cuuint64_t)a.Hkv, (cuuint64_t)a.num_pages};
     const cuuint64_t vs[4] = {(cuuint64_t)d * 2, 128, (cuuint64_t)page_size * d * 2,
                               (cuuint64_t)a.Hkv * page_size * d * 2};
-    const cuuint32_t vb[5] = {64, (cuuint32_t)std::min(page_size, 128), 2, 1, 1};
+    const cuuint32_t vb[5] = {64, (cuuint32_t)page_box_rows(page_size), 2, 1, 1};
     // d = 64: a row is one 128-byte swizzle row, so V takes the same 4-D form as K
     if (make_map_nd(&a.map_q, a.q, 3, qd, qs, qb) || make_map_nd(&a.map_k, a.kp, 4, kd, ks, kb) ||
         (d == 128 ? make_map_nd(&a.map_v, a.vp, 5, vd, vs, vb) : make_map_nd(&a.map_v, a.vp, 4, kd, ks, kb)))

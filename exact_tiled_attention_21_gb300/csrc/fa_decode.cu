@@ -233,8 +233,7 @@ cudaError_t launch_decode_d(const DecodeLaunch& a, cudaStream_t s) {
 
 // ------------------------------------------------------------------ paged, grouped-query decode
 // The general path (page sizes the tensor-core kernel of fa_decode_mma.cu
-// does not take: not a multiple of 8, or neither dividing 128 nor a multiple
-// of 128).  One CTA per (b,
+// does not take: not a multiple of 8).  One CTA per (b,
 // kv head, split, group of G <= 4 query heads).  The split's keys are the
 // logical tokens [split * chunk, min(len, (split + 1) * chunk)) of the
 // sequence, chunk = ceil(len / splits); each 128-key piece's page rows are

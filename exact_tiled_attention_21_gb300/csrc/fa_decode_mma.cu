@@ -15,10 +15,12 @@
 //   warp 4      TMA producer of K: the group's 16 q rows (rows past the group
 //               are other heads or zero fill; their columns are never used),
 //               then per stage the K rows of the pages the stage covers (block
-//               table read 32 entries at a time, two work items ahead), two
-//               boxes per page (one per 64-feature half: the score product
-//               needs all 128 keys of a half at one row stride).
-//   warp 6      TMA producer of V: one box per page holding both halves
+//               table read 32 entries at a time, two work items ahead), in
+//               boxes of R = gcd(page, 128) rows, so a box never crosses a
+//               page (a page of 48 tokens is three boxes of 16), two per box
+//               position (one per 64-feature half: the score product needs
+//               all 128 keys of a half at one row stride).
+//   warp 6      TMA producer of V: one box per R rows holding both halves
 //               (the value product steps through the keys 16 at a time and
 //               takes each step's address on its own).  A page index outside
 //               the pool is loaded from an out-of-range coordinate, which the
@@ -119,6 +121,11 @@ __device__ __forceinline__ Item item_at(const MmaParams& p, int w, int len) {
     it.k1 = (int)min(k0 + chunk, (unsigned)len);
     return it;
 }
+
+// Rows per TMA box of a page: gcd(page, 128), i.e. the lowest set bit of the page size capped at
+// 128 (page sizes are multiples of 8).  Stages start at multiples of 128 keys, so a box of R rows
+// at key key0 + i R starts at a multiple of R within one page and ends inside it.
+__device__ __forceinline__ int box_rows(int page) { return min(page & -page, 128); }
 
 // A length outside [1, max_pages * page] is out of range: clamped, never
 // dereferenced past the table (recorded when the lengths are staged).
@@ -284,20 +291,22 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 ++qn;
             }
             const int* trow = p.table ? p.table + (size_t)it.b * p.max_pages : nullptr;
-            const int rows = min(p.page, 128);
+            const int rows = box_rows(p.page);
             int tbl_base = it.k0 / p.page;  // tbl (lane i) = entry of page tbl_base + i
             for (int key0 = it.k0; key0 < it.k1; key0 += Dm::BK, ++g) {
                 const int nk = min(Dm::BK, it.k1 - key0);
-                const int pfirst = key0 / p.page;
-                const int npg = p.page <= 128 ? (nk + p.page - 1) / p.page : 1;
-                const int prow0 = key0 - pfirst * p.page;  // 0 unless pages are longer than a stage
-                if (pfirst + npg > tbl_base + 32) {
+                const int nbox = (nk + rows - 1) / rows;  // lane i < nbox: rows key0 + i R ..
+                const int pfirst = key0 / p.page, plast = (key0 + (nbox - 1) * rows) / p.page;
+                const int key = key0 + lane * rows;
+                const int pidx = key / p.page;       // this lane's page (lanes < nbox)
+                const int prow = key - pidx * p.page;  // its first row there: a multiple of R
+                if (plast >= tbl_base + 32) {  // at most 17 pages per stage (R >= 8)
                     tbl_base = pfirst;
                     const int pi = pfirst + lane;
                     tbl = pi < p.max_pages ? (trow ? __ldg(trow + pi) : it.b * p.max_pages + pi) : 0;
                 }
-                int pg = __shfl_sync(0xffffffffu, tbl, (pfirst - tbl_base + lane) & 31);
-                if (lane < npg && (pg < 0 || pg >= p.num_pages)) {
+                int pg = __shfl_sync(0xffffffffu, tbl, (pidx - tbl_base) & 31);
+                if (lane < nbox && (pg < 0 || pg >= p.num_pages)) {
                     if (atomicCAS(&p.err->code, 0, kErrInvalid) == 0) {
                         p.err->site = kSitePagedTable;
                         p.err->block = blockIdx.x;
@@ -307,21 +316,21 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 }
                 if (lane == 0) {
                     ok = mbar_wait(bar_empty(kv, g), ring_par(g) ^ 1, ctl, kSitePagedKv);
-                    if (ok) mbar_arrive_expect_tx(bar_full(kv, g), (uint32_t)(npg * rows * D * 2));
+                    if (ok) mbar_arrive_expect_tx(bar_full(kv, g), (uint32_t)(nbox * rows * D * 2));
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                if (lane < npg) {
+                if (lane < nbox) {
                     if (!kv) {
                         const uint32_t dst = s_base + Dm::OFF_K + (g % Dm::NSLOT) * Dm::SLOT + (uint32_t)(lane * rows * 128);
                         for (int c = 0; c < D / 64; ++c)
-                            tma_load_4d(dst + c * Dm::CHUNK, &map_k, bar_full(0, g), c * 64, prow0, it.kvh, pg, pol_kv);
+                            tma_load_4d(dst + c * Dm::CHUNK, &map_k, bar_full(0, g), c * 64, prow, it.kvh, pg, pol_kv);
                     } else if constexpr (D == 128) {
                         const uint32_t dst = s_base + Dm::OFF_V + (g % Dm::NSLOT) * Dm::SLOT + (uint32_t)(lane * rows * 256);
-                        tma_load_5d(dst, &map_v, bar_full(1, g), 0, prow0, 0, it.kvh, pg, pol_kv);
-                    } else {  // d = 64: a page's rows are whole 128-byte rows, back to back
+                        tma_load_5d(dst, &map_v, bar_full(1, g), 0, prow, 0, it.kvh, pg, pol_kv);
+                    } else {  // d = 64: a box's rows are whole 128-byte rows, back to back
                         const uint32_t dst = s_base + Dm::OFF_V + (g % Dm::NSLOT) * Dm::SLOT + (uint32_t)(lane * rows * 128);
-                        tma_load_4d(dst, &map_v, bar_full(1, g), 0, prow0, it.kvh, pg, pol_kv);
+                        tma_load_4d(dst, &map_v, bar_full(1, g), 0, prow, it.kvh, pg, pol_kv);
                     }
                 }
                 issued |= 1u << (g % Dm::NSLOT);
@@ -341,9 +350,9 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
         // product PV_g are issued as soon as their inputs are ready, S at most
         // one stage ahead of PV (two S^T buffers), each in stage order.
         if (lane == 0 && !*abort_flag) {
-            // V^T operand: each 16-key step starts at its own address (pages of
-            // R = min(page, 128) rows, [half][R rows][128 B] each, back to back)
-            const int R = min(p.page, 128);
+            // V^T operand: each 16-key step starts at its own address (boxes of
+            // R = gcd(page, 128) rows, [half][R rows][128 B] each, back to back)
+            const int R = box_rows(p.page);
             const uint32_t v_lbo = (uint32_t)R * 128, v_sbo = R == 8 ? 2048u : 1024u;
             uint32_t v_off[Dm::BK / 16];
 #pragma unroll
@@ -450,7 +459,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
         float* red_l = red_m + 2 * 4 * 16;                             // [4][16]
         const float c = p.scale_log2;
         uint32_t gs = 0, items = 0;
-        const int R = min(p.page, 128);
+        const int R = box_rows(p.page);
         bool failed = false;
         for (int w = first; w < p.nitems && !failed; w += grid) {
             const Item it = item_of<D, NH>(p, w, s_lens);

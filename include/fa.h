@@ -284,8 +284,8 @@ size_t fa_decode_paged_workspace_bytes(int B, int Hq, int d, int num_splits);
  * possible sequence max_pages * page_size and the SM count; at most 16).
  * Each sequence is cut into num_splits (1..256) contiguous chunks of
  * ceil(seq_lens[b] / num_splits) tokens (rounded up to whole 128-token stages
- * on the tensor-core path: page_size a multiple of 8 that divides 128 or is
- * a multiple of 128), merged as in fa_decode.  Every K/V
+ * on the tensor-core path: page_size a multiple of 8), merged as in
+ * fa_decode.  Every K/V
  * row is read once per group of up to 16 query heads on that path (4 on the
  * general one).  Tokens past seq_lens[b] in a page are never used, whatever
  * they hold.  Host checks: Hq % Hkv

@@ -50,16 +50,25 @@ CASES = [
     (2, 8, 2, 256, [1000, 300], 128, 2),        # pages longer than a stage
     (1, 32, 1, 16, [517], 128, 4),              # multi-query, 32 heads: two groups of 16
     (1, 40, 2, 32, [333], 128, 2),              # group of 20: 16 + 4 heads
-    (1, 8, 2, 48, [500], 128, 3),               # 48-token pages (not a divisor of 128)
+    (1, 8, 2, 48, [500], 128, 3),               # 48-token pages (not a divisor of 128): boxes of 16 rows
+    (2, 8, 2, 40, [1000, 41], 128, 3),          # 40-token pages: boxes of 8 rows, 16 per stage
+    (2, 16, 4, 24, [777, 24], 128, 0),          # 24-token pages, automatic split count
+    (2, 8, 2, 80, [1000, 79], 128, 4),          # 80-token pages: boxes of 16 rows
+    (2, 8, 2, 96, [1100, 97], 64, 3),           # d = 64, 96-token pages: boxes of 32 rows
+    (2, 8, 2, 136, [1000, 136], 128, 2),        # pages longer than a stage, boxes of 8 rows
+    (2, 8, 2, 200, [1500, 199], 64, 2),         # d = 64, pages longer than a stage, boxes of 8 rows
     (1, 8, 2, 16, [20000], 128, 1),             # one split: 157 stages through the ring
     (32, 32, 8, 16, [4096] * 30 + [1, 777], 128, 0),  # automatic split count (tensor-core path)
-    (3, 8, 2, 48, [1000, 3, 480], 128, 0),      # automatic split count (general path)
+    (3, 8, 2, 48, [1000, 3, 480], 128, 0),      # automatic split count, 48-token pages
+    (3, 8, 2, 20, [1000, 3, 480], 128, 0),      # automatic split count (general path: 20-token pages)
+    (2, 8, 2, 12, [500, 77], 128, 3),           # general path, group of 4
     (2, 32, 2, 8, [1000, 129], 64, 5),          # d = 64 on the tensor cores: 8-token pages, group of 16
     (2, 8, 2, 256, [1000, 300], 64, 2),         # d = 64, pages longer than a stage
     (1, 40, 2, 32, [333], 64, 2),               # d = 64, group of 20
     (1, 8, 2, 16, [20000], 64, 1),              # d = 64, 157 stages through the ring
     (32, 32, 8, 16, [4096] * 30 + [1, 777], 64, 0),  # d = 64, automatic split count
-    (2, 8, 2, 48, [500, 77], 64, 3),            # d = 64, general path (48-token pages)
+    (2, 8, 2, 48, [500, 77], 64, 3),            # d = 64, 48-token pages
+    (2, 8, 2, 20, [500, 77], 64, 3),            # d = 64, general path (20-token pages)
 ]
 
 
@@ -108,7 +117,7 @@ def test_paged_decode_rejects_bad_page_index_on_device(cuda_lib):
     assert cuda_lib.fa_get_last_device_error()[0] == 0
 
 
-@pytest.mark.parametrize("P,d", [(16, 128), (48, 128), (256, 128), (16, 64), (256, 64)])
+@pytest.mark.parametrize("P,d", [(16, 128), (48, 128), (256, 128), (20, 128), (16, 64), (48, 64), (256, 64)])
 def test_paged_decode_ignores_unused_slots(cuda_lib, P, d):
     """Tokens past seq_lens[b] in the last page, and pages no table names,
     may hold anything (NaN here): the result depends only on the tokens in
@@ -180,11 +189,11 @@ def test_paged_decode_length_out_of_range_past_the_staged_lengths(cuda_lib):
     check_out(f64(o.cpu()), f64(lse.cpu()), o_ref, lse_ref, "clamped length")
 
 
-@pytest.mark.parametrize("P", [16, 48])
+@pytest.mark.parametrize("P", [16, 48, 20])
 def test_paged_decode_cache_past_32_bit_offsets(cuda_lib, P):
     """B=64 sequences, Hq=32, Hkv=8, d=128, pages scattered in a random order over a
-    pool of 2^31 elements per cache, so page offsets need 64 bits (16-token pages
-    on the tensor-core kernel, 48-token pages on the general one).  Three sequences,
+    pool of 2^31 elements per cache, so page offsets need 64 bits (16- and 48-token
+    pages on the tensor-core kernel, 20-token pages on the general one).  Three sequences,
     one of them short, against the oracle on their own pages."""
     dev = torch.device("cuda", 0)
     B, Hq, Hkv, d = 64, 32, 8, 128
@@ -212,7 +221,7 @@ def test_paged_decode_cache_past_32_bit_offsets(cuda_lib, P):
         check_out(f64(o[b:b + 1].cpu()), f64(lse[b:b + 1].cpu()), o_ref, lse_ref, "P%d sequence %d" % (P, b))
 
 
-@pytest.mark.parametrize("P,d", [(16, 128), (48, 128), (16, 64)])
+@pytest.mark.parametrize("P,d", [(16, 128), (48, 128), (20, 128), (16, 64)])
 def test_paged_decode_repeats_bits(cuda_lib, P, d):
     """B=32, Hq=32, Hkv=8, ragged lengths: 50 back-to-back calls give the first
     call's O and LSE bit for bit."""
