@@ -258,10 +258,13 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
     padded to 8192, causal), their FLOPs counted over the pairs the mask keeps;
     the long causal forward at N=131072 with its peak device memory; decode at
     B=32, H=32 for d=128 with Nk=4096 and Nk=4000 and for d=64, with 16 splits
-    and with the automatic count.  Each entry is
+    and with the automatic count; paged decode at B=32, Hq=32, Hkv=8 with 48-,
+    80-, 40- and 20-token pages (d=128) and 48-token pages (d=64).  Each entry is
     the median over calls bracketed by CUDA events on the launching stream.  L2
     is flushed (a 256 MiB write) before every call whose inputs would otherwise
-    stay in it; decode caches (>= 1 GiB) are larger than L2.  Decode runs first
+    stay in it; decode caches (>= 1 GiB) are larger than L2, and the paged
+    caches (0.13-0.27 GiB per call, pages in a random order) come back in under
+    one L2's worth of other traffic, so their figures may include some L2 hits.  Decode runs first
     and the long forward last, so the seconds-long full load of the latter
     cannot pull the clocks of the others down."""
     import torch
@@ -284,6 +287,7 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
     out = {"fwd_bwd_causal_B1_H32_d128": [], "fwd_B2_H32_N4096_d128": [], "decode_B32_H32": [],
+           "decode_paged_B32_Hq32": [],
            "timing": "median of per-call CUDA-event times on the launching stream; L2 flushed before each "
                      "fwd/bwd call (256 MiB write, outside the events)",
            "bwd_modes": "bwd: fa_bwd (dK/dV pass + dQ pass, deterministic); bwd_fused: fa_bwd_fused (one pass, "
@@ -310,6 +314,30 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
                                           "gbs": byt / (ms * 1e-3) / 1e9})
             del ws
         del q, kc, vc, o, lse
+    # paged decode at page sizes beside the headline's 16 tokens: 48 and 80 (the tensor-core kernel in
+    # 16-row boxes), 40 (8-row boxes) and 20 (not a multiple of 8: the CUDA-core kernel); 4080 tokens
+    # (or the nearest whole number of pages below 4096) per sequence, pages in a random order,
+    # automatic splits
+    for hkv, page, d in ((8, 48, 128), (8, 80, 128), (8, 40, 128), (8, 20, 128), (8, 48, 64)):
+        mp = DEC_NK // page
+        npages = DEC_B * mp
+        kp, vp = rnd(npages, hkv, page, d), rnd(npages, hkv, page, d)
+        q = rnd(DEC_B, DEC_H, d)
+        table = torch.randperm(npages, generator=torch.Generator().manual_seed(page)).to(torch.int32)
+        table = table.reshape(DEC_B, mp).to(dev)
+        lens = torch.full((DEC_B,), mp * page, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(DEC_B, DEC_H, device=dev, dtype=torch.float32)
+        ws = torch.empty(fa.fa_decode_paged_workspace_bytes(DEC_B, DEC_H, d, 0), dtype=torch.uint8, device=dev)
+        call = lambda: fa.fa_decode_paged(q, kp, vp, table, lens, o, lse, DEC_B, DEC_H, hkv, page, mp, npages, d,
+                                          1.0 / math.sqrt(d), 0, ws, ws.numel(), stream)
+        for _ in range(3):
+            call()
+        ms = timed(call, 20, False)
+        byt = 2.0 * DEC_B * hkv * mp * page * d * 2
+        out["decode_paged_B32_Hq32"].append({"Hkv": hkv, "page": page, "d": d, "tokens": mp * page, "ms": ms,
+                                             "gbs": byt / (ms * 1e-3) / 1e9})
+        del kp, vp, q, table, lens, o, lse, ws
     out["_windows"]["decode"] = (t0, time.time())
     t0 = time.time()
     for n in SWEEP_N:
@@ -474,7 +502,7 @@ def finish_sweep(sw, pk, sampler):
     lo = sw["fwd_long_causal_B1_H32_N131072_d128"]
     lo["fwd_frac"] = lo["fwd_tflops"] / pk["bf16"]
     add_roofline(lo, H * 131072, D, pk)
-    for e in sw["decode_B32_H32"]:
+    for e in sw["decode_B32_H32"] + sw["decode_paged_B32_Hq32"]:
         e["frac_of_hbm"] = e["gbs"] / pk["hbm_gbs"]
     win = sw.pop("_windows")
     sw["peak_source"] = ("%s: bf16_tflops %.1f (burst) for TFLOP/s, hbm_gbs %.1f for GB/s"
