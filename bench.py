@@ -262,11 +262,10 @@ def run_sweep(fa, dev, stream, g, barrier, sampler):
     80-, 40- and 20-token pages (d=128) and 48-token pages (d=64).  Each entry is
     the median over calls bracketed by CUDA events on the launching stream.  L2
     is flushed (a 256 MiB write) before every call whose inputs would otherwise
-    stay in it; decode caches (>= 1 GiB) are larger than L2, and the paged
-    caches (0.13-0.27 GiB per call, pages in a random order) come back in under
-    one L2's worth of other traffic, so their figures may include some L2 hits.  Decode runs first
-    and the long forward last, so the seconds-long full load of the latter
-    cannot pull the clocks of the others down."""
+    stay in it; decode caches (>= 1 GiB) and paged caches (0.27-0.53 GB of K
+    and V per call) are larger than L2.  Decode runs first and the long forward
+    last, so the seconds-long full load of the latter cannot pull the clocks of
+    the others down."""
     import torch
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
