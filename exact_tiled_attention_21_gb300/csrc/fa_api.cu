@@ -520,8 +520,12 @@ int paged_mma_maps(PagedDecodeLaunch& a) {
     const cuuint64_t vs[4] = {(cuuint64_t)d * 2, 128, (cuuint64_t)page_size * d * 2,
                               (cuuint64_t)a.Hkv * page_size * d * 2};
     const cuuint32_t vb[5] = {64, (cuuint32_t)page_box_rows(page_size), 2, 1, 1};
-    // d = 64: a row is one 128-byte swizzle row, so V takes the same 4-D form as K
-    if (make_map_nd(&a.map_q, a.q, 3, qd, qs, qb) || make_map_nd(&a.map_k, a.kp, 4, kd, ks, kb) ||
+    // d = 64: a row is one 128-byte swizzle row, so V takes the same 4-D form as K.  d = 128 with
+    // 8-row boxes: K takes V's 5-D form too (one copy per box for both feature halves; the kernel
+    // addresses the halves 1 KB apart and the 8-row groups 2 KB apart)
+    const bool k5 = d == 128 && page_box_rows(page_size) == 8;
+    if (make_map_nd(&a.map_q, a.q, 3, qd, qs, qb) ||
+        (k5 ? make_map_nd(&a.map_k, a.kp, 5, vd, vs, vb) : make_map_nd(&a.map_k, a.kp, 4, kd, ks, kb)) ||
         (d == 128 ? make_map_nd(&a.map_v, a.vp, 5, vd, vs, vb) : make_map_nd(&a.map_v, a.vp, 4, kd, ks, kb)))
         return FA_ERR_CUDA;
     return FA_OK;

@@ -321,7 +321,12 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 if (lane < nbox) {
-                    if (!kv) {
+                    if (!kv && D == 128 && rows == 8) {
+                        // 8-row boxes: both feature halves in one box, [half][8 rows][128 B] (the score
+                        // product then steps 2 KB per 8 keys and 1 KB to the second half)
+                        const uint32_t dst = s_base + Dm::OFF_K + (g % Dm::NSLOT) * Dm::SLOT + (uint32_t)(lane * rows * 256);
+                        tma_load_5d(dst, &map_k, bar_full(0, g), 0, prow, 0, it.kvh, pg, pol_kv);
+                    } else if (!kv) {
                         const uint32_t dst = s_base + Dm::OFF_K + (g % Dm::NSLOT) * Dm::SLOT + (uint32_t)(lane * rows * 128);
                         for (int c = 0; c < D / 64; ++c)
                             tma_load_4d(dst + c * Dm::CHUNK, &map_k, bar_full(0, g), c * 64, prow, it.kvh, pg, pol_kv);
@@ -354,6 +359,9 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             // R = gcd(page, 128) rows, [half][R rows][128 B] each, back to back)
             const int R = box_rows(p.page);
             const uint32_t v_lbo = (uint32_t)R * 128, v_sbo = R == 8 ? 2048u : 1024u;
+            // K operand: [half][128 keys][128 B], or at d = 128 with 8-row boxes [box][half][8 rows][128 B]
+            const bool k_boxed = D == 128 && R == 8;
+            const uint32_t k_half = k_boxed ? 1024u : (uint32_t)Dm::CHUNK, k_sbo = k_boxed ? 2048u : 1024u;
             uint32_t v_off[Dm::BK / 16];
 #pragma unroll
             for (int k = 0; k < Dm::BK / 16; ++k) v_off[k] = (uint32_t)((16 * k) / R * (R * 256) + (16 * k) % R * 128);
@@ -390,7 +398,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
 #pragma unroll
                         for (int k = 0; k < Dm::D / 16; ++k)
                             mma_ss(tmem + Dm::COL_S + (cs.g & 1) * Dm::NG,
-                                   sdesc_sw128(sK + (k >> 2) * Dm::CHUNK + (k & 3) * 32, 16, 1024),
+                                   sdesc_sw128(sK + (k >> 2) * k_half + (k & 3) * 32, 16, k_sbo),
                                    sdesc_sw128(sQ + (k >> 2) * Dm::QCHUNK + (k & 3) * 32, 16, 1024), Dm::IDESC_S,
                                    k > 0);
                         mma_commit(BAR_SF + 8 * (cs.g & 1));
