@@ -19,7 +19,8 @@
 //               boxes of R = gcd(page, 128) rows, so a box never crosses a
 //               page (a page of 48 tokens is three boxes of 16), two per box
 //               position (one per 64-feature half: the score product needs
-//               all 128 keys of a half at one row stride).
+//               all 128 keys of a half at one row stride), or one holding
+//               both halves when d = 128 and the boxes have 8 rows.
 //   warp 6      TMA producer of V: one box per R rows holding both halves
 //               (the value product steps through the keys 16 at a time and
 //               takes each step's address on its own).  A page index outside
@@ -297,7 +298,7 @@ decode_paged_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 const int nk = min(Dm::BK, it.k1 - key0);
                 const int nbox = (nk + rows - 1) / rows;  // lane i < nbox: rows key0 + i R ..
                 const int pfirst = key0 / p.page, plast = (key0 + (nbox - 1) * rows) / p.page;
-                const int key = key0 + lane * rows;
+                const int key = key0 + min(lane, nbox - 1) * rows;  // below k1: no overflow
                 const int pidx = key / p.page;       // this lane's page (lanes < nbox)
                 const int prow = key - pidx * p.page;  // its first row there: a multiple of R
                 if (plast >= tbl_base + 32) {  // at most 17 pages per stage (R >= 8)
