@@ -56,6 +56,8 @@ CASES = [
     (2, 8, 2, 80, [1000, 79], 128, 4),          # 80-token pages: boxes of 16 rows
     (2, 8, 2, 96, [1100, 97], 64, 3),           # d = 64, 96-token pages: boxes of 32 rows
     (2, 8, 2, 136, [1000, 136], 128, 2),        # pages longer than a stage, boxes of 8 rows
+    (2, 8, 2, 160, [1000, 161], 128, 3),        # pages longer than a stage, boxes of 32 rows
+    (2, 16, 4, 192, [900, 385], 128, 0),        # boxes of 64 rows, automatic split count
     (2, 8, 2, 200, [1500, 199], 64, 2),         # d = 64, pages longer than a stage, boxes of 8 rows
     (1, 8, 2, 16, [20000], 128, 1),             # one split: 157 stages through the ring
     (32, 32, 8, 16, [4096] * 30 + [1, 777], 128, 0),  # automatic split count (tensor-core path)
