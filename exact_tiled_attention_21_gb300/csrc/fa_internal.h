@@ -112,12 +112,13 @@ struct PagedDecodeLaunch {
     int B, Hq, Hkv, page, max_pages, num_pages, d, splits;
     float scale;
     DevError* err;
-    // tensor-core path only (d = 64 or 128, page a multiple of 8 that divides 128 or is a multiple of it,
-    // or the contiguous cache as one page of any length >= 128):
+    // tensor-core path only (d = 64 or 128, page a multiple of 8, or the contiguous cache as one page
+    // of Nk tokens, a multiple of 128); R = gcd(page, 128) rows per box:
     bool mma;
     CUtensorMap map_q;         // 3-D (d, B*Hq, 1), box (64, 16, 1), 128B swizzle
-    CUtensorMap map_k;         // 4-D (d, page, Hkv, num_pages), box (64, min(page,128), 1, 1), 128B swizzle
-    CUtensorMap map_v;         // d = 128: 5-D (64, page, 2, Hkv, num_pages), box (64, min(page,128), 2, 1, 1);
+    CUtensorMap map_k;         // 4-D (d, page, Hkv, num_pages), box (64, R, 1, 1), 128B swizzle; d = 128
+                               // with R = 8: map_v's 5-D form (both halves per box)
+    CUtensorMap map_v;         // d = 128: 5-D (64, page, 2, Hkv, num_pages), box (64, R, 2, 1, 1);
                                // d = 64: as map_k; 128B swizzle
     int num_sms;
     uint64_t timeout_ns;
