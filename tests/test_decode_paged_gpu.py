@@ -243,3 +243,16 @@ def test_paged_decode_repeats_bits(cuda_lib, P, d):
     torch.cuda.synchronize()
     assert fa.fa_get_last_device_error()[0] == 0
     assert bool(same)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_paged_decode_every_page_size_multiple_of_8(cuda_lib, d):
+    """Every page size 8, 16, ..., 256 (boxes of gcd(page, 128) = 8 ... 128 rows on the
+    tensor-core kernel), B=3, Hq=8, Hkv=2: a partial last page, a single token and a
+    length past two 128-key stages, against the oracle."""
+    for P in range(8, 264, 8):
+        lens = [3 * P + 5, 1, 300]
+        q, kp, vp, table, L = _case(500 + P + d, 3, 8, 2, P, lens, d)
+        o, lse = _run(cuda_lib, q, kp, vp, table, L, 3)
+        o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(d))
+        check_out(f64(o), f64(lse), o_ref, lse_ref, "page %d d%d" % (P, d))
