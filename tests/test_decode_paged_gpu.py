@@ -256,3 +256,15 @@ def test_paged_decode_every_page_size_multiple_of_8(cuda_lib, d):
         o, lse = _run(cuda_lib, q, kp, vp, table, L, 3)
         o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(d))
         check_out(f64(o), f64(lse), o_ref, lse_ref, "page %d d%d" % (P, d))
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_paged_decode_page_sizes_off_multiples_of_8(cuda_lib, d):
+    """Page sizes that are not multiples of 8 (the CUDA-core kernel): 1 ... 7, odd,
+    even, past a 128-key piece; B=3, Hq=8, Hkv=2, against the oracle."""
+    for P in (1, 2, 3, 5, 7, 9, 12, 20, 33, 100, 130, 250):
+        lens = [3 * P + 5, 1, 300]
+        q, kp, vp, table, L = _case(700 + P + d, 3, 8, 2, P, lens, d)
+        o, lse = _run(cuda_lib, q, kp, vp, table, L, 3)
+        o_ref, lse_ref = naive.decode_paged(f64(q), f64(kp), f64(vp), table, L, 1 / math.sqrt(d))
+        check_out(f64(o), f64(lse), o_ref, lse_ref, "page %d d%d" % (P, d))
