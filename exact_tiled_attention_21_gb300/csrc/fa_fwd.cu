@@ -711,7 +711,7 @@ template <int D, bool WIN, bool VL, bool SPLIT>
 cudaError_t launch_fwd_dw(const FwdLaunch& a, cudaStream_t s) {
     using C = Fwd<D>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
-    static_assert(!SPLIT || (!WIN && !VL), "split-KV tiles are built for the plain forward only");
+    static_assert(!SPLIT || !VL, "split-KV tiles are built for the plain and the window forward only");
     cudaError_t e = set_smem_limit_once<fwd_kernel<D, WIN, VL, SPLIT>>(C::SMEM);
     if (e != cudaSuccess) return e;
     FwdParams p;
@@ -780,7 +780,10 @@ int fwd_makespan(int BH, int Nq, int Nk, int causal, int rows, int hc, bool per_
 template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
     if (a.lens_q || a.lens_k) return launch_fwd_dw<D, false, true, false>(a, s);
-    if (a.window > 0) return launch_fwd_dw<D, true, false, false>(a, s);
+    // a window of at most one key block: split-KV tiles (each warpgroup takes every other block of a
+    // 128-row tile) halve the chain per tile, whose fixed costs dominate at 2-3 blocks per tile
+    if (a.window > 0)
+        return a.window <= 128 ? launch_fwd_dw<D, true, false, true>(a, s) : launch_fwd_dw<D, true, false, false>(a, s);
     return fwd_use_split(a) ? launch_fwd_dw<D, false, false, true>(a, s) : launch_fwd_dw<D, false, false, false>(a, s);
 }
 

@@ -20,6 +20,9 @@ CASES = [
     (1, 2, 2048, 2048, 128, 512),
     (1, 2, 300, 300, 128, 4096),    # wider than the sequence: plain causal
     (2, 3, 513, 513, 64, 130),
+    (1, 2, 1000, 1000, 128, 128),   # windows of at most 128 keys take split-KV tiles
+    (2, 2, 777, 1300, 128, 37),
+    (1, 3, 1100, 900, 64, 128),
 ]
 
 
