@@ -780,10 +780,11 @@ int fwd_makespan(int BH, int Nq, int Nk, int causal, int rows, int hc, bool per_
 template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
     if (a.lens_q || a.lens_k) return launch_fwd_dw<D, false, true, false>(a, s);
-    // a window of at most one key block: split-KV tiles (each warpgroup takes every other block of a
-    // 128-row tile) halve the chain per tile, whose fixed costs dominate at 2-3 blocks per tile
+    // a window of at most 129 keys (a 128-row tile then sees at most two key blocks when Nk - Nq is a
+    // multiple of 128): split-KV tiles (each warpgroup takes every other block of a 128-row tile) halve
+    // the chain per tile, whose fixed costs dominate at so few blocks per tile
     if (a.window > 0)
-        return a.window <= 128 ? launch_fwd_dw<D, true, false, true>(a, s) : launch_fwd_dw<D, true, false, false>(a, s);
+        return a.window <= 129 ? launch_fwd_dw<D, true, false, true>(a, s) : launch_fwd_dw<D, true, false, false>(a, s);
     return fwd_use_split(a) ? launch_fwd_dw<D, false, false, true>(a, s) : launch_fwd_dw<D, false, false, false>(a, s);
 }
 

@@ -23,6 +23,7 @@ CASES = [
     (1, 2, 1000, 1000, 128, 128),   # windows of at most 128 keys take split-KV tiles
     (2, 2, 777, 1300, 128, 37),
     (1, 3, 1100, 900, 64, 128),
+    (1, 2, 1024, 1024, 128, 129),   # the widest window that takes split-KV tiles
 ]
 
 
